@@ -1,0 +1,405 @@
+"""Pins for the CPU oracle: facts that hold independently of the oracle's code.
+
+Every ``pin_*`` function takes the loaded oracle library and raises
+AssertionError when the oracle disagrees with:
+  * a worked example printed by the pages (tests/golden/*.json, each citing
+    its page and figure / section),
+  * a hand-computed closed form,
+  * PyTorch's float64 ``scaled_dot_product_attention`` on the unpaged arrays
+    (a library routine, independent of the oracle's gather),
+  * IEEE decoding of every fp16 / bf16 bit pattern by PyTorch,
+  * invariants the pages state (paging changes storage, not the result).
+
+``tests/test_oracle_pins.py`` runs them against the real oracle and
+``tests/test_oracle_mutants.py`` runs them against copies of the oracle with
+one planted mistake each, checking that some pin fails for every mistake.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def golden(name: str) -> dict:
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        return json.load(f)
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def dense_reference(q, K, V, scale):
+    """Unpaged attention by PyTorch (float64).  q [Hq, D]; K, V [L, Hkv, D]."""
+    q64 = q.double()[None, :, None, :]                       # [1, Hq, 1, D]
+    k64 = K.double().permute(1, 0, 2)[None]                  # [1, Hkv, L, D]
+    v64 = V.double().permute(1, 0, 2)[None]
+    o = F.scaled_dot_product_attention(q64, k64, v64, scale=scale,
+                                       enable_gqa=q.shape[0] != K.shape[1])
+    return o[0, :, 0, :].numpy()                             # [Hq, D]
+
+
+def scatter_dense(K_list, V_list, tables, num_blocks, B, dtype, fill=float("nan")):
+    """Write each sequence's dense [L, Hkv, D] rows into a pool through its table."""
+    Hkv, D = K_list[0].shape[1], K_list[0].shape[2]
+    kc = torch.full((num_blocks, Hkv, B, D), fill, dtype=dtype)
+    vc = torch.full((num_blocks, Hkv, B, D), fill, dtype=dtype)
+    for K, V, tab in zip(K_list, V_list, tables):
+        for t in range(K.shape[0]):
+            kc[tab[t // B], :, t % B, :] = K[t]
+            vc[tab[t // B], :, t % B, :] = V[t]
+    return kc, vc
+
+
+def table_tensor(tables, width=None):
+    W = width or max(1, max(len(t) for t in tables))
+    bt = torch.full((len(tables), W), -1, dtype=torch.int32)
+    for s, t in enumerate(tables):
+        bt[s, :len(t)] = torch.tensor(t, dtype=torch.int32)
+    return bt
+
+
+def random_case(rng, S, Hq, Hkv, D, B, dtype, max_len, extra_blocks=3):
+    """Dense K/V per sequence plus a randomly permuted pool holding them."""
+    lens = [int(x) for x in rng.integers(1, max_len + 1, size=S)]
+    need = [math.ceil(L / B) for L in lens]
+    N = sum(need) + extra_blocks
+    perm = rng.permutation(N)
+    tables, pos = [], 0
+    for n in need:
+        tables.append([int(x) for x in perm[pos:pos + n]])
+        pos += n
+    g = torch.Generator().manual_seed(int(rng.integers(0, 2**31)))
+    K = [torch.randn(L, Hkv, D, generator=g).to(dtype) for L in lens]
+    V = [torch.randn(L, Hkv, D, generator=g).to(dtype) for L in lens]
+    q = torch.randn(S, Hq, D, generator=g).to(dtype)
+    kc, vc = scatter_dense(K, V, tables, N, B, dtype)
+    return dict(lens=lens, tables=tables, N=N, K=K, V=V, q=q, kc=kc, vc=vc)
+
+
+def run_oracle(lib, q, kc, vc, tables, lens, scale, Hkv, B, width=None):
+    return oracle.paged_attention(q, kc, vc, table_tensor(tables, width),
+                                  torch.tensor(lens, dtype=torch.int32), scale, Hkv, B, lib=lib)
+
+
+def selector_case(B, n_blocks, table, D=4, H=1):
+    """A pool whose V rows name their own (block, offset), for exact mapping checks."""
+    kc = torch.zeros(n_blocks, H, B, D, dtype=torch.float64).float()
+    vc = torch.zeros(n_blocks, H, B, D).float()
+    for b in range(n_blocks):
+        for o in range(B):
+            vc[b, :, o, 0] = b
+            vc[b, :, o, 1] = o
+            vc[b, :, o, 2] = 1.0
+    return kc, vc
+
+
+# ----------------------------------------------------------------------------- pins
+
+def pin_f16_decoder(lib):
+    """Every binary16 bit pattern decodes as PyTorch decodes it."""
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    ref = bits.view(torch.float16).double().numpy()
+    got = np.array([lib.orc_f16_to_f64(i) for i in range(65536)])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert np.array_equal(ref[~nan], got[~nan])
+    assert np.array_equal(np.signbit(ref[~nan]), np.signbit(got[~nan]))
+
+
+def pin_bf16_decoder(lib):
+    """Every bfloat16 bit pattern decodes as PyTorch decodes it."""
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    ref = bits.view(torch.bfloat16).double().numpy()
+    got = np.array([lib.orc_bf16_to_f64(i) for i in range(65536)])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert np.array_equal(ref[~nan], got[~nan])
+    assert np.array_equal(np.signbit(ref[~nan]), np.signbit(got[~nan]))
+
+
+def pin_hand_3token(lib):
+    """The hand-computed 1-head, 3-token case (tests/golden/hand_3token.json)."""
+    g = golden("hand_3token.json")
+    B, D, N = g["block_size"], g["head_dim"], g["num_blocks"]
+    kc = torch.full((N, 1, B, D), float("nan"), dtype=torch.float64).float()
+    vc = kc.clone()
+    for (blk, off), k, v in zip(g["placement"], g["k"], g["v"]):
+        kc[blk, 0, off] = torch.tensor(k)
+        vc[blk, 0, off] = torch.tensor(v)
+    q = torch.tensor([[g["q"]]], dtype=torch.float32)
+    out = run_oracle(lib, q, kc, vc, [g["block_table"]], [len(g["k"])], g["scale"], 1, B)
+    np.testing.assert_allclose(out[0, 0], g["expected"], rtol=1e-15, atol=0)
+
+
+def pin_single_token_is_v0(lib):
+    """L = 1: the only weight is 1, so o equals v_0 exactly (any q, any scale)."""
+    rng = np.random.default_rng(7)
+    for dtype in (torch.float32, torch.float16, torch.bfloat16):
+        c = random_case(rng, 1, 4, 2, 32, 16, dtype, max_len=1)
+        out = run_oracle(lib, c["q"], c["kc"], c["vc"], c["tables"], c["lens"], 0.3, 2, 16)
+        ref = c["V"][0][0].double().numpy()               # [Hkv, D]
+        assert np.array_equal(out[0], ref[[0, 0, 1, 1]])
+
+
+def pin_equal_keys_give_mean(lib):
+    """All keys equal (or q = 0): uniform weights, o = mean of the values."""
+    rng = np.random.default_rng(8)
+    c = random_case(rng, 2, 2, 2, 16, 4, torch.float32, max_len=11)
+    for s, L in enumerate(c["lens"]):
+        c["K"][s][:] = c["K"][s][0:1]                     # identical keys
+    kc, vc = scatter_dense(c["K"], c["V"], c["tables"], c["N"], 4, torch.float32)
+    out = run_oracle(lib, c["q"], kc, vc, c["tables"], c["lens"], 0.7, 2, 4)
+    for s in range(2):
+        np.testing.assert_allclose(out[s], c["V"][s].double().mean(0).numpy(), rtol=1e-13,
+                                   atol=1e-15)
+    q0 = torch.zeros_like(c["q"])
+    out0 = run_oracle(lib, q0, c["kc"], c["vc"], c["tables"], c["lens"], 0.7, 2, 4)
+    for s in range(2):
+        np.testing.assert_allclose(out0[s], c["V"][s].double().mean(0).numpy(), rtol=1e-13,
+                                   atol=1e-15)
+
+
+def pin_dense_equality(lib):
+    """Paging changes only where K/V live: the oracle equals PyTorch's float64 SDPA on
+    the unpaged arrays, for MHA and GQA, every dtype, several block sizes."""
+    rng = np.random.default_rng(9)
+    cases = [(3, 4, 4, 8, 1, torch.float32, 7), (3, 4, 2, 16, 2, torch.float16, 13),
+             (4, 8, 2, 32, 4, torch.bfloat16, 29), (3, 6, 3, 64, 16, torch.float32, 70),
+             (2, 8, 1, 128, 32, torch.bfloat16, 100)]
+    for S, Hq, Hkv, D, B, dtype, max_len in cases:
+        c = random_case(rng, S, Hq, Hkv, D, B, dtype, max_len)
+        scale = 1.0 / math.sqrt(D)
+        out = run_oracle(lib, c["q"], c["kc"], c["vc"], c["tables"], c["lens"], scale, Hkv, B)
+        for s in range(S):
+            ref = dense_reference(c["q"][s], c["K"][s], c["V"][s], scale)
+            np.testing.assert_allclose(out[s], ref, rtol=1e-12, atol=1e-13)
+
+
+def pin_scale_is_applied(lib):
+    """The scale multiplies q.k (checked against SDPA at a scale far from 1/sqrt(d))."""
+    rng = np.random.default_rng(10)
+    c = random_case(rng, 2, 2, 2, 8, 4, torch.float32, 9)
+    for scale in (0.05, 2.5):
+        out = run_oracle(lib, c["q"], c["kc"], c["vc"], c["tables"], c["lens"], scale, 2, 4)
+        for s in range(2):
+            ref = dense_reference(c["q"][s], c["K"][s], c["V"][s], scale)
+            np.testing.assert_allclose(out[s], ref, rtol=1e-12, atol=1e-13)
+
+
+def pin_permutation_invariance(lib):
+    """Any relabelling of physical blocks leaves the output bit-identical."""
+    rng = np.random.default_rng(11)
+    c = random_case(rng, 3, 4, 2, 32, 8, torch.bfloat16, 60, extra_blocks=5)
+    base = run_oracle(lib, c["q"], c["kc"], c["vc"], c["tables"], c["lens"], 0.2, 2, 8)
+    relabel = rng.permutation(c["N"])
+    tables2 = [[int(relabel[b]) for b in t] for t in c["tables"]]
+    kc2, vc2 = scatter_dense(c["K"], c["V"], tables2, c["N"], 8, torch.bfloat16)
+    out2 = run_oracle(lib, c["q"], kc2, vc2, tables2, c["lens"], 0.2, 2, 8)
+    assert np.array_equal(base, out2)
+
+
+def pin_shared_vs_copied_prefix(lib):
+    """Two sequences reading one shared prefix block set, or private copies of it,
+    give bit-identical outputs (block sharing, Figures 8 and 9)."""
+    rng = np.random.default_rng(12)
+    B, Hkv, D = 4, 2, 16
+    g = torch.Generator().manual_seed(5)
+    P, L = 10, 14                                      # prefix tokens, total tokens
+    prefix_k, prefix_v = torch.randn(P, Hkv, D, generator=g), torch.randn(P, Hkv, D, generator=g)
+    tails = [(torch.randn(L - P, Hkv, D, generator=g), torch.randn(L - P, Hkv, D, generator=g))
+             for _ in range(2)]
+    K = [torch.cat([prefix_k, t[0]]) for t in tails]
+    V = [torch.cat([prefix_v, t[1]]) for t in tails]
+    q = torch.randn(2, 2, D, generator=g)
+    # private copies: 4 blocks per sequence
+    priv = [[0, 1, 2, 3], [4, 5, 6, 7]]
+    kc1, vc1 = scatter_dense(K, V, priv, 12, B, torch.float32)
+    out1 = run_oracle(lib, q, kc1, vc1, priv, [L, L], 0.25, Hkv, B)
+    # shared: the first two (full) prefix blocks are shared; block 2 holds prefix
+    # tokens 8-9 plus private tokens, so it is per sequence.
+    shared = [[9, 10, 2, 3], [9, 10, 6, 7]]
+    kc2, vc2 = scatter_dense(K, V, shared, 12, B, torch.float32)
+    out2 = run_oracle(lib, q, kc2, vc2, shared, [L, L], 0.25, Hkv, B)
+    assert np.array_equal(out1, out2)
+    del rng
+
+
+def pin_brute_force_small(lib):
+    """Exhaustive small sweep, L in [1, 3B+1], B in {1, 2, 4}, against a direct loop that
+    reads the pool slot by slot (no gather into contiguous arrays)."""
+    rng = np.random.default_rng(13)
+    D, Hq, Hkv = 3, 2, 1
+    for B in (1, 2, 4):
+        for L in range(1, 3 * B + 2):
+            n = math.ceil(L / B)
+            N = n + 2
+            tab = [int(x) for x in rng.permutation(N)[:n]]
+            kc = torch.from_numpy(rng.standard_normal((N, Hkv, B, D))).float()
+            vc = torch.from_numpy(rng.standard_normal((N, Hkv, B, D))).float()
+            q = torch.from_numpy(rng.standard_normal((1, Hq, D))).float()
+            out = run_oracle(lib, q, kc, vc, [tab], [L], 0.9, Hkv, B)
+            kk, vv, qq = kc.double().numpy(), vc.double().numpy(), q.double().numpy()
+            for h in range(Hq):
+                w = []
+                for t in range(L):
+                    blk, off = tab[t // B], t % B
+                    w.append(math.exp(0.9 * sum(qq[0, h, d] * kk[blk, 0, off, d]
+                                                for d in range(D))))
+                tot = sum(w)
+                for d in range(D):
+                    ref = sum(w[t] * vv[tab[t // B], 0, t % B, d] for t in range(L)) / tot
+                    assert abs(out[0, h, d] - ref) <= 1e-12 * max(1.0, abs(ref))
+
+
+def pin_p3_mapping_table(lib):
+    """Zero-based table (iaim.asia, section KV Cache 如何按块分配): token t of logical
+    block j is read from block_table[j].  A one-hot key selects token t; the output
+    must be the V row that the golden table places it in."""
+    g = golden("p3_mapping.json")
+    B = g["block_size"]
+    table = [5, 0, 3]
+    N = 6
+    D = 4
+    kc, vc = selector_case(B, N, table, D=D)
+    for row in g["rows"]:
+        for t in (row["first_token"], (row["first_token"] + row["last_token"]) // 2,
+                  row["last_token"]):
+            kc2 = torch.zeros_like(kc)
+            blk = table[row["table_entry"]]
+            off = t - row["first_token"]
+            kc2[blk, 0, off, 3] = 1.0                      # only token t matches q
+            q = torch.tensor([[[0.0, 0.0, 0.0, 2000.0]]])
+            out = run_oracle(lib, q, kc2, vc, [table], [48], 1.0, 1, B)
+            assert out[0, 0, 0] == blk and out[0, 0, 1] == off, (t, out[0, 0])
+
+
+def pin_fig6_decode_walkthrough(lib):
+    """Figure 6: prefill into blocks [7, 1], decode 1 fills block 1 slot 3, decode 2
+    writes block 3 slot 0; attention over the grown table equals dense attention."""
+    g = golden("fig6_block_table.json")
+    B, D, Hkv = g["block_size"], 8, 2
+    N = 8
+    gen = torch.Generator().manual_seed(21)
+    toks_k = torch.randn(9, Hkv, D, generator=gen)
+    toks_v = torch.randn(9, Hkv, D, generator=gen)
+    kc = torch.full((N, Hkv, B, D), float("nan"))
+    vc = kc.clone()
+    pre = g["prefill"]["placement"]
+    slots = torch.tensor([b * B + o for b, o in pre], dtype=torch.int64)
+    oracle.reshape_and_cache(toks_k[:7], toks_v[:7], kc, vc, slots, B, lib=lib)
+    for i, (b, o) in enumerate(pre):
+        assert torch.equal(kc[b, :, o], toks_k[i]) and torch.equal(vc[b, :, o], toks_v[i])
+    filled = [int((~torch.isnan(kc[b, 0, :, 0])).sum()) for b in g["prefill"]["block_table"]]
+    assert filled == g["prefill"]["filled"]
+    q = torch.randn(1, 4, D, generator=gen)
+    for step in ("decode1", "decode2"):
+        st = g[step]
+        t = st["token"]
+        oracle.reshape_and_cache(toks_k[t:t + 1], toks_v[t:t + 1], kc, vc,
+                                 torch.tensor([st["block"] * B + st["offset"]]), B, lib=lib)
+        assert torch.equal(kc[st["block"], :, st["offset"]], toks_k[t])
+        filled = [int((~torch.isnan(kc[b, 0, :, 0])).sum()) for b in st["block_table"]]
+        assert filled == st["filled"]
+        out = run_oracle(lib, q, kc, vc, [st["block_table"]], [t + 1], 0.3, Hkv, B)
+        ref = dense_reference(q[0], toks_k[:t + 1], toks_v[:t + 1], 0.3)
+        np.testing.assert_allclose(out[0], ref, rtol=1e-12, atol=1e-13)
+
+
+def pin_p5_block_table(lib):
+    """p5 section 2.3: 7 tokens, block_size 4, table [3, 7] (one slot left)."""
+    g = golden("p5_block_table.json")
+    B, D = g["block_size"], 4
+    gen = torch.Generator().manual_seed(22)
+    k = torch.randn(g["tokens"], 1, D, generator=gen)
+    v = torch.randn(g["tokens"], 1, D, generator=gen)
+    kc = torch.full((8, 1, B, D), float("nan"))
+    vc = kc.clone()
+    slots = torch.tensor([b * B + o for b, o in g["placement"]], dtype=torch.int64)
+    oracle.reshape_and_cache(k, v, kc, vc, slots, B, lib=lib)
+    last = g["block_table"][-1]
+    assert int(torch.isnan(kc[last, 0, :, 0]).sum()) == g["free_slots_in_last_block"]
+    q = torch.randn(1, 1, D, generator=gen)
+    out = run_oracle(lib, q, kc, vc, [g["block_table"]], [g["tokens"]], 0.5, 1, B)
+    np.testing.assert_allclose(out[0], dense_reference(q[0], k, v, 0.5), rtol=1e-12, atol=1e-13)
+
+
+def pin_fig8_copy_on_write(lib):
+    """Figure 8: copy block 1 -> 3, A1 writes into 3, A2 into 1; the prompt part of
+    both is unchanged and each sample's attention equals its own dense attention."""
+    g = golden("fig8_cow.json")
+    B, D, Hkv, N = g["block_size"], 8, 2, 8
+    gen = torch.Generator().manual_seed(23)
+    pk, pv = torch.randn(7, Hkv, D, generator=gen), torch.randn(7, Hkv, D, generator=gen)
+    kc = torch.full((N, Hkv, B, D), float("nan"))
+    vc = kc.clone()
+    shared = g["shared_table"]
+    slots = torch.tensor([shared[t // B] * B + t % B for t in range(7)])
+    oracle.reshape_and_cache(pk, pv, kc, vc, slots, B, lib=lib)
+    before7 = kc[7].clone()
+    oracle.copy_blocks([kc, vc], [[g["copy"]["src"], g["copy"]["dst"]]], lib=lib)
+    src, dst = g["copy"]["src"], g["copy"]["dst"]
+    assert torch.equal(kc[dst].view(torch.int32), kc[src].view(torch.int32))
+    assert torch.equal(vc[dst].view(torch.int32), vc[src].view(torch.int32))
+    assert torch.equal(kc[7].view(torch.int32), before7.view(torch.int32))
+    pos = g["write_position"]
+    a1k, a1v = torch.randn(1, Hkv, D, generator=gen), torch.randn(1, Hkv, D, generator=gen)
+    a2k, a2v = torch.randn(1, Hkv, D, generator=gen), torch.randn(1, Hkv, D, generator=gen)
+    t1, t2 = g["a1_table_after"], g["a2_table_after"]
+    oracle.reshape_and_cache(a1k, a1v, kc, vc, torch.tensor([t1[pos // B] * B + pos % B]), B,
+                             lib=lib)
+    oracle.reshape_and_cache(a2k, a2v, kc, vc, torch.tensor([t2[pos // B] * B + pos % B]), B,
+                             lib=lib)
+    q = torch.randn(2, 2, D, generator=gen)
+    out = run_oracle(lib, q, kc, vc, [t1, t2], [pos + 1, pos + 1], 0.35, Hkv, B)
+    np.testing.assert_allclose(out[0], dense_reference(q[0], torch.cat([pk, a1k]),
+                                                       torch.cat([pv, a1v]), 0.35),
+                               rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(out[1], dense_reference(q[1], torch.cat([pk, a2k]),
+                                                       torch.cat([pv, a2v]), 0.35),
+                               rtol=1e-12, atol=1e-13)
+
+
+def pin_copy_blocks_reads_pre_copy_state(lib):
+    """Copies read the state before the call: with pairs (a->b, b->c), c receives the
+    old content of b, not a's."""
+    pool = torch.arange(5 * 6, dtype=torch.float32).reshape(5, 6)
+    old = pool.clone()
+    oracle.copy_blocks([pool], [[0, 1], [1, 2]], lib=lib)
+    assert torch.equal(pool[1], old[0]) and torch.equal(pool[2], old[1])
+    assert torch.equal(pool[[0, 3, 4]], old[[0, 3, 4]])
+
+
+def pin_reshape_bytes(lib):
+    """reshape_and_cache is a byte copy: NaN payloads, -0.0 and untouched bytes survive,
+    negative slots are skipped, each head's row lands at [slot/B][h][slot%B]."""
+    B, Hkv, D, N = 4, 3, 8, 5
+    gen = torch.Generator().manual_seed(24)
+    for dtype in (torch.float32, torch.float16, torch.bfloat16):
+        kc = torch.randn(N, Hkv, B, D, generator=gen).to(dtype)
+        vc = torch.randn(N, Hkv, B, D, generator=gen).to(dtype)
+        k = torch.randn(3, Hkv, D, generator=gen).to(dtype)
+        v = torch.randn(3, Hkv, D, generator=gen).to(dtype)
+        ib = torch.int32 if dtype == torch.float32 else torch.int16
+        k.view(ib)[0, 0, 0] = -1              # a NaN with a payload
+        k[0, 0, 1] = -0.0
+        k0, v0 = kc.clone(), vc.clone()
+        slots = torch.tensor([13, -1, 6])
+        oracle.reshape_and_cache(k, v, kc, vc, slots, B, lib=lib)
+        exp_k, exp_v = k0.clone(), v0.clone()
+        exp_k[3, :, 1] = k[0]
+        exp_v[3, :, 1] = v[0]
+        exp_k[1, :, 2] = k[2]
+        exp_v[1, :, 2] = v[2]
+        assert torch.equal(kc.view(ib), exp_k.view(ib))
+        assert torch.equal(vc.view(ib), exp_v.view(ib))
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
