@@ -1,0 +1,451 @@
+#!/usr/bin/env python3
+"""Benchmark of one paged decode step on GB300.
+
+A step is the whole hot path over one batch: pa_reshape_and_cache of the new
+tokens' K/V (plus pa_copy_blocks where the workload has copy-on-write pairs),
+then pa_decode (and its merge pass when the call splits contexts).
+
+Default workload: the LLaMA-13B-shaped batched decode (256 sequences, 40 query
+/ 40 kv heads, head_dim 128, bf16, block_size 16, lognormal context lengths with
+median 400 clipped to [16, 2048], 256 new tokens per step).  Its KV pool is
+about 3 GB, far larger than the 129 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle instead,
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+WORKLOADS = {
+    "llama13b": "LLaMA-13B-shaped batched decode: 256 seqs, 40 q / 40 kv heads, head_dim 128, "
+                "bf16, block_size 16, context lognormal(median 400, sigma 0.8) in [16, 2048], "
+                "N(0, 0.5), reshape_and_cache of 256 new tokens per step",
+    "opt13b": "OPT-13B-shaped decode layer: 64 seqs, 40 q / 40 kv heads, head_dim 128, fp16, "
+              "block_size 16, context uniform in [1, 2048], N(0, 1)",
+    "long16": "long-context split decode: 8 seqs x 32768 tokens, 64 q / 8 kv heads, head_dim 128, "
+              "bf16, block_size 16, 512-token partitions + reduce",
+    "long32": "long-context split decode: 8 seqs x 32768 tokens, 64 q / 8 kv heads, head_dim 128, "
+              "bf16, block_size 32, 512-token partitions + reduce",
+    "prefix": "shared-prefix decode: 16 groups x 8 seqs, 32 q / 8 kv heads, head_dim 128, bf16, "
+              "block_size 16, 1024-token shared prefix, CoW tail copies each step",
+}
+DTYPE_NAME = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}
+METRIC = "paged decode attention KV GB/s"
+KERNEL_SRC = os.path.join(ROOT, "paged_kv_cache_119_gb300", "csrc", "decode_kernel.cuh")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=sorted(WORKLOADS), default="llama13b")
+    ap.add_argument("--partition-size", type=int, default=None,
+                    help="pa_decode partition_size (default: the workload's)")
+    ap.add_argument("--flush-l2", action="store_true",
+                    help="write a 512 MB buffer between timed steps (outside the events)")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------------------ helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def aggregate(per_rank_seconds, per_rank_units):
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    t = max(per_rank_seconds)
+    return sum(per_rank_units) / t, t
+
+
+def max_over_ranks(seconds: float, device) -> float:
+    """The slowest rank's time (an all-reduce MAX over the default process group)."""
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("decode_kernel.cuh", "pa_device.cuh", "pa_internal.h"):
+        with open(os.path.join(ROOT, "paged_kv_cache_119_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config: str):
+    """ncu DRAM bytes per decode launch, if recorded for the current kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(config)
+    if not ent or ent.get("kernel_hash") != kernel_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def algorithmic_bytes(w) -> dict:
+    """Bytes a decode step must move at minimum (each cached K/V byte read once)."""
+    esz = torch.tensor([], dtype=w.dtype).element_size()
+    lens = w.context_lens.tolist()
+    kv = w.kv_bytes()
+    qo = 2 * w.num_seqs * w.num_q_heads * w.head_dim * esz
+    tables = 4 * sum(math.ceil(L / w.block_size) for L in lens) + 4 * w.num_seqs
+    T = w.slot_mapping.numel()
+    reshape = 2 * 2 * T * w.num_kv_heads * w.head_dim * esz + 8 * T
+    copies = 0
+    if w.copy_pairs is not None:
+        copies = 2 * 2 * len(w.copy_pairs) * w.num_kv_heads * w.block_size * w.head_dim * esz
+    return {"kv": kv, "decode": kv + qo + tables, "reshape": reshape, "copy": copies,
+            "step": kv + qo + tables + reshape + copies}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self, t0_wall: float, t1_wall: float) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for r in csv.reader(io.StringIO(out)):
+            if len(r) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(r[0].strip().split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + r[0].strip().split(".")[1]) if "." in r[0] else 0.0
+                rows.append((ts, float(r[1]), float(r[2]), r[4].strip(),
+                             [x.strip() for x in r[5:9]]))
+            except (ValueError, IndexError):
+                continue
+        inside = [x for x in rows if t0_wall - 0.05 <= x[0] <= t1_wall + 0.05]
+        use = inside or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = sorted(x[1] for x in use)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for x in use for i, v in enumerate(x[4]) if v == "Active"})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(x[2] for x in use),
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+def make_workload(config: str, device):
+    from paged_kv_cache_119_gb300 import workloads
+    return workloads.make(config, device=device)
+
+
+# ------------------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, local):
+    import paged_kv_cache_119_gb300 as pa
+    from paged_kv_cache_119_gb300 import build as pa_build
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pa_build.build()
+    w = make_workload(args.config, dev)
+    part = w.partition_size if args.partition_size is None else args.partition_size
+    nbytes = algorithmic_bytes(w)
+    out = torch.empty(w.num_seqs, w.num_q_heads, w.head_dim, dtype=w.dtype, device=dev)
+    ws_bytes = pa.pa_decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.head_dim,
+                                            w.max_context_len, w.block_size, max(part, 0)) \
+        if part >= 0 else 0
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if args.flush_l2 else None
+    cow_src = None
+    if w.copy_pairs is not None:
+        # the CoW copy reads the original tails and writes scratch destinations each step,
+        # so the decoded state stays the same from step to step
+        pa.pa_copy_blocks([w.k_cache], [w.v_cache], w.copy_pairs)
+        cow_src = w.copy_pairs.copy()
+
+    def step(e=None):
+        if cow_src is not None:
+            pa.pa_copy_blocks([w.k_cache], [w.v_cache], cow_src)
+        if e is not None:
+            e[0].record()
+        pa.pa_reshape_and_cache(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping)
+        if e is not None:
+            e[1].record()
+        pa.pa_decode(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale,
+                     w.num_kv_heads, w.block_size, max_context_len=w.max_context_len,
+                     partition_size=part, workspace=ws)
+        if e is not None:
+            e[2].record()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if pa.pa_get_device_error():
+        raise RuntimeError("device error word set during warm-up")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    begin, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0_wall = time.time()
+    if flush is None:
+        begin.record()
+        for i in range(args.steps):
+            step(ev[i])
+        end.record()
+        torch.cuda.synchronize()
+        total_ms = begin.elapsed_time(end)
+    else:
+        total_ms = 0.0
+        for i in range(args.steps):
+            flush.fill_(i & 0xff)
+            begin.record()
+            step(ev[i])
+            end.record()
+            torch.cuda.synchronize()
+            total_ms += begin.elapsed_time(end)
+    if world > 1:
+        torch.distributed.barrier()
+    t1_wall = time.time()
+    clocks = sampler.stop(t0_wall, t1_wall) if rank == 0 else None
+    torch.cuda.synchronize()
+    reshape_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    decode_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    if pa.pa_get_device_error():
+        raise RuntimeError("device error word set during the timed steps")
+
+    sec = max_over_ranks(total_ms / 1e3, dev) if world > 1 else total_ms / 1e3
+    value, _ = aggregate([sec], [nbytes["kv"] * args.steps * world])
+    value /= 1e9
+
+    e2e = None if args.no_e2e else measure_e2e(args, pa, w, out, ws, part, dev)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return None
+    peak, peak_kind = load_peaks()
+    achieved = nbytes["decode"] / (decode_ms / 1e3) / 1e9
+    split = part > 0 and w.max_context_len > part
+    launches_per_step = 2 + (1 if split else 0) + (1 if cow_src is not None else 0)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[w.dtype],
+        "data": "synthetic",
+        "config": {"workload": WORKLOADS[args.config], "name": args.config,
+                   "num_seqs": w.num_seqs, "kv_bytes_per_step": nbytes["kv"],
+                   "partition_size": part,
+                   "l2": ("flushed between steps (512 MB write outside the events)"
+                          if flush is not None else
+                          f"no flush: KV pool {2 * w.k_cache.numel() * w.k_cache.element_size() / 1e9:.2f} GB "
+                          "is larger than the 129 MB L2"),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "us_per_step": round(total_ms / args.steps * 1e3, 2),
+        "decode_us": round(decode_ms * 1e3, 2), "reshape_us": round(reshape_ms * 1e3, 2),
+        "decode_kv_gbs": round(nbytes["kv"] / (decode_ms / 1e3) / 1e9, 1),
+        "pct_of_hbm_peak": round(100 * achieved / peak, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic(args.config),
+                     "kernel": "decode_kernel" + (" + reduce_kernel" if split else ""),
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": nbytes["decode"]},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
+    return line
+
+
+def measure_e2e(args, pa, w, out, ws, part, dev):
+    """Same step through the public API with per-step inputs in pinned host memory:
+    H2D of q, new K/V, slots, block tables and context lengths, the kernels, and a
+    D2H read of the output, all inside the timed region."""
+    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+    host = {n: getattr(w, n).cpu().pin_memory() for n in names}
+    devb = {n: torch.empty_like(getattr(w, n)) for n in names}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def step():
+        for n in names:
+            devb[n].copy_(host[n], non_blocking=True)
+        pa.pa_reshape_and_cache(devb["k_new"], devb["v_new"], w.k_cache, w.v_cache,
+                                devb["slot_mapping"])
+        pa.pa_decode(out, devb["q"], w.k_cache, w.v_cache, devb["block_tables"],
+                     devb["context_lens"], w.scale, w.num_kv_heads, w.block_size,
+                     max_context_len=w.max_context_len, partition_size=part, workspace=ws)
+        out_host.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b.record()
+    for _ in range(args.steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = b.elapsed_time(e) / args.steps
+    return {"value": round(w.kv_bytes() / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------------------------ oracle arms
+
+def _host_inputs(w):
+    return {n: getattr(w, n).cpu() for n in ("q", "k_cache", "v_cache", "k_new", "v_new",
+                                             "slot_mapping", "block_tables", "context_lens")}
+
+
+def _oracle_step(h, w, seqs, threads):
+    """The oracle's step on sequences [0, seqs): reshape of their new tokens, then decode."""
+    import oracle
+    nt = sum(1 for (s, _) in w.meta["new_tokens"] if s < seqs)
+    oracle.reshape_and_cache(h["k_new"][:nt], h["v_new"][:nt], h["k_cache"], h["v_cache"],
+                             h["slot_mapping"][:nt], w.block_size)
+    oracle.paged_attention(h["q"][:seqs], h["k_cache"], h["v_cache"], h["block_tables"][:seqs],
+                           h["context_lens"][:seqs], w.scale, w.num_kv_heads, w.block_size,
+                           num_threads=threads)
+
+
+def _sample_bytes(w, seqs):
+    esz = torch.tensor([], dtype=w.dtype).element_size()
+    return int(sum(w.context_lens.tolist()[:seqs])) * w.num_kv_heads * 2 * w.head_dim * esz
+
+
+def cpu_baseline(w, budget_s: float) -> dict:
+    """The oracle, as it stands, on the first sequences of the same workload, growing the
+    sample until about budget_s seconds of CPU work."""
+    import oracle
+    h = _host_inputs(w)
+    threads = oracle.max_threads()
+    seqs, elapsed = 0, 0.0
+    chunk = 8
+    t_all = time.perf_counter()
+    while seqs < w.num_seqs and elapsed < budget_s:
+        n = min(chunk, w.num_seqs - seqs)
+        sub = {k: v for k, v in h.items()}
+        sub["q"] = h["q"][seqs:seqs + n]
+        sub["block_tables"] = h["block_tables"][seqs:seqs + n]
+        sub["context_lens"] = h["context_lens"][seqs:seqs + n]
+        t = time.perf_counter()
+        oracle.paged_attention(sub["q"], h["k_cache"], h["v_cache"], sub["block_tables"],
+                               sub["context_lens"], w.scale, w.num_kv_heads, w.block_size,
+                               num_threads=threads)
+        elapsed += time.perf_counter() - t
+        seqs += n
+    del t_all
+    gbs = _sample_bytes(w, seqs) / elapsed / 1e9
+    return {"value": round(gbs, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"fp64 C oracle (OpenMP, {threads} threads) over the first {seqs} of "
+                      f"{w.num_seqs} sequences, all heads: {elapsed:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    w = make_workload(args.config, "cpu")
+    h = _host_inputs(w)
+    threads = oracle.max_threads()
+    # a bounded sample: enough sequences for ~0.5 s of oracle work per step
+    seqs = max(1, min(w.num_seqs, 16))
+    for _ in range(args.warmup):
+        _oracle_step(h, w, seqs, threads)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(h, w, seqs, threads)
+    sec = (time.perf_counter() - t) / args.steps
+    value = _sample_bytes(w, seqs) / sec / 1e9
+    sample = (f"fp64 C oracle (OpenMP, {threads} threads): reshape + decode of the first {seqs} "
+              f"of {w.num_seqs} sequences per step")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOADS[args.config], "name": args.config,
+                       "num_seqs": w.num_seqs, "sampled_seqs": seqs},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.gpus != world and world > 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    line = run_reference(args, rank, world) if args.impl == "reference" else \
+        run_ours(args, rank, world, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

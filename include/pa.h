@@ -1,0 +1,166 @@
+/*
+ * pa.h -- C ABI of the paged decode attention library (libpa.so), GB300 / sm_103a.
+ *
+ * Three operations over a paged KV cache, each a hand-written CUDA kernel:
+ *
+ *   pa_reshape_and_cache  write each new token's K/V rows into the cache slots
+ *                         named by slot_mapping ("PagedAttention 完全拆解",
+ *                         section 原理详解（三）：kernel 实现, item 1: fused reshape
+ *                         and block write; Figure 6 decode steps).
+ *   pa_decode             one query per sequence attends over its context through
+ *                         its block table (same page, section 原理详解（二）：块式注意
+ *                         力的数学, block-wise attention equation; section 原理详解
+ *                         （三） item 2: fused block read and attention), with a
+ *                         split-context second pass for long contexts
+ *                         (iaim.asia/ai-infra/182, section vLLM 内核里的缓解写法:
+ *                         segments merged by a reduce).
+ *   pa_copy_blocks        copy whole blocks src -> dst for copy-on-write (first page,
+ *                         section 原理详解（三） item 3: fused block copy; section
+ *                         内存共享, Figure 8).
+ *
+ * Layout (the pages leave the in-block layout to the backend; iaim.asia page,
+ * section KV Cache 如何按块分配).  All tensors are dense, row-major, in device
+ * memory, and owned by the caller:
+ *
+ *   k_cache, v_cache  [num_blocks][num_kv_heads][block_size][head_dim]   dtype T
+ *   q, out            [num_seqs][num_q_heads][head_dim]   (out may be fp32)
+ *   block_tables      [num_seqs][block_table_stride]      int32 physical block ids;
+ *                     token t of sequence s lives in block block_tables[s][t / B]
+ *                     at slot t % B
+ *   context_lens      [num_seqs]                           int32, current token included
+ *   new k, v          [num_tokens][num_kv_heads][head_dim] dtype T
+ *   slot_mapping      [num_tokens]                         int64, slot = block * B + offset;
+ *                                                          slot < 0 skips the token
+ *   query head h reads kv head h / (num_q_heads / num_kv_heads).
+ *
+ * Conventions:
+ *   - Every call is asynchronous on the given stream (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream).  The library never synchronises,
+ *     never allocates device memory and keeps no state except a per-device SM
+ *     count and a per-device error word (see pa_get_device_error).
+ *   - Host-side validation runs before any launch.  A failed check returns a
+ *     negative pa_status and launches nothing.  A failed launch returns
+ *     PA_ERR_CUDA.
+ *   - Device-side checks (always on, one compare per block): a block id outside
+ *     [0, num_blocks), a slot outside the pool, or a context length that is
+ *     negative or exceeds max_context_len sets a bit in the device error word,
+ *     skips the access and, for pa_decode, writes NaN to the affected outputs.
+ *     Kernels never trap.
+ *   - A context length of 0 yields an all-zero output row.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID = -1,      /* a pointer, size, alignment or value is out of range */
+    PA_ERR_UNSUPPORTED = -2,  /* head_dim / block_size / dtype combination not built */
+    PA_ERR_WORKSPACE = -3,    /* split-context workspace missing or too small */
+    PA_ERR_CUDA = -4          /* a CUDA runtime call or kernel launch failed */
+} pa_status;
+
+/* Bits of the device error word. */
+#define PA_DEVERR_BLOCK_ID    0x1u  /* block table entry outside [0, num_blocks) */
+#define PA_DEVERR_CONTEXT_LEN 0x2u  /* context_len < 0 or > max_context_len */
+#define PA_DEVERR_SLOT        0x4u  /* slot_mapping entry >= num_blocks * block_size */
+#define PA_DEVERR_TIMEOUT     0x8u  /* a bounded pipeline wait gave up */
+
+/*
+ * Bytes of device workspace pa_decode needs when it splits contexts into
+ * partitions of partition_size tokens (0 = the automatic choice, which never
+ * needs more than this; < 0 = never split, returns 0).  The workspace holds,
+ * per (sequence, query head, partition), one fp32 partial output row of head_dim
+ * values plus its running max and sum.  Pure host arithmetic; no CUDA call.
+ * Returns 0 for invalid sizes.
+ */
+size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                 int32_t max_context_len, int32_t block_size,
+                                 int32_t partition_size);
+
+/*
+ * Paged decode attention: for every sequence s and query head h,
+ *   out[s][h][:] = sum_t a_t v_t,  a_t = exp(scale q.k_t) / sum_u exp(scale q.k_u),
+ * over the context_lens[s] tokens reached through block_tables[s].
+ *
+ *   out               device, [S][Hq][D] of out_dtype (PA_F32 or kv_dtype)
+ *   q                 device, [S][Hq][D] of kv_dtype
+ *   k_cache, v_cache  device, 16-byte aligned, [num_blocks][Hkv][B][D] of kv_dtype
+ *   block_tables      device, [S][block_table_stride] int32
+ *   context_lens      device, [S] int32
+ *   max_context_len   host upper bound on every context_lens[s]; sizes the grid
+ *                     (no device-to-host read happens).  Must be <=
+ *                     block_table_stride * block_size.
+ *   head_dim          64 or 128; block_size 16 or 32; num_q_heads a multiple of
+ *                     num_kv_heads.  kv_dtype PA_F32, PA_F16 or PA_BF16.
+ *   scale             multiplies q.k (1/sqrt(head_dim) in the usual case)
+ *   partition_size    0 = automatic; < 0 = one pass per (sequence, kv head);
+ *                     > 0 = split each context into partitions of this many tokens
+ *                     (a multiple of block_size) and merge them in a second kernel.
+ *   workspace         device buffer of workspace_bytes, only used (and only
+ *                     required) when the call splits; see pa_decode_workspace_bytes.
+ *   stream            cudaStream_t (as void*).
+ * out must not overlap q, the caches or the workspace.
+ */
+int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
+              const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
+              const int32_t* block_tables, int64_t block_table_stride,
+              const int32_t* context_lens, int32_t max_context_len, int32_t num_seqs,
+              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+              float scale, int32_t partition_size, void* workspace, size_t workspace_bytes,
+              void* stream);
+
+/*
+ * Cache write: for each token i < num_tokens with slot = slot_mapping[i] >= 0 and
+ * each kv head h, k_cache[slot / B][h][slot % B][:] = k[i][h][:] and likewise for v.
+ * A bit-exact copy.  k, v, k_cache, v_cache: device, 16-byte aligned;
+ * slot_mapping: device int64.  Two tokens naming the same slot is a caller error
+ * (which one lands is unspecified).  Slots >= num_blocks * B are skipped and flag
+ * PA_DEVERR_SLOT.
+ */
+int pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                         const int64_t* slot_mapping, int64_t num_tokens, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                         pa_dtype dtype, void* stream);
+
+/*
+ * Block copy for copy-on-write: for every layer l < num_layers and every pair p,
+ * the whole block src = pairs[2p] of k_caches[l] and of v_caches[l] is copied to
+ * block dst = pairs[2p+1] (block_bytes bytes each; every block of every pool).
+ *   k_caches, v_caches  HOST arrays of num_layers DEVICE pointers (16-byte aligned)
+ *   src_dst_pairs_host  HOST array of 2 * num_pairs int64 block ids
+ *   block_bytes         bytes of one block (a multiple of 16)
+ * Validation (host): ids in [0, num_blocks), destinations pairwise distinct, and
+ * no destination is also a source -- so the result equals copying from the
+ * pre-copy state.  The pairs travel as kernel parameters; one launch per chunk of
+ * pairs and layers, nothing is allocated.
+ */
+int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
+                   const int64_t* src_dst_pairs_host, int64_t num_pairs, int64_t block_bytes,
+                   int64_t num_blocks, void* stream);
+
+/*
+ * Reads and clears the calling device's error word (PA_DEVERR_* bits).
+ * Synchronises with `stream` to do so.  flags: host pointer.
+ */
+int pa_get_device_error(uint32_t* flags, void* stream);
+
+/* Human-readable name of a pa_status value.  Never NULL. */
+const char* pa_status_string(int status);
+
+/* Library version string, e.g. "paged_kv_cache_119_gb300 0.1 sm_103a". */
+const char* pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,162 @@
+"""Python binding of libpa.so: argument marshalling only.
+
+Each function takes PyTorch tensors (device memory owned by the caller), checks
+shapes/dtypes/devices, and calls the C ABI function of the same name on the
+current CUDA stream.  Every step of the computation runs in the library's CUDA
+kernels; there is no PyTorch or CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _native as N
+
+_DT = {torch.float32: N.PA_F32, torch.float16: N.PA_F16, torch.bfloat16: N.PA_BF16}
+
+
+def _dtype(t: torch.Tensor) -> int:
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}; expected float32, float16 or bfloat16")
+
+
+def _cuda(name: str, t: torch.Tensor) -> None:
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def pa_decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int,
+                              max_context_len: int, block_size: int,
+                              partition_size: int = 0) -> int:
+    """Workspace bytes pa_decode needs for a split call (0 when it never splits)."""
+    return int(N.load().pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim,
+                                                  max_context_len, block_size, partition_size))
+
+
+def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+              block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+              num_kv_heads: int, block_size: int, max_context_len: int | None = None,
+              partition_size: int = 0, workspace: torch.Tensor | None = None,
+              stream=None) -> torch.Tensor:
+    """Paged decode attention: out[s, h] = softmax(scale q[s, h] . K_s^T) V_s, where
+    K_s, V_s are sequence s's first context_lens[s] tokens reached through
+    block_tables[s].
+
+    out [S, Hq, D] (float32 or q's dtype), q [S, Hq, D], k_cache / v_cache
+    [N, Hkv, B, D], block_tables [S, W] int32, context_lens [S] int32.
+    max_context_len defaults to W * block_size (an upper bound needing no
+    device-to-host read).  A workspace is allocated with torch if the call
+    splits and none is given.
+    """
+    for name, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                    ("block_tables", block_tables), ("context_lens", context_lens)):
+        _cuda(name, t)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    if q.dim() != 3 or out.shape != q.shape:
+        raise ValueError(f"q and out must be [S, Hq, D] of one shape, got {tuple(q.shape)}, "
+                         f"{tuple(out.shape)}")
+    S, Hq, D = q.shape
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape or \
+            tuple(k_cache.shape[1:]) != (num_kv_heads, block_size, D):
+        raise ValueError(f"k_cache/v_cache must be [N, {num_kv_heads}, {block_size}, {D}], "
+                         f"got {tuple(k_cache.shape)}, {tuple(v_cache.shape)}")
+    if k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise TypeError("q, k_cache and v_cache must share a dtype")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [S, W] and context_lens [S]")
+    W = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = W * block_size
+    ws_need = pa_decode_workspace_bytes(S, Hq, D, max_context_len, block_size,
+                                        max(partition_size, 0)) if partition_size >= 0 else 0
+    if ws_need and workspace is None:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
+    ws_ptr, ws_bytes = (0, 0) if workspace is None else (workspace.data_ptr(),
+                                                         workspace.numel() *
+                                                         workspace.element_size())
+    status = N.load().pa_decode(out.data_ptr(), _dtype(out), q.data_ptr(), k_cache.data_ptr(),
+                                v_cache.data_ptr(), _dtype(q), k_cache.shape[0],
+                                block_tables.data_ptr(), block_tables.stride(0),
+                                context_lens.data_ptr(), int(max_context_len), S, Hq,
+                                num_kv_heads, D, block_size, float(scale), int(partition_size),
+                                ws_ptr, ws_bytes, _stream(stream))
+    N.check("pa_decode", status)
+    return out
+
+
+def pa_reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
+                         v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                         stream=None) -> None:
+    """Write k[i], v[i] ([T, Hkv, D]) into the cache slot slot_mapping[i] (int64;
+    negative = skip), bit for bit.  Caches are [N, Hkv, B, D]."""
+    for name, t in (("k", k), ("v", v), ("k_cache", k_cache), ("v_cache", v_cache),
+                    ("slot_mapping", slot_mapping)):
+        _cuda(name, t)
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    if k.dim() != 3 or v.shape != k.shape or k_cache.dim() != 4 or \
+            v_cache.shape != k_cache.shape:
+        raise ValueError("k, v must be [T, Hkv, D] and caches [N, Hkv, B, D]")
+    T, Hkv, D = k.shape
+    Nb, Hc, B, Dc = k_cache.shape
+    if (Hc, Dc) != (Hkv, D) or slot_mapping.shape != (T,):
+        raise ValueError("k/v heads and head_dim must match the caches; slot_mapping is [T]")
+    if not (k.dtype == v.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("k, v and the caches must share a dtype")
+    status = N.load().pa_reshape_and_cache(k.data_ptr(), v.data_ptr(), k_cache.data_ptr(),
+                                           v_cache.data_ptr(), slot_mapping.data_ptr(), T, Hkv,
+                                           D, B, Nb, _dtype(k), _stream(stream))
+    N.check("pa_reshape_and_cache", status)
+
+
+def pa_copy_blocks(k_caches, v_caches, src_dst_pairs, stream=None) -> None:
+    """Copy whole blocks src -> dst in every layer's K and V pool (copy-on-write).
+
+    k_caches, v_caches: lists of [N, ...] CUDA tensors, one per layer, all of one
+    shape; src_dst_pairs: host sequence / array / CPU tensor of (src, dst) int pairs.
+    """
+    if isinstance(k_caches, torch.Tensor):
+        k_caches, v_caches = [k_caches], [v_caches]
+    if len(k_caches) != len(v_caches) or not k_caches:
+        raise ValueError("k_caches and v_caches must be non-empty lists of equal length")
+    shape = k_caches[0].shape
+    for t in list(k_caches) + list(v_caches):
+        _cuda("cache", t)
+        if t.shape != shape or t.dtype != k_caches[0].dtype:
+            raise ValueError("every cache must have the same shape and dtype")
+    pairs = torch.as_tensor(src_dst_pairs, dtype=torch.int64).reshape(-1, 2).contiguous()
+    if pairs.device.type != "cpu":
+        raise ValueError("src_dst_pairs must live in host memory")
+    n_blocks = shape[0]
+    block_bytes = k_caches[0].numel() * k_caches[0].element_size() // n_blocks
+    L = len(k_caches)
+    kp = (ctypes.c_void_p * L)(*[t.data_ptr() for t in k_caches])
+    vp = (ctypes.c_void_p * L)(*[t.data_ptr() for t in v_caches])
+    pp = ctypes.cast(pairs.data_ptr(), ctypes.POINTER(ctypes.c_int64))
+    status = N.load().pa_copy_blocks(kp, vp, L, pp, pairs.shape[0], block_bytes, n_blocks,
+                                     _stream(stream))
+    N.check("pa_copy_blocks", status)
+
+
+def pa_get_device_error(stream=None) -> int:
+    """Read and clear the device error word (PA_DEVERR_* bits).  Synchronises."""
+    flags = ctypes.c_uint32(0)
+    N.check("pa_get_device_error", N.load().pa_get_device_error(ctypes.byref(flags),
+                                                                 _stream(stream)))
+    return int(flags.value)
+
+
+def pa_version() -> str:
+    return N.load().pa_version().decode()

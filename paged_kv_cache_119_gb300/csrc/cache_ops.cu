@@ -1,0 +1,93 @@
+// cache_ops.cu -- the two cache-maintenance kernels: reshape_and_cache and
+// copy_blocks.  Both are bit-exact 16-byte vector copies; neither touches a value.
+//
+// reshape_and_cache ("PagedAttention 完全拆解", section 原理详解（三）：kernel 实现,
+// item 1, fused reshape and block write; Figure 6 decode steps): the row of each
+// new token and kv head moves to the pool slot its slot_mapping entry names, in
+// the pool's [block][head][slot][dim] order, in one launch.
+//
+// copy_blocks (same section, item 3, fused block copy; section 内存共享, Figure 8):
+// many non-contiguous whole-block copies in one launch instead of one
+// cudaMemcpyAsync per block.  The (src, dst) pairs and per-layer pool pointers
+// travel in the kernel parameter block, so nothing is allocated or uploaded.
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+// One thread per 16-byte vector of a (token, head) row, for K and for V.
+// Consecutive threads cover consecutive vectors of one row, so both the read of
+// k[i][h][:] and the write to the cache slot are fully coalesced.
+__global__ void __launch_bounds__(256) reshape_and_cache_kernel(const ReshapeParams p)
+{
+    const int64_t per_tensor = p.num_tokens * p.num_kv_heads * p.row_vecs;
+    const int64_t total = 2 * per_tensor;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const bool is_v = i >= per_tensor;
+        const int64_t j = is_v ? i - per_tensor : i;
+        const int c = (int)(j % p.row_vecs);
+        const int64_t th = j / p.row_vecs;           // token * num_kv_heads + head
+        const int h = (int)(th % p.num_kv_heads);
+        const int64_t tok = th / p.num_kv_heads;
+        const int64_t slot = p.slot_mapping[tok];
+        if (slot < 0)
+            continue;                                // padding token
+        if (slot >= p.num_blocks * p.block_size) {
+            if (c == 0 && h == 0 && !is_v)
+                atomicOr(p.err, PA_DEVERR_SLOT);
+            continue;
+        }
+        const int64_t blk = slot / p.block_size;
+        const int64_t off = slot - blk * p.block_size;
+        const int64_t dst = ((blk * p.num_kv_heads + h) * p.block_size + off) * p.row_vecs + c;
+        if (is_v)
+            p.v_cache[dst] = p.v[j];
+        else
+            p.k_cache[dst] = p.k[j];
+    }
+}
+
+cudaError_t launch_reshape_and_cache(const ReshapeParams& p, cudaStream_t stream)
+{
+    const int64_t total = 2 * p.num_tokens * p.num_kv_heads * p.row_vecs;
+    if (total == 0)
+        return cudaSuccess;
+    const int sms = device_sm_count();
+    const int64_t want = (total + 255) / 256;
+    const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 16;
+    const int blocks = (int)(want < cap ? want : cap);
+    reshape_and_cache_kernel<<<blocks, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// grid = (pairs, 2 * layers, splits): CTA (p, l2, s) copies the s-th slice of
+// block pairs[p].src of pool l2 (K pools first, then V pools) to pairs[p].dst.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(const CopyParams p)
+{
+    const int pair = blockIdx.x;
+    const int layer = blockIdx.y >> 1;
+    uint4* pool = (blockIdx.y & 1) ? p.v[layer] : p.k[layer];
+    const int64_t src = (int64_t)p.pairs[pair].x * p.block_vecs;
+    const int64_t dst = (int64_t)p.pairs[pair].y * p.block_vecs;
+    const int64_t slice = (p.block_vecs + gridDim.z - 1) / gridDim.z;
+    const int64_t lo = blockIdx.z * slice;
+    const int64_t hi = min(p.block_vecs, lo + slice);
+    for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x)
+        pool[dst + i] = pool[src + i];
+}
+
+cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream)
+{
+    if (p.num_pairs == 0 || p.num_layers == 0)
+        return cudaSuccess;
+    // about 8 vectors per thread per CTA; large blocks are split across CTAs
+    int64_t splits = (p.block_vecs + 2047) / 2048;
+    if (splits > 64)
+        splits = 64;
+    dim3 grid(p.num_pairs, 2 * p.num_layers, (unsigned)splits);
+    copy_blocks_kernel<<<grid, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,489 @@
+// decode_kernel.cuh -- paged decode attention kernels (sm_103a).
+//
+// What is computed ("PagedAttention 完全拆解", section 原理详解（二）：块式注意力的数学):
+// for sequence s and query head h, with kv head h / group,
+//     a_t = exp(scale q.k_t) / sum_u exp(scale q.k_u),   o = sum_t a_t v_t,
+// where k_t, v_t are read from physical block block_tables[s][t / B], slot t % B
+// (iaim.asia/ai-infra/182, section KV Cache 如何按块分配).  The block-wise form
+// on the first page shows the sum may be taken block by block with no
+// approximation; we use the running-max form (online softmax, iaim.asia page,
+// section vLLM 内核里的缓解写法) so every K/V byte is read exactly once.
+//
+// GB300 design:
+//   * CTA = (partition, kv head x query-head chunk, sequence).  All GC query
+//     heads of a chunk share one pass over the kv head's blocks, so with GQA a
+//     K/V tile is read from HBM once per group, not once per query head.
+//   * Warp NCW is the producer: it prefetches the CTA's block-table slice
+//     (int32, 32 entries per coalesced load, one round ahead), turns each entry
+//     into an int64 address and issues one 1-D bulk TMA copy per K tile and per
+//     V tile ([B][D] is contiguous in the pool) into an NSTAGE-deep shared-memory
+//     ring guarded by full/empty mbarriers.  No register staging, no address
+//     arithmetic in the consumers.
+//   * Warps 0..NCW-1 consume tiles round-robin (tile i -> warp i % NCW).  Each
+//     lane owns D/32 contiguous head dims.  Scores: per-token partial dots
+//     reduced by a transposed butterfly (one shuffle per value per halving step,
+//     instead of a full warp reduction per token).  Online softmax in base 2
+//     (scale * log2 e is folded into q), fp32 everywhere.  P is published through
+//     shared memory and P.V accumulates in registers.
+//   * Each warp keeps its own (max, sum, acc); the warps are merged through
+//     shared memory at the end in a fixed order, so the result depends only on
+//     logical token positions, never on physical block ids.
+//   * Split contexts write a normalised partial row plus (max, sum) per
+//     partition; reduce_kernel merges them.
+//   * Masking of the ragged last block is done by select (score = -inf, and the
+//     P.V loop stops at the last valid token) so NaN-filled unused slots never
+//     reach the arithmetic.
+#pragma once
+
+#include <math.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+// Sums v[0..N-1] over the 32 lanes of the warp.  On return, lane l holds the
+// full sum of value index (l >> (5 - log2 N)).  Each halving step exchanges
+// half of the remaining values with the partner lane, so N values cost
+// N - 1 + (5 - log2 N) shuffles instead of 5N.
+template <int N>
+__device__ __forceinline__ float butterfly_sum(float (&v)[N], int lane)
+{
+    static_assert(N >= 1 && N <= 32 && (N & (N - 1)) == 0, "N must be a power of two <= 32");
+    int mask = 16;
+#pragma unroll
+    for (int n = N; n > 1; n >>= 1) {
+        const bool upper = (lane & mask) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = upper ? v[i] : v[i + n / 2];
+            const float keep = upper ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(kFullMask, send, mask);
+        }
+        mask >>= 1;
+    }
+    float r = v[0];
+#pragma unroll
+    for (; mask >= 1; mask >>= 1)
+        r += __shfl_xor_sync(kFullMask, r, mask);
+    return r;
+}
+
+template <int N>
+struct Log2 {
+    static constexpr int value = 1 + Log2<N / 2>::value;
+};
+template <>
+struct Log2<1> {
+    static constexpr int value = 0;
+};
+
+template <typename T, int D, int BS, int GC, int NSTAGE>
+struct DecodeSmem {
+    static constexpr int kTile = BS * D;                       // elements of one K or V tile
+    static constexpr int kTileBytes = kTile * (int)sizeof(T);
+    static constexpr int kRingBytes = NSTAGE * 2 * kTileBytes;
+    static constexpr int kBarOffset = kRingBytes;              // full[NSTAGE], empty[NSTAGE]
+    static constexpr int kOkOffset = kBarOffset + 2 * NSTAGE * 8;
+    static constexpr int kFlagOffset = kOkOffset + NSTAGE * 4;
+    static constexpr int kPOffset = (kFlagOffset + 4 + 15) / 16 * 16;
+    static constexpr int kPBytes = kDecodeConsumerWarps * GC * BS * 4;
+    static constexpr int kAccOffset = kPOffset + kPBytes;
+    static constexpr int kAccBytes = kDecodeConsumerWarps * GC * D * 4;
+    static constexpr int kMlOffset = kAccOffset + kAccBytes;
+    static constexpr int kMlBytes = kDecodeConsumerWarps * GC * 2 * 4;
+    static constexpr int kBytes = kMlOffset + kMlBytes;
+    static_assert(kTileBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
+};
+
+template <typename T>
+__device__ __forceinline__ void store_out(const DecodeParams& p, int64_t idx, float x)
+{
+    if (p.out_f32)
+        store_as(reinterpret_cast<float*>(p.out) + idx, x);
+    else
+        store_as(reinterpret_cast<T*>(p.out) + idx, x);
+}
+
+template <typename T, int D, int BS, int GC, int NSTAGE>
+__global__ void __launch_bounds__(kDecodeThreads)
+    decode_kernel(const DecodeParams p)
+{
+    using Smem = DecodeSmem<T, D, BS, GC, NSTAGE>;
+    constexpr int NCW = kDecodeConsumerWarps;
+    constexpr int E = D / 32;                  // head dims per lane
+    constexpr int TC = BS < 8 ? BS : 8;        // tokens per butterfly
+    constexpr int NCH = BS / TC;               // butterflies per tile
+    constexpr int TOK_SHIFT = 5 - Log2<TC>::value;
+    constexpr int kTile = Smem::kTile;
+    static_assert(D % 32 == 0 && (E == 2 || E == 4), "head_dim must be 64 or 128");
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    T* ring = reinterpret_cast<T*>(smem);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Smem::kBarOffset);
+    uint64_t* empty = full + NSTAGE;
+    int* stage_ok = reinterpret_cast<int*>(smem + Smem::kOkOffset);
+    int* poison = reinterpret_cast<int*>(smem + Smem::kFlagOffset);
+    float* pbuf = reinterpret_cast<float*>(smem + Smem::kPOffset);
+    float* mrg_acc = reinterpret_cast<float*>(smem + Smem::kAccOffset);
+    float* mrg_ml = reinterpret_cast<float*>(smem + Smem::kMlOffset);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int seq = blockIdx.z;
+    const int kvh = blockIdx.y / p.chunks;
+    const int h0 = kvh * p.group + (blockIdx.y % p.chunks) * GC;
+    const int part = blockIdx.x;
+    const bool split = p.partition_tokens > 0;
+
+    const int L = p.context_lens[seq];
+    if (L < 0 || L > p.max_context_len) {
+        if (part == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+            atomicOr(p.err, PA_DEVERR_CONTEXT_LEN);
+        if (!split) {                             // the reduce pass handles split calls
+            for (int idx = threadIdx.x; idx < GC * D; idx += blockDim.x)
+                store_out<T>(p, ((int64_t)seq * p.num_q_heads + h0) * D + idx,
+                             __int_as_float(0x7fc00000));
+        }
+        return;
+    }
+    int t0 = 0, t1 = L;
+    if (split) {
+        t0 = part * p.partition_tokens;
+        if (t0 >= L)
+            return;                               // this partition lies past the context
+        t1 = min(L, t0 + p.partition_tokens);
+    }
+    const int jb = t0 / BS;                       // partitions start on block boundaries
+    const int ntiles = (t1 > t0) ? (t1 + BS - 1) / BS - jb : 0;
+
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        *poison = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == NCW) {
+        // ------------------------------------------------------------------ producer
+        const int32_t* bt_row = p.block_tables + (int64_t)seq * p.bt_stride + jb;
+        const T* kpool = reinterpret_cast<const T*>(p.k_cache) + (int64_t)kvh * kTile;
+        const T* vpool = reinterpret_cast<const T*>(p.v_cache) + (int64_t)kvh * kTile;
+        const int64_t blk_stride = (int64_t)p.num_kv_heads * kTile;
+        const uint64_t policy = l2_evict_first_policy();
+        int next = (lane < ntiles) ? __ldg(bt_row + lane) : 0;
+        bool aborted = false;
+        for (int base = 0; base < ntiles && !aborted; base += 32) {
+            const int cur = next;
+            if (base + 32 + lane < ntiles)
+                next = __ldg(bt_row + base + 32 + lane);   // next round, in flight meanwhile
+            const int cnt = min(32, ntiles - base);
+            for (int i = 0; i < cnt; ++i) {
+                const int pbn = __shfl_sync(kFullMask, cur, i);
+                const int it = base + i;
+                const int stage = it % NSTAGE;
+                int ok = 1;
+                if (lane == 0) {
+                    if (it >= NSTAGE && !mbar_wait(&empty[stage], ((it / NSTAGE) - 1) & 1)) {
+                        atomicOr(p.err, PA_DEVERR_TIMEOUT);
+                        ok = 0;
+                    }
+                    if (ok) {
+                        const bool valid = pbn >= 0 && (int64_t)pbn < p.num_blocks;
+                        stage_ok[stage] = valid ? 1 : 0;
+                        if (valid) {
+                            const int64_t off = (int64_t)pbn * blk_stride;
+                            T* dst = ring + stage * 2 * kTile;
+                            mbar_arrive_expect_tx(&full[stage], 2u * Smem::kTileBytes);
+                            bulk_g2s(dst, kpool + off, Smem::kTileBytes, &full[stage], policy);
+                            bulk_g2s(dst + kTile, vpool + off, Smem::kTileBytes, &full[stage], policy);
+                        } else {
+                            atomicOr(p.err, PA_DEVERR_BLOCK_ID);
+                            mbar_arrive(&full[stage]);
+                        }
+                    }
+                }
+                if (!__shfl_sync(kFullMask, ok, 0)) {
+                    aborted = true;
+                    break;
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------------- consumers
+    float qf[GC][E];
+#pragma unroll
+    for (int g = 0; g < GC; ++g) {
+        const T* qp = reinterpret_cast<const T*>(p.q) + ((int64_t)seq * p.num_q_heads + h0 + g) * D +
+                      lane * E;
+        Load<T, E>::run(qp, qf[g]);
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            qf[g][e] *= p.scale_log2;
+    }
+    float m[GC], lsum[GC], acc[GC][E];
+#pragma unroll
+    for (int g = 0; g < GC; ++g) {
+        m[g] = -INFINITY;
+        lsum[g] = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            acc[g][e] = 0.f;
+    }
+    bool poisoned = false;
+    float* my_p = pbuf + warp * GC * BS;
+    const int mytok = lane >> TOK_SHIFT;
+
+    for (int it = warp; it < ntiles; it += NCW) {
+        const int stage = it % NSTAGE;
+        if (!mbar_wait(&full[stage], (it / NSTAGE) & 1)) {
+            if (lane == 0)
+                atomicOr(p.err, PA_DEVERR_TIMEOUT);
+            poisoned = true;
+            break;
+        }
+        if (!stage_ok[stage]) {
+            poisoned = true;
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[stage]);
+            continue;
+        }
+        const T* Ks = ring + stage * 2 * kTile;
+        const T* Vs = Ks + kTile;
+        const int nvalid = min(BS, t1 - (jb + it) * BS);
+
+        // scores s[g][c] for token c * TC + mytok, base-2 units
+        float s[GC][NCH];
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            float kf[TC][E];
+#pragma unroll
+            for (int tt = 0; tt < TC; ++tt)
+                Load<T, E>::run(Ks + (c * TC + tt) * D + lane * E, kf[tt]);
+#pragma unroll
+            for (int g = 0; g < GC; ++g) {
+                float part_dot[TC];
+#pragma unroll
+                for (int tt = 0; tt < TC; ++tt) {
+                    float a = qf[g][0] * kf[tt][0];
+#pragma unroll
+                    for (int e = 1; e < E; ++e)
+                        a = fmaf(qf[g][e], kf[tt][e], a);
+                    part_dot[tt] = a;
+                }
+                s[g][c] = butterfly_sum<TC>(part_dot, lane);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < NCH; ++c)
+            if (c * TC + mytok >= nvalid) {
+#pragma unroll
+                for (int g = 0; g < GC; ++g)
+                    s[g][c] = -INFINITY;
+            }
+
+        // online softmax update per head
+#pragma unroll
+        for (int g = 0; g < GC; ++g) {
+            float tmax = s[g][0];
+#pragma unroll
+            for (int c = 1; c < NCH; ++c)
+                tmax = fmaxf(tmax, s[g][c]);
+#pragma unroll
+            for (int msk = 16; msk >= (1 << TOK_SHIFT); msk >>= 1)
+                tmax = fmaxf(tmax, __shfl_xor_sync(kFullMask, tmax, msk));
+            const float mnew = fmaxf(m[g], tmax);        // finite: nvalid >= 1
+            const float alpha = exp2f(m[g] - mnew);       // 0 on the first tile
+            m[g] = mnew;
+            float psum = 0.f;
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+                s[g][c] = exp2f(s[g][c] - mnew);
+                psum += s[g][c];
+            }
+            lsum[g] = fmaf(lsum[g], alpha, psum);
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                acc[g][e] *= alpha;
+            if ((lane & ((1 << TOK_SHIFT) - 1)) == 0) {
+#pragma unroll
+                for (int c = 0; c < NCH; ++c)
+                    my_p[g * BS + c * TC + mytok] = s[g][c];
+            }
+        }
+        __syncwarp();
+
+        // acc += P . V over the valid tokens of the tile
+#pragma unroll
+        for (int t4 = 0; t4 < BS; t4 += 4) {
+            if (t4 < nvalid) {
+                float4 pv[GC];
+#pragma unroll
+                for (int g = 0; g < GC; ++g)
+                    pv[g] = *reinterpret_cast<const float4*>(my_p + g * BS + t4);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (t4 + u < nvalid) {
+                        float vf[E];
+                        Load<T, E>::run(Vs + (t4 + u) * D + lane * E, vf);
+#pragma unroll
+                        for (int g = 0; g < GC; ++g) {
+                            const float pt = u == 0 ? pv[g].x : u == 1 ? pv[g].y : u == 2 ? pv[g].z : pv[g].w;
+#pragma unroll
+                            for (int e = 0; e < E; ++e)
+                                acc[g][e] = fmaf(pt, vf[e], acc[g][e]);
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[stage]);
+    }
+
+    // ------------------------------------------------------------- merge the warps
+#pragma unroll
+    for (int g = 0; g < GC; ++g) {
+        float l = lsum[g];
+#pragma unroll
+        for (int msk = 16; msk >= (1 << TOK_SHIFT); msk >>= 1)
+            l += __shfl_xor_sync(kFullMask, l, msk);
+        if (lane == 0) {
+            mrg_ml[(warp * GC + g) * 2 + 0] = m[g];
+            mrg_ml[(warp * GC + g) * 2 + 1] = l;
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            mrg_acc[(warp * GC + g) * D + lane * E + e] = acc[g][e];
+    }
+    if (poisoned)
+        *poison = 1;
+    named_barrier(1, NCW * 32);
+
+    const bool bad = *poison != 0;
+    for (int idx = threadIdx.x; idx < GC * D; idx += NCW * 32) {
+        const int g = idx / D;
+        const int d = idx - g * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w)
+            M = fmaxf(M, mrg_ml[(w * GC + g) * 2]);
+        float num = 0.f, den = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NCW; ++w) {
+                const float c = exp2f(mrg_ml[(w * GC + g) * 2] - M);
+                num = fmaf(c, mrg_acc[(w * GC + g) * D + d], num);
+                den = fmaf(c, mrg_ml[(w * GC + g) * 2 + 1], den);
+            }
+        }
+        float o = den > 0.f ? num / den : 0.f;
+        if (bad)
+            o = __int_as_float(0x7fc00000);
+        const int64_t row = (int64_t)seq * p.num_q_heads + h0 + g;
+        if (split) {
+            const int64_t prow = row * p.max_parts + part;
+            p.part_o[prow * D + d] = o;
+            if (d == 0) {
+                p.part_ml[prow * 2 + 0] = M;
+                p.part_ml[prow * 2 + 1] = den;
+            }
+        } else {
+            store_out<T>(p, row * D + d, o);
+        }
+    }
+}
+
+// Second pass of a split call: merges the partitions of one (sequence, query
+// head).  With per-partition maxima m_p, sums l_p and normalised rows o_p:
+//   M = max m_p,  w_p = 2^(m_p - M) l_p,  o = sum w_p o_p / sum w_p.
+// Launched with D threads per CTA, grid (num_q_heads, num_seqs).
+template <typename T, int D>
+__global__ void __launch_bounds__(D) reduce_kernel(const DecodeParams p)
+{
+    const int h = blockIdx.x;
+    const int seq = blockIdx.y;
+    const int d = threadIdx.x;
+    const int64_t row = (int64_t)seq * p.num_q_heads + h;
+    const int L = p.context_lens[seq];
+    if (L < 0 || L > p.max_context_len) {
+        store_out<T>(p, row * D + d, __int_as_float(0x7fc00000));
+        return;
+    }
+    const int nparts = (L + p.partition_tokens - 1) / p.partition_tokens;
+    const float* ml = p.part_ml + row * p.max_parts * 2;
+    const float* po = p.part_o + row * p.max_parts * D + d;
+    float M = -INFINITY;
+    for (int i = 0; i < nparts; ++i)
+        M = fmaxf(M, ml[2 * i]);
+    float num = 0.f, den = 0.f;
+    for (int i = 0; i < nparts; ++i) {
+        const float w = exp2f(ml[2 * i] - M) * ml[2 * i + 1];
+        num = fmaf(w, po[(int64_t)i * D], num);
+        den += w;
+    }
+    store_out<T>(p, row * D + d, den > 0.f ? num / den : 0.f);
+}
+
+// Chooses the ring depth: about 48 KB of K/V stages per CTA, at least 2.
+template <typename T, int D, int BS>
+struct DecodeStages {
+    static constexpr int kStageBytes = 2 * BS * D * (int)sizeof(T);
+    static constexpr int kRaw = 49152 / kStageBytes;
+    static constexpr int value = kRaw < 2 ? 2 : (kRaw > 12 ? 12 : kRaw);
+};
+
+template <typename T, int D, int BS, int GC>
+cudaError_t launch_decode_variant(const DecodeParams& p, cudaStream_t stream)
+{
+    constexpr int NSTAGE = DecodeStages<T, D, BS>::value;
+    using Smem = DecodeSmem<T, D, BS, GC, NSTAGE>;
+    auto kern = decode_kernel<T, D, BS, GC, NSTAGE>;
+    static int configured_device = -1;      // dynamic smem opt-in, once per device
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    if (configured_device != dev) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem::kBytes);
+        if (err != cudaSuccess)
+            return err;
+        configured_device = dev;
+    }
+    const bool split = p.partition_tokens > 0;
+    dim3 grid(split ? p.max_parts : 1, p.num_kv_heads * p.chunks, p.num_seqs);
+    kern<<<grid, kDecodeThreads, Smem::kBytes, stream>>>(p);
+    err = cudaGetLastError();
+    if (err != cudaSuccess || !split)
+        return err;
+    reduce_kernel<T, D><<<dim3(p.num_q_heads, p.num_seqs), D, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_decode_typed(const DecodeParams& p, int head_dim, int block_size, int gc,
+                                cudaStream_t stream)
+{
+#define PA_DECODE_CASE(D_, BS_, GC_)                                  \
+    if (head_dim == D_ && block_size == BS_ && gc == GC_)             \
+        return launch_decode_variant<T, D_, BS_, GC_>(p, stream);
+#define PA_DECODE_GC(D_, BS_) \
+    PA_DECODE_CASE(D_, BS_, 1) PA_DECODE_CASE(D_, BS_, 2) PA_DECODE_CASE(D_, BS_, 4) PA_DECODE_CASE(D_, BS_, 8)
+    PA_DECODE_GC(128, 16)
+    PA_DECODE_GC(128, 32)
+    PA_DECODE_GC(64, 16)
+    PA_DECODE_GC(64, 32)
+#undef PA_DECODE_GC
+#undef PA_DECODE_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

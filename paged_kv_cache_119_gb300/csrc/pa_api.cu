@@ -1,0 +1,333 @@
+// pa_api.cu -- the C ABI of libpa.so (declared in include/pa.h): argument
+// validation, the split-context decision, workspace carving and kernel dispatch.
+// Everything here is host code except the device error word.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace pa {
+
+// Device error word (PA_DEVERR_* bits); one per device, set by the kernels.
+__device__ unsigned g_device_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+unsigned* g_error_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t elem_size(int dt) { return dt == PA_F32 ? 4 : 2; }
+
+bool valid_dtype(int dt) { return dt == PA_F32 || dt == PA_F16 || dt == PA_BF16; }
+
+// [a, a + na) and [b, b + nb) share a byte.
+bool overlaps(const void* a, size_t na, const void* b, size_t nb)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return na && nb && x < y + nb && y < x + na;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Query heads served by one decode CTA: the largest of 8, 4, 2, 1 dividing the group.
+int heads_per_cta(int group)
+{
+    for (int gc : {8, 4, 2, 1})
+        if (group % gc == 0)
+            return gc;
+    return 1;
+}
+
+// Partition length in tokens, or 0 for one pass per (sequence, kv head).
+int choose_partition(int partition_size, int max_context_len, int64_t ctas_unsplit, int sms)
+{
+    if (partition_size < 0)
+        return 0;
+    if (partition_size > 0)
+        return max_context_len > partition_size ? partition_size : 0;
+    const int P = kAutoPartitionTokens;
+    if (max_context_len <= P)
+        return 0;
+    if (ctas_unsplit < 2LL * (sms > 0 ? sms : 148))
+        return P;                    // too few CTAs to keep every SM streaming
+    if (max_context_len > 8 * P)
+        return P;                    // very long contexts: bound the work of one CTA
+    return 0;
+}
+
+size_t workspace_layout(int64_t rows, int max_parts, int head_dim, size_t* ml_offset)
+{
+    const size_t o_bytes = align_up((size_t)rows * max_parts * head_dim * sizeof(float), 256);
+    if (ml_offset)
+        *ml_offset = o_bytes;
+    return o_bytes + (size_t)rows * max_parts * 2 * sizeof(float);
+}
+
+}  // namespace
+
+unsigned* device_error_word()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    if (!g_error_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess)
+            return nullptr;
+        g_error_ptr[dev] = static_cast<unsigned*>(ptr);
+    }
+    return g_error_ptr[dev];
+}
+
+int device_sm_count()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return 0;
+    if (!g_sm_count[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char* pa_status_string(int status)
+{
+    switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID: return "PA_ERR_INVALID: invalid argument";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: head_dim/block_size/dtype not built";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: split-context workspace missing or too small";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA runtime or launch failure";
+    default: return "unknown pa_status";
+    }
+}
+
+const char* pa_version(void) { return "paged_kv_cache_119_gb300 0.1 sm_103a"; }
+
+size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                 int32_t max_context_len, int32_t block_size,
+                                 int32_t partition_size)
+{
+    if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0 ||
+        block_size <= 0 || partition_size < 0)
+        return 0;
+    const int P = partition_size > 0 ? partition_size : kAutoPartitionTokens;
+    if (max_context_len <= P)
+        return 0;
+    const int max_parts = (max_context_len + P - 1) / P;
+    return workspace_layout((int64_t)num_seqs * num_q_heads, max_parts, head_dim, nullptr);
+}
+
+int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
+              const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
+              const int32_t* block_tables, int64_t block_table_stride,
+              const int32_t* context_lens, int32_t max_context_len, int32_t num_seqs,
+              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+              float scale, int32_t partition_size, void* workspace, size_t workspace_bytes,
+              void* stream)
+{
+    if (!valid_dtype(kv_dtype) || !(out_dtype == PA_F32 || out_dtype == kv_dtype))
+        return PA_ERR_INVALID;
+    if (num_seqs < 0 || num_seqs > 65535 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        num_q_heads % num_kv_heads != 0)
+        return PA_ERR_INVALID;
+    if (!(head_dim == 64 || head_dim == 128) || !(block_size == 16 || block_size == 32))
+        return PA_ERR_UNSUPPORTED;
+    if (num_blocks <= 0 || num_blocks > INT32_MAX || block_table_stride <= 0 ||
+        max_context_len < 0 || (int64_t)max_context_len > block_table_stride * block_size ||
+        !std::isfinite(scale))
+        return PA_ERR_INVALID;
+    if (partition_size > 0 && partition_size % block_size != 0)
+        return PA_ERR_INVALID;
+    if (num_seqs == 0)
+        return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return PA_ERR_INVALID;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID;
+
+    const int group = num_q_heads / num_kv_heads;
+    const int gc = heads_per_cta(group);
+    const int chunks = group / gc;
+    if ((int64_t)num_kv_heads * chunks > 65535)
+        return PA_ERR_INVALID;
+    const size_t esz = elem_size(kv_dtype);
+    const size_t q_bytes = (size_t)num_seqs * num_q_heads * head_dim * esz;
+    const size_t out_bytes = (size_t)num_seqs * num_q_heads * head_dim * elem_size(out_dtype);
+    const size_t pool_bytes = (size_t)num_blocks * num_kv_heads * block_size * head_dim * esz;
+    if (overlaps(out, out_bytes, q, q_bytes) || overlaps(out, out_bytes, k_cache, pool_bytes) ||
+        overlaps(out, out_bytes, v_cache, pool_bytes))
+        return PA_ERR_INVALID;
+
+    const int sms = device_sm_count();
+    const int P = choose_partition(partition_size, max_context_len,
+                                   (int64_t)num_seqs * num_kv_heads * chunks, sms);
+    DecodeParams p{};
+    p.out = out;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.num_blocks = num_blocks;
+    p.bt_stride = block_table_stride;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = group;
+    p.chunks = chunks;
+    p.max_context_len = max_context_len;
+    p.partition_tokens = P;
+    p.max_parts = 1;
+    p.out_f32 = out_dtype == PA_F32 ? 1 : 0;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);  // log2(e)
+    if (P > 0) {
+        p.max_parts = (max_context_len + P - 1) / P;
+        size_t ml_off = 0;
+        const size_t need = workspace_layout((int64_t)num_seqs * num_q_heads, p.max_parts,
+                                             head_dim, &ml_off);
+        if (!workspace || workspace_bytes < need || !aligned16(workspace))
+            return PA_ERR_WORKSPACE;
+        if (overlaps(out, out_bytes, workspace, need))
+            return PA_ERR_INVALID;
+        p.part_o = static_cast<float*>(workspace);
+        p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ml_off);
+    }
+    p.err = device_error_word();
+    if (!p.err)
+        return PA_ERR_CUDA;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (kv_dtype) {
+    case PA_F32: e = launch_decode_f32(p, head_dim, block_size, gc, st); break;
+    case PA_F16: e = launch_decode_f16(p, head_dim, block_size, gc, st); break;
+    case PA_BF16: e = launch_decode_bf16(p, head_dim, block_size, gc, st); break;
+    }
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                         const int64_t* slot_mapping, int64_t num_tokens, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size, int64_t num_blocks,
+                         pa_dtype dtype, void* stream)
+{
+    if (!valid_dtype(dtype) || num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        block_size <= 0 || num_blocks <= 0)
+        return PA_ERR_INVALID;
+    const size_t row_bytes = (size_t)head_dim * elem_size(dtype);
+    if (row_bytes % 16 != 0)
+        return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0)
+        return PA_OK;
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping)
+        return PA_ERR_INVALID;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID;
+    const size_t pool_bytes = (size_t)num_blocks * num_kv_heads * block_size * row_bytes;
+    if (overlaps(k_cache, pool_bytes, v_cache, pool_bytes))
+        return PA_ERR_INVALID;
+    ReshapeParams p{};
+    p.k = static_cast<const uint4*>(k);
+    p.v = static_cast<const uint4*>(v);
+    p.k_cache = static_cast<uint4*>(k_cache);
+    p.v_cache = static_cast<uint4*>(v_cache);
+    p.slot_mapping = slot_mapping;
+    p.err = device_error_word();
+    if (!p.err)
+        return PA_ERR_CUDA;
+    p.num_tokens = num_tokens;
+    p.num_blocks = num_blocks;
+    p.num_kv_heads = num_kv_heads;
+    p.row_vecs = (int)(row_bytes / 16);
+    p.block_size = block_size;
+    return launch_reshape_and_cache(p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
+                   const int64_t* src_dst_pairs_host, int64_t num_pairs, int64_t block_bytes,
+                   int64_t num_blocks, void* stream)
+{
+    if (num_layers < 0 || num_pairs < 0 || block_bytes <= 0 || block_bytes % 16 != 0 ||
+        num_blocks <= 0 || num_blocks > INT32_MAX)
+        return PA_ERR_INVALID;
+    if (num_layers == 0 || num_pairs == 0)
+        return PA_OK;
+    if (!k_caches || !v_caches || !src_dst_pairs_host)
+        return PA_ERR_INVALID;
+    for (int l = 0; l < num_layers; ++l)
+        if (!k_caches[l] || !v_caches[l] || !aligned16(k_caches[l]) || !aligned16(v_caches[l]))
+            return PA_ERR_INVALID;
+    std::vector<int64_t> dst(num_pairs), src(num_pairs);
+    for (int64_t i = 0; i < num_pairs; ++i) {
+        src[i] = src_dst_pairs_host[2 * i];
+        dst[i] = src_dst_pairs_host[2 * i + 1];
+        if (src[i] < 0 || src[i] >= num_blocks || dst[i] < 0 || dst[i] >= num_blocks)
+            return PA_ERR_INVALID;
+    }
+    std::sort(dst.begin(), dst.end());
+    if (std::adjacent_find(dst.begin(), dst.end()) != dst.end())
+        return PA_ERR_INVALID;                       // two pairs write one block
+    for (int64_t s : src)
+        if (std::binary_search(dst.begin(), dst.end(), s))
+            return PA_ERR_INVALID;                   // a destination is also a source
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    for (int l0 = 0; l0 < num_layers; l0 += kCopyMaxLayers) {
+        for (int64_t p0 = 0; p0 < num_pairs; p0 += kCopyMaxPairs) {
+            CopyParams p{};
+            p.num_layers = std::min<int>(kCopyMaxLayers, num_layers - l0);
+            p.num_pairs = (int)std::min<int64_t>(kCopyMaxPairs, num_pairs - p0);
+            p.block_vecs = block_bytes / 16;
+            for (int l = 0; l < p.num_layers; ++l) {
+                p.k[l] = static_cast<uint4*>(k_caches[l0 + l]);
+                p.v[l] = static_cast<uint4*>(v_caches[l0 + l]);
+            }
+            for (int i = 0; i < p.num_pairs; ++i)
+                p.pairs[i] = make_int2((int)src_dst_pairs_host[2 * (p0 + i)],
+                                       (int)src_dst_pairs_host[2 * (p0 + i) + 1]);
+            if (launch_copy_blocks(p, st) != cudaSuccess)
+                return PA_ERR_CUDA;
+        }
+    }
+    return PA_OK;
+}
+
+int pa_get_device_error(uint32_t* flags, void* stream)
+{
+    if (!flags)
+        return PA_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned value = 0;
+    const unsigned zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&value, g_device_error, sizeof value, 0,
+                                  cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof zero, 0, cudaMemcpyHostToDevice,
+                                st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return PA_ERR_CUDA;
+    *flags = value;
+    return PA_OK;
+}
+
+}  // extern "C"

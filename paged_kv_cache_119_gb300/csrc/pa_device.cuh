@@ -1,0 +1,200 @@
+// pa_device.cuh -- device-side helpers shared by the library's kernels:
+// mbarrier and bulk-copy (TMA) PTX wrappers, bounded waits, dtype loads/stores.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// A bounded pipeline wait gives up after this many nanoseconds of %globaltimer.
+// No legitimate wait in these kernels comes near it (a whole launch takes well
+// under a millisecond); it only turns a lost completion into an error flag.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+// Makes mbarrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    uint64_t state;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 %0, [%1], %2;"
+                 : "=l"(state)
+                 : "r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+    (void)state;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    uint64_t state;
+    asm volatile("mbarrier.arrive.shared::cta.b64 %0, [%1];"
+                 : "=l"(state)
+                 : "r"(smem_addr(bar))
+                 : "memory");
+    (void)state;
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Waits for the phase with the given parity to complete.  Returns false (and
+// stops waiting) once kWaitLimitNs has passed.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity))
+                return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs)
+            return false;
+    }
+}
+
+// L2 policy for data read exactly once per launch (the KV stream).
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 1-D bulk copy global -> shared through the TMA unit; completion is counted in
+// bytes on `bar`.  dst, src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// Named barrier over a subset of the CTA's warps.
+__device__ __forceinline__ void named_barrier(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ----------------------------------------------------------------------------- dtypes
+
+template <typename T>
+struct DType;
+template <>
+struct DType<float> {
+    static constexpr pa_dtype id = PA_F32;
+};
+template <>
+struct DType<__half> {
+    static constexpr pa_dtype id = PA_F16;
+};
+template <>
+struct DType<__nv_bfloat16> {
+    static constexpr pa_dtype id = PA_BF16;
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Loads N consecutive elements (N * sizeof(T) bytes, naturally aligned) as fp32.
+template <typename T, int N>
+struct Load;
+
+template <>
+struct Load<__nv_bfloat16, 4> {
+    __device__ __forceinline__ static void run(const __nv_bfloat16* p, float (&f)[4])
+    {
+        const uint2 w = *reinterpret_cast<const uint2*>(p);
+        f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x); f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
+    }
+};
+template <>
+struct Load<__nv_bfloat16, 2> {
+    __device__ __forceinline__ static void run(const __nv_bfloat16* p, float (&f)[2])
+    {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+        f[0] = bf16_lo(w); f[1] = bf16_hi(w);
+    }
+};
+template <>
+struct Load<__half, 4> {
+    __device__ __forceinline__ static void run(const __half* p, float (&f)[4])
+    {
+        const uint2 w = *reinterpret_cast<const uint2*>(p);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+        f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    }
+};
+template <>
+struct Load<__half, 2> {
+    __device__ __forceinline__ static void run(const __half* p, float (&f)[2])
+    {
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(p));
+        f[0] = a.x; f[1] = a.y;
+    }
+};
+template <>
+struct Load<float, 4> {
+    __device__ __forceinline__ static void run(const float* p, float (&f)[4])
+    {
+        const float4 w = *reinterpret_cast<const float4*>(p);
+        f[0] = w.x; f[1] = w.y; f[2] = w.z; f[3] = w.w;
+    }
+};
+template <>
+struct Load<float, 2> {
+    __device__ __forceinline__ static void run(const float* p, float (&f)[2])
+    {
+        const float2 w = *reinterpret_cast<const float2*>(p);
+        f[0] = w.x; f[1] = w.y;
+    }
+};
+
+// Stores one fp32 value as T, rounding to nearest even.
+__device__ __forceinline__ void store_as(float* p, float x) { *p = x; }
+__device__ __forceinline__ void store_as(__half* p, float x) { *p = __float2half_rn(x); }
+__device__ __forceinline__ void store_as(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+}  // namespace pa

@@ -1,0 +1,86 @@
+// pa_internal.h -- declarations shared by the library's translation units
+// (kernel parameter blocks and per-dtype launchers).  Not part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// Consumer warps per decode CTA; one more warp issues the bulk copies.
+constexpr int kDecodeConsumerWarps = 4;
+constexpr int kDecodeThreads = (kDecodeConsumerWarps + 1) * 32;
+// Partition length the automatic split uses (a multiple of every block size).
+constexpr int kAutoPartitionTokens = 512;
+
+struct DecodeParams {
+    void* out;
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    float* part_o;       // [S][Hq][max_parts][D] normalised partial outputs (split only)
+    float* part_ml;      // [S][Hq][max_parts][2] (running max in log2 units, sum)
+    unsigned* err;       // device error word
+    int64_t num_blocks;
+    int64_t bt_stride;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;           // num_q_heads / num_kv_heads
+    int chunks;          // group / heads-per-CTA
+    int max_context_len;
+    int partition_tokens;  // 0: one CTA covers the whole context
+    int max_parts;
+    int out_f32;
+    float scale_log2;    // scale * log2(e): scores are kept in base-2 units
+};
+
+// Per-dtype decode launchers (one translation unit each).  `gc` is the number of
+// query heads one CTA serves (1, 2, 4 or 8).  Return cudaErrorInvalidValue for
+// an unsupported (head_dim, block_size, gc) combination.
+cudaError_t launch_decode_f32(const DecodeParams& p, int head_dim, int block_size, int gc,
+                              cudaStream_t stream);
+cudaError_t launch_decode_f16(const DecodeParams& p, int head_dim, int block_size, int gc,
+                              cudaStream_t stream);
+cudaError_t launch_decode_bf16(const DecodeParams& p, int head_dim, int block_size, int gc,
+                               cudaStream_t stream);
+
+struct ReshapeParams {
+    const uint4* k;
+    const uint4* v;
+    uint4* k_cache;
+    uint4* v_cache;
+    const int64_t* slot_mapping;
+    unsigned* err;
+    int64_t num_tokens;
+    int64_t num_blocks;
+    int num_kv_heads;
+    int row_vecs;       // 16-byte vectors per head row (head_dim * elem_size / 16)
+    int block_size;
+};
+cudaError_t launch_reshape_and_cache(const ReshapeParams& p, cudaStream_t stream);
+
+// One copy_blocks launch covers up to kCopyMaxLayers layers and kCopyMaxPairs
+// pairs; the parameter block stays under the classic 4 KB kernel-parameter limit.
+constexpr int kCopyMaxLayers = 8;
+constexpr int kCopyMaxPairs = 480;
+struct CopyParams {
+    uint4* k[kCopyMaxLayers];
+    uint4* v[kCopyMaxLayers];
+    int2 pairs[kCopyMaxPairs];
+    int64_t block_vecs;  // 16-byte vectors per block
+    int num_layers;
+    int num_pairs;
+};
+cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);
+
+// The calling device's error word (device address), or nullptr on failure.
+unsigned* device_error_word();
+// SM count of the calling device (cached), or 0 on failure.
+int device_sm_count();
+
+}  // namespace pa

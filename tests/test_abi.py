@@ -1,0 +1,144 @@
+"""The C ABI without a GPU: the library loads, exports every symbol include/pa.h
+declares, and rejects invalid arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_119_gb300 import _native as N
+from paged_kv_cache_119_gb300 import build as B
+
+HEADER = os.path.join(B.ROOT, "include", "pa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return N.load()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(N.SIGNATURES)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert b"sm_103a" in lib.pa_version()
+    for st in (N.PA_OK, N.PA_ERR_INVALID, N.PA_ERR_UNSUPPORTED, N.PA_ERR_WORKSPACE,
+               N.PA_ERR_CUDA, 12345):
+        assert lib.pa_status_string(st)
+
+
+def test_workspace_bytes(lib):
+    # 8 seqs x 64 heads x 64 partitions x (128 + 2) fp32 values, o rows 256-aligned
+    ws = lib.pa_decode_workspace_bytes(8, 64, 128, 32768, 16, 512)
+    assert ws == 8 * 64 * 64 * 128 * 4 + 8 * 64 * 64 * 2 * 4
+    assert lib.pa_decode_workspace_bytes(8, 64, 128, 512, 16, 512) == 0      # never splits
+    assert lib.pa_decode_workspace_bytes(8, 64, 128, 4096, 16, 0) > 0         # auto upper bound
+    assert lib.pa_decode_workspace_bytes(-1, 64, 128, 4096, 16, 0) == 0
+
+
+FAKE = 1 << 20        # a 16-byte-aligned non-null address; never dereferenced here
+
+
+def decode_args(**kw):
+    a = dict(out=FAKE, out_dtype=N.PA_BF16, q=FAKE * 2, k=FAKE * 3, v=FAKE * 4,
+             kv_dtype=N.PA_BF16, num_blocks=10, bt=FAKE * 5, bt_stride=8, cl=FAKE * 6,
+             max_ctx=64, S=2, Hq=4, Hkv=2, D=128, B=16, scale=0.1, part=0, ws=0, ws_bytes=0,
+             stream=0)
+    a.update(kw)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(kv_dtype=7), N.PA_ERR_INVALID),
+    (dict(out_dtype=N.PA_F16), N.PA_ERR_INVALID),                 # out neither f32 nor kv dtype
+    (dict(Hq=5), N.PA_ERR_INVALID),                               # Hq % Hkv != 0
+    (dict(D=96), N.PA_ERR_UNSUPPORTED),
+    (dict(B=8), N.PA_ERR_UNSUPPORTED),
+    (dict(max_ctx=8 * 16 + 1), N.PA_ERR_INVALID),                 # beyond the table row
+    (dict(num_blocks=0), N.PA_ERR_INVALID),
+    (dict(num_blocks=1 << 31), N.PA_ERR_INVALID),
+    (dict(scale=float("nan")), N.PA_ERR_INVALID),
+    (dict(part=24), N.PA_ERR_INVALID),                            # not a multiple of B
+    (dict(q=0), N.PA_ERR_INVALID),
+    (dict(k=FAKE + 8), N.PA_ERR_INVALID),                         # misaligned cache
+    (dict(out=FAKE * 2), N.PA_ERR_INVALID),                       # out aliases q
+    (dict(S=70000), N.PA_ERR_INVALID),
+])
+def test_decode_rejects(lib, kw, status):
+    assert lib.pa_decode(*decode_args(**kw)) == status
+
+
+def test_decode_split_needs_workspace(lib):
+    # an explicit split with no workspace is rejected before any launch
+    assert lib.pa_decode(*decode_args(part=16, max_ctx=64)) == N.PA_ERR_WORKSPACE
+
+
+def test_decode_empty_batch_is_a_no_op(lib):
+    assert lib.pa_decode(*decode_args(S=0)) == N.PA_OK
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=9), N.PA_ERR_INVALID),
+    (dict(D=4, dtype=N.PA_F16), N.PA_ERR_UNSUPPORTED),            # row not a multiple of 16 B
+    (dict(k=FAKE + 4), N.PA_ERR_INVALID),
+    (dict(T=-1), N.PA_ERR_INVALID),
+    (dict(kc=FAKE * 8, vc=FAKE * 8), N.PA_ERR_INVALID),          # K and V pools overlap
+])
+def test_reshape_rejects(lib, kw, status):
+    a = dict(k=FAKE, v=FAKE * 2, kc=FAKE * 8, vc=FAKE * 64, slots=FAKE * 4, T=3, Hkv=2, D=64,
+             B=16, N=4, dtype=N.PA_BF16, stream=0)
+    a.update(kw)
+    assert lib.pa_reshape_and_cache(*a.values()) == status
+
+
+def test_reshape_zero_tokens_is_a_no_op(lib):
+    assert lib.pa_reshape_and_cache(0, 0, 0, 0, 0, 0, 2, 64, 16, 4, N.PA_BF16, 0) == N.PA_OK
+
+
+def _copy(lib, pairs, num_blocks=8, block_bytes=64, layers=1):
+    ptrs = (ctypes.c_void_p * layers)(*[FAKE * (i + 1) for i in range(layers)])
+    flat = [x for p in pairs for x in p]
+    arr = (ctypes.c_int64 * max(1, len(flat)))(*flat)
+    return lib.pa_copy_blocks(ptrs, ptrs, layers, arr, len(pairs), block_bytes, num_blocks, None)
+
+
+@pytest.mark.parametrize("pairs", [
+    [(0, 8)],               # dst out of range
+    [(-1, 2)],              # src out of range
+    [(0, 2), (1, 2)],       # two pairs write one block
+    [(0, 2), (2, 3)],       # a destination is also a source
+])
+def test_copy_blocks_rejects(lib, pairs):
+    assert _copy(lib, pairs) == N.PA_ERR_INVALID
+
+
+def test_copy_blocks_rejects_bad_sizes(lib):
+    assert _copy(lib, [(0, 1)], block_bytes=24) == N.PA_ERR_INVALID
+    assert _copy(lib, [], block_bytes=64) == N.PA_OK
+
+
+def test_get_device_error_needs_a_pointer(lib):
+    assert lib.pa_get_device_error(None, None) == N.PA_ERR_INVALID
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    import paged_kv_cache_119_gb300 as P
+    x = torch.zeros(2, 4, 64)
+    with pytest.raises(ValueError, match="CUDA"):
+        P.pa_decode(x, x, torch.zeros(1, 4, 16, 64), torch.zeros(1, 4, 16, 64),
+                    torch.zeros(2, 1, dtype=torch.int32), torch.zeros(2, dtype=torch.int32),
+                    0.125, 4, 16)
