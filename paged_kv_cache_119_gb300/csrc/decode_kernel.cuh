@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
     constexpr int TOK_SHIFT = 5 - Log2<TC>::value;
     constexpr int kTile = Smem::kTile;
     static_assert(D % 32 == 0 && (E == 2 || E == 4), "head_dim must be 64 or 128");
+    static_assert(NSTAGE % NCW == 0, "each ring stage must belong to one consumer warp");
 
     extern __shared__ __align__(128) unsigned char smem[];
     T* ring = reinterpret_cast<T*>(smem);
@@ -433,12 +434,19 @@ __global__ void __launch_bounds__(D) reduce_kernel(const DecodeParams p)
     store_out<T>(p, row * D + d, den > 0.f ? num / den : 0.f);
 }
 
-// Chooses the ring depth: about 48 KB of K/V stages per CTA, at least 2.
+// Ring depth: a multiple of the consumer-warp count (about 64 KB of K/V per CTA,
+// 1 to 3 stages per warp).  Because tile i uses stage i % NSTAGE and is consumed
+// by warp i % NCW, NCW | NSTAGE makes every stage belong to exactly one warp,
+// which consumes its rounds in order.  So a consumer never waits on a phase more
+// than one ahead of its barrier, and parity waits are exact.  (With NSTAGE not a
+// multiple of NCW, two warps can hold different rounds of one stage at once and
+// a parity wait can succeed a full phase early.)
 template <typename T, int D, int BS>
 struct DecodeStages {
     static constexpr int kStageBytes = 2 * BS * D * (int)sizeof(T);
-    static constexpr int kRaw = 49152 / kStageBytes;
-    static constexpr int value = kRaw < 2 ? 2 : (kRaw > 12 ? 12 : kRaw);
+    static constexpr int kPerWarp = 65536 / (kDecodeConsumerWarps * kStageBytes);
+    static constexpr int value =
+        kDecodeConsumerWarps * (kPerWarp < 1 ? 1 : (kPerWarp > 3 ? 3 : kPerWarp));
 };
 
 template <typename T, int D, int BS, int GC>

@@ -27,7 +27,12 @@ if not torch.cuda.is_available():
 def built():
     from paged_kv_cache_119_gb300 import build
     build.build()
-    P.pa_get_device_error()          # start from a clear error word
+
+
+@pytest.fixture(autouse=True)
+def clear_error_word(built):
+    P.pa_get_device_error()          # every test starts from a clear error word
+    yield
 
 
 def bits(t: torch.Tensor) -> torch.Tensor:
@@ -217,7 +222,7 @@ def test_head_groupings(Hq, Hkv, D, B):
 def test_many_layers_and_pairs_copy_in_chunks():
     """copy_blocks over more layers and pairs than one launch carries."""
     torch.manual_seed(0)
-    layers, n, pairs = 11, 1200, 700
+    layers, n, pairs = 11, 1600, 700
     kc = [torch.randn(n, 2, 16, 64, device="cuda", dtype=torch.float16) for _ in range(layers)]
     vc = [torch.randn(n, 2, 16, 64, device="cuda", dtype=torch.float16) for _ in range(layers)]
     perm = torch.randperm(n, generator=torch.Generator().manual_seed(1))
