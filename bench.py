@@ -59,6 +59,8 @@ def parse_args(argv=None):
     ap.add_argument("--config", choices=sorted(WORKLOADS), default="llama13b")
     ap.add_argument("--partition-size", type=int, default=None,
                     help="pa_decode partition_size (default: the workload's)")
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="shrink the workload to this many sequences (profiling cases)")
     ap.add_argument("--flush-l2", action="store_true",
                     help="write a 512 MB buffer between timed steps (outside the events)")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
@@ -185,9 +187,10 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside)}
 
 
-def make_workload(config: str, device):
+def make_workload(config: str, device, num_seqs=None):
     from paged_kv_cache_119_gb300 import workloads
-    return workloads.make(config, device=device)
+    kw = {} if num_seqs is None else {"num_seqs": num_seqs}
+    return workloads.make(config, device=device, **kw)
 
 
 # ------------------------------------------------------------------------------ our arm
@@ -201,7 +204,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pa_build.build()
-    w = make_workload(args.config, dev)
+    w = make_workload(args.config, dev, args.num_seqs)
     part = w.partition_size if args.partition_size is None else args.partition_size
     nbytes = algorithmic_bytes(w)
     out = torch.empty(w.num_seqs, w.num_q_heads, w.head_dim, dtype=w.dtype, device=dev)
@@ -416,7 +419,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     import oracle
-    w = make_workload(args.config, "cpu")
+    w = make_workload(args.config, "cpu", args.num_seqs)
     h = _host_inputs(w)
     threads = oracle.max_threads()
     # a bounded sample: enough sequences for ~0.5 s of oracle work per step
