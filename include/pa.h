@@ -119,6 +119,41 @@ int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
               void* stream);
 
 /*
+ * Bytes of the static device scratch pa_decode_noalloc uses (32 MiB).  Every GPU
+ * that loads the library's no-alloc module keeps this much device memory until
+ * the process exits.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * pa_decode_noalloc -- the split-context pa_decode with its scratch in a fixed
+ * static device array (PA_NOALLOC_SCRATCH_BYTES) instead of a caller workspace.
+ * The pages have no counterpart: this entry point exists for callers that cannot
+ * allocate device memory on the decode path, such as a plugin whose host runtime
+ * owns all device memory and forbids cudaMalloc in its enqueue hook, or a C caller
+ * with no allocator.  The caller still owns and passes every input and the output.
+ *
+ * Arguments, layout and results are those of pa_decode, minus the workspace.
+ * partition_size: 0 = 512 tokens, > 0 = that many (a multiple of block_size),
+ * < 0 is rejected (PA_ERR_INVALID): this entry point always splits.
+ * Returns PA_ERR_WORKSPACE, launching nothing, when the split needs more than
+ * PA_NOALLOC_SCRATCH_BYTES (pa_decode_workspace_bytes gives the need).
+ * Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ * The first call on each device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.
+ * All calls share the one array, so calls that overlap on the GPU (say, on two
+ * streams) race and corrupt each other's results; serialise them.  The array
+ * keeps the last call's contents; nothing in it needs to start at zero, because
+ * each call writes every partial it reads.
+ */
+int pa_decode_noalloc(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
+                      const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
+                      const int32_t* block_tables, int64_t block_table_stride,
+                      const int32_t* context_lens, int32_t max_context_len, int32_t num_seqs,
+                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, float scale, int32_t partition_size, void* stream);
+
+/*
  * Cache write: for each token i < num_tokens with slot = slot_mapping[i] >= 0 and
  * each kv head h, k_cache[slot / B][h][slot % B][:] = k[i][h][:] and likewise for v.
  * A bit-exact copy.  k, v, k_cache, v_cache: device, 16-byte aligned;

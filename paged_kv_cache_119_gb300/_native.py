@@ -14,6 +14,7 @@ _lib = None
 PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0, -1, -2, -3, -4
 PA_DEVERR_BLOCK_ID, PA_DEVERR_CONTEXT_LEN, PA_DEVERR_SLOT, PA_DEVERR_TIMEOUT = 1, 2, 4, 8
+PA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 # Every symbol include/pa.h declares, with (restype, argtypes).
 _i32, _i64, _sz, _vp, _f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, \
@@ -23,6 +24,9 @@ SIGNATURES = {
     "pa_decode": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp, _vp, ctypes.c_int, _i64, _vp, _i64,
                                  _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp, _sz,
                                  _vp]),
+    "pa_decode_noalloc": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp, _vp, ctypes.c_int, _i64, _vp,
+                                         _i64, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32,
+                                         _i32, _vp]),
     "pa_reshape_and_cache": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i64,
                                             ctypes.c_int, _vp]),
     "pa_copy_blocks": (ctypes.c_int, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32,

@@ -96,6 +96,35 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
     return out
 
 
+def pa_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, block_tables: torch.Tensor,
+                      context_lens: torch.Tensor, scale: float, num_kv_heads: int,
+                      block_size: int, max_context_len: int | None = None,
+                      partition_size: int = 0, stream=None) -> torch.Tensor:
+    """pa_decode's split path with its scratch in the library's static device array
+    (no workspace argument, nothing allocated).  For callers that cannot allocate
+    device memory on the decode path.  Calls overlapping on the GPU share that one
+    array and race; the first call on a device looks up its address, so make it
+    before any stream capture."""
+    for name, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                    ("block_tables", block_tables), ("context_lens", context_lens)):
+        _cuda(name, t)
+    if q.dim() != 3 or out.shape != q.shape or k_cache.dim() != 4:
+        raise ValueError("q and out must be [S, Hq, D]; caches [N, Hkv, B, D]")
+    S, Hq, D = q.shape
+    if max_context_len is None:
+        max_context_len = block_tables.shape[1] * block_size
+    status = N.load().pa_decode_noalloc(out.data_ptr(), _dtype(out), q.data_ptr(),
+                                        k_cache.data_ptr(), v_cache.data_ptr(), _dtype(q),
+                                        k_cache.shape[0], block_tables.data_ptr(),
+                                        block_tables.stride(0), context_lens.data_ptr(),
+                                        int(max_context_len), S, Hq, num_kv_heads, D,
+                                        block_size, float(scale), int(partition_size),
+                                        _stream(stream))
+    N.check("pa_decode_noalloc", status)
+    return out
+
+
 def pa_reshape_and_cache(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
                          v_cache: torch.Tensor, slot_mapping: torch.Tensor,
                          stream=None) -> None:

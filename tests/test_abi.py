@@ -142,3 +142,13 @@ def test_binding_refuses_cpu_tensors(lib):
         P.pa_decode(x, x, torch.zeros(1, 4, 16, 64), torch.zeros(1, 4, 16, 64),
                     torch.zeros(2, 1, dtype=torch.int32), torch.zeros(2, dtype=torch.int32),
                     0.125, 4, 16)
+
+
+def test_noalloc_rejects_oversized_and_unsplit_requests(lib):
+    # the size and partition checks happen before any CUDA call
+    args = decode_args(max_ctx=32768, S=64, Hq=64, Hkv=8, bt_stride=2048, part=512)
+    del args[18:20]                           # pa_decode_noalloc has no workspace arguments
+    assert lib.pa_decode_noalloc(*args) == N.PA_ERR_WORKSPACE
+    args = decode_args(part=-1)
+    del args[18:20]
+    assert lib.pa_decode_noalloc(*args) == N.PA_ERR_INVALID
