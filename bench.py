@@ -47,7 +47,7 @@ WORKLOADS = {
 DTYPE_NAME = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}
 METRIC = "paged decode attention KV GB/s"
 KERNEL_SRC = os.path.join(ROOT, "paged_kv_cache_119_gb300", "csrc", "decode_kernel.cuh")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.md")
 
 
 def parse_args(argv=None):
@@ -111,16 +111,21 @@ def kernel_hash() -> str:
 
 
 def recorded_traffic(config: str):
-    """ncu DRAM bytes per decode launch, if recorded for the current kernel source."""
+    """ncu DRAM bytes per decode launch, if recorded for the current kernel source
+    (a row of the markdown table in profiles/decode_traffic.md)."""
     try:
-        with open(TRAFFIC_FILE) as f:
-            rec = json.load(f)
-    except (OSError, ValueError):
+        with open(TRAFFIC_FILE, encoding="utf-8") as f:
+            lines = f.read().splitlines()
+    except OSError:
         return None
-    ent = rec.get(config)
-    if not ent or ent.get("kernel_hash") != kernel_hash():
-        return None
-    return ent.get("dram_bytes_per_launch")
+    for line in lines:
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 3 and cells[0] == config and cells[1] == kernel_hash():
+            try:
+                return int(cells[2])
+            except ValueError:
+                return None
+    return None
 
 
 def algorithmic_bytes(w) -> dict:
