@@ -1,0 +1,506 @@
+// decode_mma.cuh -- paged decode attention for grouped-query heads on the tensor
+// cores (sm_103a), fp16/bf16 caches.
+//
+// Same result as decode_kernel (the block-wise attention of "PagedAttention
+// 完全拆解", section 原理详解（二）, evaluated with a running max), organised for
+// GQA: one CTA serves NH (4 or 8) query heads that share a kv head, so a K/V tile
+// is read once for all of them and q.K^T, P.V become small dense contractions
+// (4 multiply-adds per K/V byte at group 8, more than the CUDA cores sustain at
+// HBM speed).
+//
+//   * Producer warp: per tile, D/64 tensor-map TMA copies of K and of V
+//     (cp.async.bulk.tensor, box = 64 dims x B tokens, 128-byte swizzle) into an
+//     mbarrier ring; the tensor map's third coordinate is block * Hkv + kv head,
+//     so the block-table entry is the only address input.
+//   * Consumer warps (tile i -> warp i % 4, each stage owned by one warp):
+//       S^T[16 tok x 8 heads] = K[16 x D] . Q^T  -- mma.sync m16n8k16, K from
+//         ldmatrix on the swizzled tile, Q^T fragments held in registers;
+//       running max / sum per head in fp32 (base 2);
+//       P^T is split into hi + lo halves of the cache dtype (P = hi + lo to
+//         ~2^-16 relative), and each 8x8 block is transposed in registers with
+//         movmatrix into the B operand of the second product;
+//       O^T[D x 8 heads] += V^T . P^T  -- mma.sync, V^T from ldmatrix.trans.
+//   * Tokens past the context in the last tile: scores become -inf by select,
+//     and their V fragments are zeroed before the product (unused slots may
+//     hold NaN, and 0 * NaN is NaN).
+//   * Warps merge through shared memory (reusing the ring) in a fixed order.
+#pragma once
+
+#include <cuda.h>
+
+#include "decode_kernel.cuh"
+
+namespace pa {
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 3-D tensor-map TMA load (x = head dim, y = token in block, z = block*Hkv + head).
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)),
+        "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+template <typename T>
+struct Mma;
+
+template <>
+struct Mma<__nv_bfloat16> {
+    __device__ __forceinline__ static void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1)
+    {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    // packs (lo, hi) into one 32-bit register, rounding to nearest even
+    __device__ __forceinline__ static uint32_t pack(float lo, float hi)
+    {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+    __device__ __forceinline__ static float2 unpack(uint32_t w)
+    {
+        return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w));
+    }
+};
+
+template <>
+struct Mma<__half> {
+    __device__ __forceinline__ static void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1)
+    {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    __device__ __forceinline__ static uint32_t pack(float lo, float hi)
+    {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+    __device__ __forceinline__ static float2 unpack(uint32_t w)
+    {
+        return __half22float2(*reinterpret_cast<__half2*>(&w));
+    }
+};
+
+template <typename T, int D, int BS, int NSTAGE>
+struct MmaSmem {
+    static constexpr int kHalfBytes = BS * 128;                // one 64-dim box: B rows x 128 B
+    static constexpr int kTileBytes = (D / 64) * kHalfBytes;   // K (or V) of one block
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kRingBytes = NSTAGE * kStageBytes;
+    static constexpr int kBarOffset = kRingBytes;
+    static constexpr int kOkOffset = kBarOffset + 2 * NSTAGE * 8;
+    static constexpr int kFlagOffset = kOkOffset + NSTAGE * 4;
+    static constexpr int kBytes = kFlagOffset + 16;
+    static constexpr int kAlloc = kBytes + 1024;                 // room to align the ring to 1 KB
+    // merge area, aliased onto the ring once every tile is consumed
+    static constexpr int kMergeAcc = kDecodeConsumerWarps * 8 * D * 4;
+    static constexpr int kMergeBytes = kMergeAcc + kDecodeConsumerWarps * 8 * 2 * 4;
+    static_assert(kMergeBytes <= kRingBytes, "merge area must fit in the ring");
+    static_assert(kHalfBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
+};
+
+template <typename T, int D, int BS, int NH, int NSTAGE>
+__global__ void __launch_bounds__(kDecodeThreads)
+    decode_mma_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tk,
+                      const __grid_constant__ CUtensorMap tv)
+{
+    using Sm = MmaSmem<T, D, BS, NSTAGE>;
+    constexpr int NCW = kDecodeConsumerWarps;
+    constexpr int KS = D / 16;        // k-steps of the score product / m-blocks of P.V
+    constexpr int MB = BS / 16;       // 16-token row blocks per tile
+    static_assert(NH == 4 || NH == 8, "4 or 8 query heads per CTA");
+    static_assert(NSTAGE % NCW == 0, "each ring stage must belong to one consumer warp");
+    static_assert(BS % 16 == 0 && D % 64 == 0, "block_size 16/32, head_dim 64/128");
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sm::kBarOffset);
+    uint64_t* empty = full + NSTAGE;
+    int* stage_ok = reinterpret_cast<int*>(smem + Sm::kOkOffset);
+    int* poison = reinterpret_cast<int*>(smem + Sm::kFlagOffset);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int seq = blockIdx.z;
+    const int kvh = blockIdx.y / p.chunks;
+    const int h0 = kvh * p.group + (blockIdx.y % p.chunks) * NH;
+    const int part = blockIdx.x;
+    const bool split = p.partition_tokens > 0;
+
+    const int L = p.context_lens[seq];
+    if (L < 0 || L > p.max_context_len) {
+        if (part == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+            atomicOr(p.err, PA_DEVERR_CONTEXT_LEN);
+        if (!split) {
+            for (int idx = threadIdx.x; idx < NH * D; idx += blockDim.x)
+                store_out<T>(p, ((int64_t)seq * p.num_q_heads + h0) * D + idx,
+                             __int_as_float(0x7fc00000));
+        }
+        return;
+    }
+    int t0 = 0, t1 = L;
+    if (split) {
+        t0 = part * p.partition_tokens;
+        if (t0 >= L)
+            return;
+        t1 = min(L, t0 + p.partition_tokens);
+    }
+    const int jb = t0 / BS;
+    const int ntiles = (t1 > t0) ? (t1 + BS - 1) / BS - jb : 0;
+
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        *poison = 0;
+        fence_mbar_init();
+    }
+    if (warp == NCW && lane == 0) {
+        prefetch_tensormap(&tk);
+        prefetch_tensormap(&tv);
+    }
+    __syncthreads();
+
+    if (warp == NCW) {
+        // ------------------------------------------------------------------ producer
+        const int32_t* bt_row = p.block_tables + (int64_t)seq * p.bt_stride + jb;
+        const uint64_t policy = l2_evict_first_policy();
+        int next = (lane < ntiles) ? __ldg(bt_row + lane) : 0;
+        bool aborted = false;
+        for (int base = 0; base < ntiles && !aborted; base += 32) {
+            const int cur = next;
+            if (base + 32 + lane < ntiles)
+                next = __ldg(bt_row + base + 32 + lane);
+            const int cnt = min(32, ntiles - base);
+            for (int i = 0; i < cnt; ++i) {
+                const int pbn = __shfl_sync(kFullMask, cur, i);
+                const int it = base + i;
+                const int stage = it % NSTAGE;
+                int ok = 1;
+                if (lane == 0) {
+                    if (it >= NSTAGE && !mbar_wait(&empty[stage], ((it / NSTAGE) - 1) & 1)) {
+                        atomicOr(p.err, PA_DEVERR_TIMEOUT);
+                        ok = 0;
+                    }
+                    if (ok) {
+                        const bool valid = pbn >= 0 && (int64_t)pbn < p.num_blocks;
+                        stage_ok[stage] = valid ? 1 : 0;
+                        if (valid) {
+                            unsigned char* dst = smem + stage * Sm::kStageBytes;
+                            const int z = pbn * p.num_kv_heads + kvh;   // < 2^31: N * Hkv rows of tiles
+                            mbar_arrive_expect_tx(&full[stage], Sm::kStageBytes);
+#pragma unroll
+                            for (int h = 0; h < D / 64; ++h) {
+                                tma_load_3d(dst + h * Sm::kHalfBytes, &tk, 64 * h, 0, z, &full[stage],
+                                            policy);
+                                tma_load_3d(dst + Sm::kTileBytes + h * Sm::kHalfBytes, &tv, 64 * h, 0,
+                                            z, &full[stage], policy);
+                            }
+                        } else {
+                            atomicOr(p.err, PA_DEVERR_BLOCK_ID);
+                            mbar_arrive(&full[stage]);
+                        }
+                    }
+                }
+                if (!__shfl_sync(kFullMask, ok, 0)) {
+                    aborted = true;
+                    break;
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------------- consumers
+    const int g = lane >> 2;          // fragment row group
+    const int c = lane & 3;           // fragment column pair
+    // Q^T fragments: b0 = q[head g][16ks + 2c, +1], b1 = q[head g][16ks + 2c + 8, +9]
+    uint32_t qb[KS][2];
+    {
+        const bool live = g < NH;
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+            reinterpret_cast<const T*>(p.q) + ((int64_t)seq * p.num_q_heads + h0 + (live ? g : 0)) * D);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            qb[ks][0] = live ? __ldg(qrow + (16 * ks + 2 * c) / 2) : 0u;
+            qb[ks][1] = live ? __ldg(qrow + (16 * ks + 2 * c + 8) / 2) : 0u;
+        }
+    }
+    // per-thread statistics for heads 2c and 2c+1 (base-2 units)
+    float m[2] = {-INFINITY, -INFINITY};
+    float lsum[2] = {0.f, 0.f};
+    float o[KS][4];                   // O^T fragments: (d = 16mb + g (+8), heads 2c, 2c+1)
+#pragma unroll
+    for (int i = 0; i < KS; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            o[i][j] = 0.f;
+    bool poisoned = false;
+    const float sl2 = p.scale_log2;
+
+    for (int it = warp; it < ntiles; it += NCW) {
+        const int stage = it % NSTAGE;
+        if (!mbar_wait(&full[stage], (it / NSTAGE) & 1)) {
+            if (lane == 0)
+                atomicOr(p.err, PA_DEVERR_TIMEOUT);
+            poisoned = true;
+            break;
+        }
+        if (!stage_ok[stage]) {
+            poisoned = true;
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[stage]);
+            continue;
+        }
+        const uint32_t kbase = smem_addr(smem + stage * Sm::kStageBytes);
+        const uint32_t vbase = kbase + Sm::kTileBytes;
+        const int nvalid = min(BS, t1 - (jb + it) * BS);
+
+#pragma unroll
+        for (int mb = 0; mb < MB; ++mb) {
+            if (16 * mb >= nvalid)
+                break;                         // the rest of the tile lies past the context
+            // ---- S^T = K . Q^T for tokens 16mb .. 16mb+15
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+                const int r = 16 * mb + (lane & 7) + 8 * ((lane >> 3) & 1);   // token row
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int chunk = 2 * ks + (lane >> 4);                   // 16-byte column
+                    const uint32_t addr = kbase + (chunk >> 3) * Sm::kHalfBytes + r * 128 +
+                                          (((chunk & 7) ^ (r & 7)) << 4);
+                    uint32_t a[4];
+                    ldsm_x4(addr, a);
+                    Mma<T>::run(s, a, qb[ks][0], qb[ks][1]);
+                }
+            }
+            // ---- online softmax: s[0], s[1] = token 16mb+g; s[2], s[3] = token 16mb+g+8
+            const int tok_a = 16 * mb + g, tok_b = tok_a + 8;
+            float x[4];
+            x[0] = tok_a < nvalid ? s[0] * sl2 : -INFINITY;
+            x[1] = tok_a < nvalid ? s[1] * sl2 : -INFINITY;
+            x[2] = tok_b < nvalid ? s[2] * sl2 : -INFINITY;
+            x[3] = tok_b < nvalid ? s[3] * sl2 : -INFINITY;
+            float alpha[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float tmax = fmaxf(x[j], x[j + 2]);
+                tmax = fmaxf(tmax, __shfl_xor_sync(kFullMask, tmax, 4));
+                tmax = fmaxf(tmax, __shfl_xor_sync(kFullMask, tmax, 8));
+                tmax = fmaxf(tmax, __shfl_xor_sync(kFullMask, tmax, 16));
+                const float mnew = fmaxf(m[j], tmax);       // -inf only for padded heads
+                alpha[j] = (mnew == -INFINITY) ? 1.f : exp2f(m[j] - mnew);
+                m[j] = mnew;
+                const float pa = (mnew == -INFINITY) ? 0.f : exp2f(x[j] - mnew);
+                const float pb = (mnew == -INFINITY) ? 0.f : exp2f(x[j + 2] - mnew);
+                x[j] = pa;
+                x[j + 2] = pb;
+                lsum[j] = fmaf(lsum[j], alpha[j], pa + pb);
+            }
+#pragma unroll
+            for (int i = 0; i < KS; ++i) {
+                o[i][0] *= alpha[0];
+                o[i][1] *= alpha[1];
+                o[i][2] *= alpha[0];
+                o[i][3] *= alpha[1];
+            }
+            // ---- P^T (hi + lo) into B fragments: transpose each 8x8 block in registers
+            const uint32_t hi_a = Mma<T>::pack(x[0], x[1]);
+            const uint32_t hi_b = Mma<T>::pack(x[2], x[3]);
+            const float2 fa = Mma<T>::unpack(hi_a), fb = Mma<T>::unpack(hi_b);
+            const uint32_t lo_a = Mma<T>::pack(x[0] - fa.x, x[1] - fa.y);
+            const uint32_t lo_b = Mma<T>::pack(x[2] - fb.x, x[3] - fb.y);
+            const uint32_t bh0 = movmatrix_trans(hi_a), bh1 = movmatrix_trans(hi_b);
+            const uint32_t bl0 = movmatrix_trans(lo_a), bl1 = movmatrix_trans(lo_b);
+            // ---- O^T += V^T . P^T over tokens 16mb .. 16mb+15
+            const int vr = 16 * mb + (lane & 7) + 8 * (lane >> 4);            // token row
+            const bool ragged = nvalid < 16 * (mb + 1);
+#pragma unroll
+            for (int i = 0; i < KS; ++i) {
+                const int chunk = 2 * i + ((lane >> 3) & 1);
+                const uint32_t addr = vbase + (chunk >> 3) * Sm::kHalfBytes + vr * 128 +
+                                      (((chunk & 7) ^ (vr & 7)) << 4);
+                uint32_t a[4];
+                ldsm_x4_trans(addr, a);
+                if (ragged) {
+                    // a0, a1 hold tokens 16mb + 2c, +1; a2, a3 tokens 16mb + 2c + 8, +9
+                    const int t = 16 * mb + 2 * c;
+                    const uint32_t m01 = (t < nvalid ? 0x0000ffffu : 0u) | (t + 1 < nvalid ? 0xffff0000u : 0u);
+                    const uint32_t m23 = (t + 8 < nvalid ? 0x0000ffffu : 0u) |
+                                         (t + 9 < nvalid ? 0xffff0000u : 0u);
+                    a[0] &= m01;
+                    a[1] &= m01;
+                    a[2] &= m23;
+                    a[3] &= m23;
+                }
+                Mma<T>::run(o[i], a, bh0, bh1);
+                Mma<T>::run(o[i], a, bl0, bl1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[stage]);
+    }
+
+    // ------------------------------------------------------------- merge the warps
+    named_barrier(1, NCW * 32);            // every tile consumed: the ring is free
+    float* mrg_acc = reinterpret_cast<float*>(smem);                    // [NCW][8][D]
+    float* mrg_ml = mrg_acc + NCW * 8 * D;                               // [NCW][8][2]
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        float l = lsum[j];
+        l += __shfl_xor_sync(kFullMask, l, 4);
+        l += __shfl_xor_sync(kFullMask, l, 8);
+        l += __shfl_xor_sync(kFullMask, l, 16);
+        if (g == 0) {
+            mrg_ml[(warp * 8 + 2 * c + j) * 2 + 0] = m[j];
+            mrg_ml[(warp * 8 + 2 * c + j) * 2 + 1] = l;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < KS; ++i) {
+        const int d = 16 * i + g;
+        mrg_acc[(warp * 8 + 2 * c) * D + d] = o[i][0];
+        mrg_acc[(warp * 8 + 2 * c + 1) * D + d] = o[i][1];
+        mrg_acc[(warp * 8 + 2 * c) * D + d + 8] = o[i][2];
+        mrg_acc[(warp * 8 + 2 * c + 1) * D + d + 8] = o[i][3];
+    }
+    if (poisoned)
+        *poison = 1;
+    named_barrier(1, NCW * 32);
+
+    const bool bad = *poison != 0;
+    for (int idx = threadIdx.x; idx < NH * D; idx += NCW * 32) {
+        const int h = idx / D;
+        const int d = idx - h * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w)
+            M = fmaxf(M, mrg_ml[(w * 8 + h) * 2]);
+        float num = 0.f, den = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NCW; ++w) {
+                const float cw = exp2f(mrg_ml[(w * 8 + h) * 2] - M);
+                num = fmaf(cw, mrg_acc[(w * 8 + h) * D + d], num);
+                den = fmaf(cw, mrg_ml[(w * 8 + h) * 2 + 1], den);
+            }
+        }
+        float out = den > 0.f ? num / den : 0.f;
+        if (bad)
+            out = __int_as_float(0x7fc00000);
+        const int64_t row = (int64_t)seq * p.num_q_heads + h0 + h;
+        if (split) {
+            const int64_t prow = row * p.max_parts + part;
+            p.part_o[prow * D + d] = out;
+            if (d == 0) {
+                p.part_ml[prow * 2 + 0] = M;
+                p.part_ml[prow * 2 + 1] = den;
+            }
+        } else {
+            store_out<T>(p, row * D + d, out);
+        }
+    }
+}
+
+// Ring depth of the tensor-core kernel: one or two stages per consumer warp.
+template <typename T, int D, int BS>
+struct MmaStages {
+    static constexpr int kStageBytes = 2 * (D / 64) * BS * 128;
+    static constexpr int value = kDecodeConsumerWarps * (kStageBytes <= 8192 ? 2 : 1);
+};
+
+template <typename T, int D, int BS, int NH>
+cudaError_t launch_decode_mma_variant(const DecodeParams& p, const CUtensorMap& tk,
+                                      const CUtensorMap& tv, cudaStream_t stream)
+{
+    constexpr int NSTAGE = MmaStages<T, D, BS>::value;
+    using Sm = MmaSmem<T, D, BS, NSTAGE>;
+    auto kern = decode_mma_kernel<T, D, BS, NH, NSTAGE>;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    if (configured_device != dev) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::kAlloc);
+        if (err != cudaSuccess)
+            return err;
+        configured_device = dev;
+    }
+    const bool split = p.partition_tokens > 0;
+    dim3 grid(split ? p.max_parts : 1, p.num_kv_heads * p.chunks, p.num_seqs);
+    kern<<<grid, kDecodeThreads, Sm::kAlloc, stream>>>(p, tk, tv);
+    err = cudaGetLastError();
+    if (err != cudaSuccess || !split)
+        return err;
+    reduce_kernel<T, D><<<dim3(p.num_q_heads, p.num_seqs), D, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// Tensor-core path for 16-bit caches with 4 or 8 query heads per CTA.
+template <typename T>
+cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, int block_size, int gc,
+                              cudaStream_t stream)
+{
+    CUtensorMap tk, tv;
+    cudaError_t e = kv_tensor_map(&tk, p.k_cache, p.num_blocks, p.num_kv_heads, block_size,
+                                  head_dim, DType<T>::id);
+    if (e == cudaSuccess)
+        e = kv_tensor_map(&tv, p.v_cache, p.num_blocks, p.num_kv_heads, block_size, head_dim,
+                          DType<T>::id);
+    if (e != cudaSuccess)
+        return e;
+#define PA_MMA_CASE(D_, BS_, NH_)                                         \
+    if (head_dim == D_ && block_size == BS_ && gc == NH_)                 \
+        return launch_decode_mma_variant<T, D_, BS_, NH_>(p, tk, tv, stream);
+    PA_MMA_CASE(128, 16, 8) PA_MMA_CASE(128, 16, 4)
+    PA_MMA_CASE(128, 32, 8) PA_MMA_CASE(128, 32, 4)
+    PA_MMA_CASE(64, 16, 8) PA_MMA_CASE(64, 16, 4)
+    PA_MMA_CASE(64, 32, 8) PA_MMA_CASE(64, 32, 4)
+#undef PA_MMA_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

@@ -4,6 +4,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 #include <vector>
 
 #include <cuda_runtime.h>
@@ -72,6 +73,85 @@ size_t workspace_layout(int64_t rows, int max_parts, int head_dim, size_t* ml_of
 }
 
 }  // namespace
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn()
+{
+    static EncodeTiledFn fn = [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            ptr = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(ptr);
+    }();
+    return fn;
+}
+
+struct MapKey {
+    const void* base;
+    int64_t num_blocks;
+    int num_kv_heads, block_size, head_dim, dtype;
+    bool operator==(const MapKey& o) const
+    {
+        return base == o.base && num_blocks == o.num_blocks && num_kv_heads == o.num_kv_heads &&
+               block_size == o.block_size && head_dim == o.head_dim && dtype == o.dtype;
+    }
+};
+
+constexpr int kMapCache = 16;
+struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+    bool used;
+};
+MapEntry g_map_cache[kMapCache];
+int g_map_next = 0;
+std::mutex g_map_mutex;
+
+}  // namespace
+
+cudaError_t kv_tensor_map(CUtensorMap* map, const void* base, int64_t num_blocks, int num_kv_heads,
+                          int block_size, int head_dim, pa_dtype dtype)
+{
+    const MapKey key{base, num_blocks, num_kv_heads, block_size, head_dim, (int)dtype};
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    for (const MapEntry& e : g_map_cache)
+        if (e.used && e.key == key) {
+            *map = e.map;
+            return cudaSuccess;
+        }
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn || elem_size(dtype) != 2)
+        return cudaErrorNotSupported;
+    if (num_blocks * (int64_t)num_kv_heads >= (int64_t(1) << 31))
+        return cudaErrorInvalidValue;           // the TMA z coordinate is a signed 32-bit int
+    const cuuint64_t esz = 2;
+    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)block_size,
+                                (cuuint64_t)num_blocks * (cuuint64_t)num_kv_heads};
+    const cuuint64_t strides[2] = {head_dim * esz, (cuuint64_t)block_size * head_dim * esz};
+    const cuuint32_t box[3] = {64, (cuuint32_t)block_size, 1};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    CUtensorMap m;
+    const CUresult r = fn(&m, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          3, const_cast<void*>(base), dims, strides, box, estride,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    g_map_cache[g_map_next] = MapEntry{key, m, true};
+    g_map_next = (g_map_next + 1) % kMapCache;
+    *map = m;
+    return cudaSuccess;
+}
 
 unsigned* device_error_word()
 {

@@ -2,6 +2,7 @@
 // (kernel parameter blocks and per-dtype launchers).  Not part of the C ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -77,6 +78,13 @@ struct CopyParams {
     int num_pairs;
 };
 cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);
+
+// Tensor map over a [num_blocks][num_kv_heads][block_size][head_dim] cache of a
+// 16-bit dtype, as 3-D (head_dim, block_size, num_blocks * num_kv_heads) with a
+// box of 64 dims x block_size tokens and 128-byte swizzle.  Encoded maps are
+// cached per (base, shape, dtype).
+cudaError_t kv_tensor_map(CUtensorMap* map, const void* base, int64_t num_blocks, int num_kv_heads,
+                          int block_size, int head_dim, pa_dtype dtype);
 
 // The calling device's error word (device address), or nullptr on failure.
 unsigned* device_error_word();

@@ -3,7 +3,7 @@
 Cache writes and block copies must match bit for bit (whole pools compared as
 raw bytes, NaN fill included).  Attention written as fp32 must be within
 2e-3 max abs error of the fp64 oracle; written in the cache dtype it must be
-within one unit in the last place of the correctly rounded oracle value.
+the round-to-nearest-even of a value within 5e-5 of the oracle.
 """
 import math
 
@@ -70,25 +70,25 @@ def oracle_step(w, snap):
     return out, kc, vc
 
 
-def ulp(x: np.ndarray, dtype: torch.dtype) -> np.ndarray:
-    """Spacing of the dtype's representable numbers at |x| (normal range)."""
-    mant = {torch.bfloat16: 7, torch.float16: 10, torch.float32: 23}[dtype]
-    tiny = {torch.bfloat16: 2.0 ** -126, torch.float16: 2.0 ** -14, torch.float32: 2.0 ** -126}
-    e = np.floor(np.log2(np.maximum(np.abs(x), tiny[dtype])))
-    return 2.0 ** (e - mant)
+NATIVE_EPS = 5e-5    # native-dtype output: the rounding of a value within this of the oracle
 
 
 def check_attention(out_gpu, ref, dtype):
+    """fp32 output: max abs error <= ATOL.  Native fp16/bf16 output: each value is the
+    round-to-nearest-even of some y with |y - ref| <= NATIVE_EPS; rounding is monotone,
+    so that is RNE(ref - eps) <= out <= RNE(ref + eps) elementwise."""
     got = out_gpu.double().cpu().numpy()
     assert np.isfinite(got).all(), "non-finite output"
     if out_gpu.dtype == torch.float32:
         err = np.abs(got - ref).max()
         assert err <= ATOL, f"max abs error {err:.3e} > {ATOL}"
         return err
-    rounded = torch.from_numpy(ref).to(out_gpu.dtype).double().numpy()
-    dev = np.abs(got - rounded)
-    assert (dev <= ulp(ref, out_gpu.dtype) * 1.0001).all(), f"max deviation {dev.max():.3e}"
-    return dev.max()
+    lo = torch.from_numpy((ref - NATIVE_EPS).astype(np.float32)).to(out_gpu.dtype).double().numpy()
+    hi = torch.from_numpy((ref + NATIVE_EPS).astype(np.float32)).to(out_gpu.dtype).double().numpy()
+    bad = (got < lo) | (got > hi)
+    assert not bad.any(), (f"{int(bad.sum())} values are not a rounding of the oracle "
+                           f"within {NATIVE_EPS}: e.g. got {got[bad][:4]}, ref {ref[bad][:4]}")
+    return np.abs(got - ref).max()
 
 
 def run_and_compare(w, out_dtype=torch.float32, partition_size=None):
