@@ -58,7 +58,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", choices=sorted(WORKLOADS), default="llama13b")
     ap.add_argument("--partition-size", type=int, default=None,
-                    help="pa_decode partition_size (default: the workload's)")
+                    help="pa_decode partition_size (default 0: the library's automatic split)")
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="shrink the workload to this many sequences (profiling cases)")
     ap.add_argument("--flush-l2", action="store_true",
@@ -210,7 +210,7 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     pa_build.build()
     w = make_workload(args.config, dev, args.num_seqs)
-    part = w.partition_size if args.partition_size is None else args.partition_size
+    part = 0 if args.partition_size is None else args.partition_size
     nbytes = algorithmic_bytes(w)
     out = torch.empty(w.num_seqs, w.num_q_heads, w.head_dim, dtype=w.dtype, device=dev)
     ws_bytes = pa.pa_decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.head_dim,

@@ -13,4 +13,11 @@ cudaError_t launch_decode_f16(const DecodeParams& p, int head_dim, int block_siz
     return launch_decode_typed<__half>(p, head_dim, block_size, gc, stream);
 }
 
+int occupancy_decode_f16(int head_dim, int block_size, int gc)
+{
+    if (gc >= 4)
+        return occupancy_decode_mma<__half>(head_dim, block_size, gc);
+    return occupancy_decode_typed<__half>(head_dim, block_size, gc);
+}
+
 }  // namespace pa

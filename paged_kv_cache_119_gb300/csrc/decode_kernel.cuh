@@ -37,6 +37,10 @@
 
 #include <math.h>
 
+#include <mutex>
+#include <utility>
+#include <vector>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -449,49 +453,91 @@ struct DecodeStages {
         kDecodeConsumerWarps * (kPerWarp < 1 ? 1 : (kPerWarp > 3 ? 3 : kPerWarp));
 };
 
-template <typename T, int D, int BS, int GC>
-cudaError_t launch_decode_variant(const DecodeParams& p, cudaStream_t stream)
+// Sets the dynamic shared-memory limit of a kernel once per device and process.
+inline cudaError_t configure_once(const void* kernel, int smem_bytes)
 {
-    constexpr int NSTAGE = DecodeStages<T, D, BS>::value;
-    using Smem = DecodeSmem<T, D, BS, GC, NSTAGE>;
-    auto kern = decode_kernel<T, D, BS, GC, NSTAGE>;
-    static int configured_device = -1;      // dynamic smem opt-in, once per device
+    static std::mutex mu;
+    static std::vector<std::pair<const void*, int>> done;   // (kernel, device)
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
         return err;
-    if (configured_device != dev) {
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem::kBytes);
+    std::lock_guard<std::mutex> lock(mu);
+    for (const auto& d : done)
+        if (d.first == kernel && d.second == dev)
+            return cudaSuccess;
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (err == cudaSuccess)
+        done.emplace_back(kernel, dev);
+    return err;
+}
+
+// Resident CTAs per SM for a decode kernel with this dynamic shared memory.
+inline int kernel_occupancy(const void* kernel, int smem_bytes)
+{
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kDecodeThreads, smem_bytes) !=
+        cudaSuccess)
+        return 0;
+    return n;
+}
+
+template <typename T, int D, int BS, int GC>
+struct CoreVariant {
+    static constexpr int kStages = DecodeStages<T, D, BS>::value;
+    using Smem = DecodeSmem<T, D, BS, GC, kStages>;
+    static constexpr auto kernel() { return decode_kernel<T, D, BS, GC, kStages>; }
+    static cudaError_t configure()
+    {
+        return configure_once(reinterpret_cast<const void*>(kernel()), Smem::kBytes);
+    }
+    static cudaError_t launch(const DecodeParams& p, cudaStream_t stream)
+    {
+        cudaError_t err = configure();
         if (err != cudaSuccess)
             return err;
-        configured_device = dev;
+        const bool split = p.partition_tokens > 0;
+        dim3 grid(split ? p.max_parts : 1, p.num_kv_heads * p.chunks, p.num_seqs);
+        kernel()<<<grid, kDecodeThreads, Smem::kBytes, stream>>>(p);
+        err = cudaGetLastError();
+        if (err != cudaSuccess || !split)
+            return err;
+        reduce_kernel<T, D><<<dim3(p.num_q_heads, p.num_seqs), D, 0, stream>>>(p);
+        return cudaGetLastError();
     }
-    const bool split = p.partition_tokens > 0;
-    dim3 grid(split ? p.max_parts : 1, p.num_kv_heads * p.chunks, p.num_seqs);
-    kern<<<grid, kDecodeThreads, Smem::kBytes, stream>>>(p);
-    err = cudaGetLastError();
-    if (err != cudaSuccess || !split)
-        return err;
-    reduce_kernel<T, D><<<dim3(p.num_q_heads, p.num_seqs), D, 0, stream>>>(p);
-    return cudaGetLastError();
-}
+};
+
+#define PA_CORE_VARIANTS(X)                                                              \
+    X(128, 16, 1) X(128, 16, 2) X(128, 16, 4) X(128, 16, 8) X(128, 32, 1) X(128, 32, 2) \
+    X(128, 32, 4) X(128, 32, 8) X(64, 16, 1) X(64, 16, 2) X(64, 16, 4) X(64, 16, 8)     \
+    X(64, 32, 1) X(64, 32, 2) X(64, 32, 4) X(64, 32, 8)
 
 template <typename T>
 cudaError_t launch_decode_typed(const DecodeParams& p, int head_dim, int block_size, int gc,
                                 cudaStream_t stream)
 {
-#define PA_DECODE_CASE(D_, BS_, GC_)                                  \
-    if (head_dim == D_ && block_size == BS_ && gc == GC_)             \
-        return launch_decode_variant<T, D_, BS_, GC_>(p, stream);
-#define PA_DECODE_GC(D_, BS_) \
-    PA_DECODE_CASE(D_, BS_, 1) PA_DECODE_CASE(D_, BS_, 2) PA_DECODE_CASE(D_, BS_, 4) PA_DECODE_CASE(D_, BS_, 8)
-    PA_DECODE_GC(128, 16)
-    PA_DECODE_GC(128, 32)
-    PA_DECODE_GC(64, 16)
-    PA_DECODE_GC(64, 32)
-#undef PA_DECODE_GC
-#undef PA_DECODE_CASE
+#define PA_CORE_CASE(D_, BS_, GC_)                                   \
+    if (head_dim == D_ && block_size == BS_ && gc == GC_)            \
+        return CoreVariant<T, D_, BS_, GC_>::launch(p, stream);
+    PA_CORE_VARIANTS(PA_CORE_CASE)
+#undef PA_CORE_CASE
     return cudaErrorInvalidValue;
+}
+
+// Resident CTAs per SM of the CUDA-core kernel for this shape (0 if unknown).
+template <typename T>
+int occupancy_decode_typed(int head_dim, int block_size, int gc)
+{
+#define PA_CORE_OCC(D_, BS_, GC_)                                    \
+    if (head_dim == D_ && block_size == BS_ && gc == GC_) {          \
+        using V = CoreVariant<T, D_, BS_, GC_>;                      \
+        return V::configure() == cudaSuccess                         \
+                   ? kernel_occupancy(reinterpret_cast<const void*>(V::kernel()), V::Smem::kBytes) \
+                   : 0;                                              \
+    }
+    PA_CORE_VARIANTS(PA_CORE_OCC)
+#undef PA_CORE_OCC
+    return 0;
 }
 
 }  // namespace pa

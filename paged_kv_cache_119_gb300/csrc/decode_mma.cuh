@@ -444,42 +444,46 @@ __global__ void __launch_bounds__(kDecodeThreads)
     }
 }
 
-// Ring depth of the tensor-core kernel: one or two stages per consumer warp.
+// Ring depth of the tensor-core kernel: one stage per consumer warp.  The
+// consumers need little time per tile, so a shallow ring and more resident CTAs
+// per SM beat a deeper ring (measured on GB300: 75 vs 95 us for the shared-prefix
+// decode, 175 vs 194 us for the 8 x 32768-token decode at 2048-token partitions).
 template <typename T, int D, int BS>
 struct MmaStages {
-    static constexpr int kStageBytes = 2 * (D / 64) * BS * 128;
-    static constexpr int value = kDecodeConsumerWarps * (kStageBytes <= 8192 ? 2 : 1);
+    static constexpr int value = kDecodeConsumerWarps;
 };
 
 template <typename T, int D, int BS, int NH>
-cudaError_t launch_decode_mma_variant(const DecodeParams& p, const CUtensorMap& tk,
-                                      const CUtensorMap& tv, cudaStream_t stream)
-{
-    constexpr int NSTAGE = MmaStages<T, D, BS>::value;
-    using Sm = MmaSmem<T, D, BS, NSTAGE>;
-    auto kern = decode_mma_kernel<T, D, BS, NH, NSTAGE>;
-    static int configured_device = -1;
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess)
-        return err;
-    if (configured_device != dev) {
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::kAlloc);
+struct MmaVariant {
+    static constexpr int kStages = MmaStages<T, D, BS>::value;
+    using Sm = MmaSmem<T, D, BS, kStages>;
+    static constexpr auto kernel() { return decode_mma_kernel<T, D, BS, NH, kStages>; }
+    static cudaError_t configure()
+    {
+        return configure_once(reinterpret_cast<const void*>(kernel()), Sm::kAlloc);
+    }
+    static cudaError_t launch(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                              cudaStream_t stream)
+    {
+        cudaError_t err = configure();
         if (err != cudaSuccess)
             return err;
-        configured_device = dev;
+        const bool split = p.partition_tokens > 0;
+        dim3 grid(split ? p.max_parts : 1, p.num_kv_heads * p.chunks, p.num_seqs);
+        kernel()<<<grid, kDecodeThreads, Sm::kAlloc, stream>>>(p, tk, tv);
+        err = cudaGetLastError();
+        if (err != cudaSuccess || !split)
+            return err;
+        reduce_kernel<T, D><<<dim3(p.num_q_heads, p.num_seqs), D, 0, stream>>>(p);
+        return cudaGetLastError();
     }
-    const bool split = p.partition_tokens > 0;
-    dim3 grid(split ? p.max_parts : 1, p.num_kv_heads * p.chunks, p.num_seqs);
-    kern<<<grid, kDecodeThreads, Sm::kAlloc, stream>>>(p, tk, tv);
-    err = cudaGetLastError();
-    if (err != cudaSuccess || !split)
-        return err;
-    reduce_kernel<T, D><<<dim3(p.num_q_heads, p.num_seqs), D, 0, stream>>>(p);
-    return cudaGetLastError();
-}
+};
 
 // Tensor-core path for 16-bit caches with 4 or 8 query heads per CTA.
+#define PA_MMA_VARIANTS(X)                                                          \
+    X(128, 16, 8) X(128, 16, 4) X(128, 32, 8) X(128, 32, 4) X(64, 16, 8) X(64, 16, 4) \
+    X(64, 32, 8) X(64, 32, 4)
+
 template <typename T>
 cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, int block_size, int gc,
                               cudaStream_t stream)
@@ -492,15 +496,28 @@ cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, int block_siz
                           DType<T>::id);
     if (e != cudaSuccess)
         return e;
-#define PA_MMA_CASE(D_, BS_, NH_)                                         \
-    if (head_dim == D_ && block_size == BS_ && gc == NH_)                 \
-        return launch_decode_mma_variant<T, D_, BS_, NH_>(p, tk, tv, stream);
-    PA_MMA_CASE(128, 16, 8) PA_MMA_CASE(128, 16, 4)
-    PA_MMA_CASE(128, 32, 8) PA_MMA_CASE(128, 32, 4)
-    PA_MMA_CASE(64, 16, 8) PA_MMA_CASE(64, 16, 4)
-    PA_MMA_CASE(64, 32, 8) PA_MMA_CASE(64, 32, 4)
+#define PA_MMA_CASE(D_, BS_, NH_)                                  \
+    if (head_dim == D_ && block_size == BS_ && gc == NH_)          \
+        return MmaVariant<T, D_, BS_, NH_>::launch(p, tk, tv, stream);
+    PA_MMA_VARIANTS(PA_MMA_CASE)
 #undef PA_MMA_CASE
     return cudaErrorInvalidValue;
+}
+
+// Resident CTAs per SM of the tensor-core kernel for this shape (0 if unknown).
+template <typename T>
+int occupancy_decode_mma(int head_dim, int block_size, int gc)
+{
+#define PA_MMA_OCC(D_, BS_, NH_)                                   \
+    if (head_dim == D_ && block_size == BS_ && gc == NH_) {        \
+        using V = MmaVariant<T, D_, BS_, NH_>;                     \
+        return V::configure() == cudaSuccess                       \
+                   ? kernel_occupancy(reinterpret_cast<const void*>(V::kernel()), V::Sm::kAlloc) \
+                   : 0;                                            \
+    }
+    PA_MMA_VARIANTS(PA_MMA_OCC)
+#undef PA_MMA_OCC
+    return 0;
 }
 
 }  // namespace pa

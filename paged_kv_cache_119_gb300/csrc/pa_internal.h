@@ -50,6 +50,11 @@ cudaError_t launch_decode_f16(const DecodeParams& p, int head_dim, int block_siz
 cudaError_t launch_decode_bf16(const DecodeParams& p, int head_dim, int block_size, int gc,
                                cudaStream_t stream);
 
+// Resident decode CTAs per SM for this dtype / shape / heads-per-CTA (0 if unknown).
+int occupancy_decode_f32(int head_dim, int block_size, int gc);
+int occupancy_decode_f16(int head_dim, int block_size, int gc);
+int occupancy_decode_bf16(int head_dim, int block_size, int gc);
+
 struct ReshapeParams {
     const uint4* k;
     const uint4* v;

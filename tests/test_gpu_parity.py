@@ -140,10 +140,12 @@ FULL = ["opt13b", "llama13b", "prefix", "long16", "long32"]
 
 
 @pytest.mark.parametrize("name", FULL)
-def test_config_full_size(name):
-    """The full workload, in the launch configuration the benchmark times."""
+@pytest.mark.parametrize("part", ["config", "auto"])
+def test_config_full_size(name, part):
+    """The full workload: with the config's partition size (512 tokens for the long
+    contexts) and with the automatic split the benchmark times."""
     w = workloads.make(name, device="cuda")
-    run_and_compare(w)
+    run_and_compare(w, partition_size=None if part == "config" else 0)
 
 
 # ------------------------------------------------------------------ invariants
