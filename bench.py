@@ -104,7 +104,7 @@ def load_peaks():
 
 def kernel_hash() -> str:
     h = hashlib.sha256()
-    for name in ("decode_kernel.cuh", "pa_device.cuh", "pa_internal.h"):
+    for name in ("decode_kernel.cuh", "decode_mma.cuh", "pa_device.cuh", "pa_internal.h"):
         with open(os.path.join(ROOT, "paged_kv_cache_119_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
