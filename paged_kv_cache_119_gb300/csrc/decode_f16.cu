@@ -1,5 +1,5 @@
 // decode_f16.cu -- paged decode attention, __half KV cache: the tensor-core kernel
-// (decode_mma.cuh) when a CTA serves 4 or 8 query heads of one kv head, else the
+// (decode_mma.cuh) when a CTA serves at least kMmaMinHeads query heads of one kv head, else the
 // CUDA-core kernel (decode_kernel.cuh).
 #include "decode_mma.cuh"
 
@@ -8,14 +8,14 @@ namespace pa {
 cudaError_t launch_decode_f16(const DecodeParams& p, int head_dim, int block_size, int gc,
                               cudaStream_t stream)
 {
-    if (gc >= 4)
+    if (gc >= kMmaMinHeads)
         return launch_decode_mma<__half>(p, head_dim, block_size, gc, stream);
     return launch_decode_typed<__half>(p, head_dim, block_size, gc, stream);
 }
 
 int occupancy_decode_f16(int head_dim, int block_size, int gc)
 {
-    if (gc >= 4)
+    if (gc >= kMmaMinHeads)
         return occupancy_decode_mma<__half>(head_dim, block_size, gc);
     return occupancy_decode_typed<__half>(head_dim, block_size, gc);
 }

@@ -122,6 +122,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
     constexpr int kTile = Smem::kTile;
     static_assert(D % 32 == 0 && (E == 2 || E == 4), "head_dim must be 64 or 128");
     static_assert(NSTAGE % NCW == 0, "each ring stage must belong to one consumer warp");
+    // copy a tile to registers and release its stage early when K + V take <= 64 registers
+    constexpr bool kEarlyRelease = 2 * BS * E * (int)sizeof(T) / 4 <= 64;
 
     extern __shared__ __align__(128) unsigned char smem[];
     T* ring = reinterpret_cast<T*>(smem);
@@ -264,6 +266,33 @@ __global__ void __launch_bounds__(kDecodeThreads)
         const T* Vs = Ks + kTile;
         const int nvalid = min(BS, t1 - (jb + it) * BS);
 
+        // Small tiles are copied to registers and the stage is released at once, so
+        // the producer refills it while this warp computes (the stage would
+        // otherwise be held through the whole tile's arithmetic).
+        Raw<T, E> kr[kEarlyRelease ? BS : 1], vr[kEarlyRelease ? BS : 1];
+        if constexpr (kEarlyRelease) {
+#pragma unroll
+            for (int t = 0; t < BS; ++t) {
+                load_raw<T, E>(Ks + t * D + lane * E, kr[t]);
+                load_raw<T, E>(Vs + t * D + lane * E, vr[t]);
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[stage]);
+        }
+        auto k_row = [&](int t, float (&f)[E]) {
+            if constexpr (kEarlyRelease)
+                raw_to_float<T, E>(kr[t], f);
+            else
+                Load<T, E>::run(Ks + t * D + lane * E, f);
+        };
+        auto v_row = [&](int t, float (&f)[E]) {
+            if constexpr (kEarlyRelease)
+                raw_to_float<T, E>(vr[t], f);
+            else
+                Load<T, E>::run(Vs + t * D + lane * E, f);
+        };
+
         // scores s[g][c] for token c * TC + mytok, base-2 units
         float s[GC][NCH];
 #pragma unroll
@@ -271,7 +300,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
             float kf[TC][E];
 #pragma unroll
             for (int tt = 0; tt < TC; ++tt)
-                Load<T, E>::run(Ks + (c * TC + tt) * D + lane * E, kf[tt]);
+                k_row(c * TC + tt, kf[tt]);
 #pragma unroll
             for (int g = 0; g < GC; ++g) {
                 float part_dot[TC];
@@ -337,7 +366,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
                 for (int u = 0; u < 4; ++u) {
                     if (t4 + u < nvalid) {
                         float vf[E];
-                        Load<T, E>::run(Vs + (t4 + u) * D + lane * E, vf);
+                        v_row(t4 + u, vf);
 #pragma unroll
                         for (int g = 0; g < GC; ++g) {
                             const float pt = u == 0 ? pv[g].x : u == 1 ? pv[g].y : u == 2 ? pv[g].z : pv[g].w;
@@ -349,9 +378,11 @@ __global__ void __launch_bounds__(kDecodeThreads)
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&empty[stage]);
+        if constexpr (!kEarlyRelease) {
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[stage]);
+        }
     }
 
     // ------------------------------------------------------------- merge the warps

@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
     constexpr int NCW = kDecodeConsumerWarps;
     constexpr int KS = D / 16;        // k-steps of the score product / m-blocks of P.V
     constexpr int MB = BS / 16;       // 16-token row blocks per tile
-    static_assert(NH == 4 || NH == 8, "4 or 8 query heads per CTA");
+    static_assert(NH == 1 || NH == 2 || NH == 4 || NH == 8, "1, 2, 4 or 8 query heads per CTA");
     static_assert(NSTAGE % NCW == 0, "each ring stage must belong to one consumer warp");
     static_assert(BS % 16 == 0 && D % 64 == 0, "block_size 16/32, head_dim 64/128");
 
@@ -479,10 +479,11 @@ struct MmaVariant {
     }
 };
 
-// Tensor-core path for 16-bit caches with 4 or 8 query heads per CTA.
-#define PA_MMA_VARIANTS(X)                                                          \
-    X(128, 16, 8) X(128, 16, 4) X(128, 32, 8) X(128, 32, 4) X(64, 16, 8) X(64, 16, 4) \
-    X(64, 32, 8) X(64, 32, 4)
+// Tensor-core path for 16-bit caches (1, 2, 4 or 8 query heads per CTA).
+#define PA_MMA_VARIANTS(X)                                                                    \
+    X(128, 16, 8) X(128, 16, 4) X(128, 16, 2) X(128, 16, 1) X(128, 32, 8) X(128, 32, 4)         \
+    X(128, 32, 2) X(128, 32, 1) X(64, 16, 8) X(64, 16, 4) X(64, 16, 2) X(64, 16, 1) X(64, 32, 8) \
+    X(64, 32, 4) X(64, 32, 2) X(64, 32, 1)
 
 template <typename T>
 cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, int block_size, int gc,

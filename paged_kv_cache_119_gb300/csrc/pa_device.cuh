@@ -192,6 +192,51 @@ struct Load<float, 2> {
     }
 };
 
+// N consecutive elements of T held as raw 32-bit words (N * sizeof(T) / 4 of them),
+// loaded with one vector load and converted to fp32 later.
+template <typename T, int N>
+struct Raw {
+    static constexpr int W = N * (int)sizeof(T) / 4;
+    uint32_t w[W];
+};
+
+template <typename T, int N>
+__device__ __forceinline__ void load_raw(const T* p, Raw<T, N>& r)
+{
+    if constexpr (Raw<T, N>::W == 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(p);
+        r.w[0] = v.x; r.w[1] = v.y; r.w[2] = v.z; r.w[3] = v.w;
+    } else if constexpr (Raw<T, N>::W == 2) {
+        const uint2 v = *reinterpret_cast<const uint2*>(p);
+        r.w[0] = v.x; r.w[1] = v.y;
+    } else {
+        r.w[0] = *reinterpret_cast<const uint32_t*>(p);
+    }
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void raw_to_float(const Raw<T, N>& r, float (&f)[N])
+{
+    if constexpr (sizeof(T) == 4) {
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            f[i] = __uint_as_float(r.w[i]);
+    } else if constexpr (DType<T>::id == PA_BF16) {
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            f[2 * i] = bf16_lo(r.w[i]);
+            f[2 * i + 1] = bf16_hi(r.w[i]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&r.w[i]));
+            f[2 * i] = v.x;
+            f[2 * i + 1] = v.y;
+        }
+    }
+}
+
 // Stores one fp32 value as T, rounding to nearest even.
 __device__ __forceinline__ void store_as(float* p, float x) { *p = x; }
 __device__ __forceinline__ void store_as(__half* p, float x) { *p = __float2half_rn(x); }

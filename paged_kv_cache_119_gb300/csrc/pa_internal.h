@@ -13,6 +13,9 @@ namespace pa {
 // Consumer warps per decode CTA; one more warp issues the bulk copies.
 constexpr int kDecodeConsumerWarps = 4;
 constexpr int kDecodeThreads = (kDecodeConsumerWarps + 1) * 32;
+// 16-bit caches use the tensor-core decode when a CTA serves at least this many
+// query heads, else the CUDA-core decode.
+constexpr int kMmaMinHeads = 4;
 // Partition length the automatic split uses (a multiple of every block size).
 constexpr int kAutoPartitionTokens = 512;
 
