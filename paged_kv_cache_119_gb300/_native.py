@@ -16,7 +16,7 @@ PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0, -1
 PA_DEVERR_BLOCK_ID, PA_DEVERR_CONTEXT_LEN, PA_DEVERR_SLOT, PA_DEVERR_TIMEOUT = 1, 2, 4, 8
 PA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
-# Every symbol include/pa.h declares, with (restype, argtypes).
+# Every symbol include/pa.h and include/pa_block_manager.h declare, with (restype, argtypes).
 _i32, _i64, _sz, _vp, _f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, \
     ctypes.c_float
 SIGNATURES = {
@@ -32,6 +32,18 @@ SIGNATURES = {
     "pa_copy_blocks": (ctypes.c_int, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32,
                                       ctypes.POINTER(_i64), _i64, _i64, _i64, _vp]),
     "pa_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), _vp]),
+    "pa_bm_create": (_vp, [_i32, _i32, ctypes.POINTER(_i32)]),
+    "pa_bm_destroy": (None, [_vp]),
+    "pa_bm_add_sequence": (ctypes.c_int, [_vp, _i64, _i32, ctypes.POINTER(_i64)]),
+    "pa_bm_fork": (ctypes.c_int, [_vp, _i64, _i64]),
+    "pa_bm_append": (ctypes.c_int, [_vp, ctypes.POINTER(_i64), _i32, ctypes.POINTER(_i64),
+                                    ctypes.POINTER(_i64), ctypes.POINTER(_i32)]),
+    "pa_bm_free": (ctypes.c_int, [_vp, _i64]),
+    "pa_bm_block_tables": (ctypes.c_int, [_vp, ctypes.POINTER(_i64), _i32, ctypes.POINTER(_i32),
+                                          _i32, ctypes.POINTER(_i32)]),
+    "pa_bm_num_free_blocks": (_i32, [_vp]),
+    "pa_bm_ref_count": (_i32, [_vp, _i32]),
+    "pa_bm_num_tokens": (_i32, [_vp, _i64]),
     "pa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pa_version": (ctypes.c_char_p, []),
 }

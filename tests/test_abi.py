@@ -9,7 +9,7 @@ import pytest
 from paged_kv_cache_119_gb300 import _native as N
 from paged_kv_cache_119_gb300 import build as B
 
-HEADER = os.path.join(B.ROOT, "include", "pa.h")
+HEADERS = [os.path.join(B.ROOT, "include", h) for h in ("pa.h", "pa_block_manager.h")]
 
 
 @pytest.fixture(scope="module")
@@ -19,9 +19,12 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER, encoding="utf-8").read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = open(h, encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_and_binding_agree():
