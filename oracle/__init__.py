@@ -30,7 +30,7 @@ _SRC = os.path.join(_HERE, "pa_oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libpa_oracle.so")
 
-F32, F16, BF16 = 0, 1, 2
+F32, F16, BF16, E4M3 = 0, 1, 2, 3
 _lock = threading.Lock()
 _lib = None
 
@@ -52,8 +52,16 @@ def build(src: str = _SRC, out: str = _LIB_PATH, extra_flags=()) -> str:
 def _declare(lib):
     c_i64, c_i32, c_vp, c_dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_double
     lib.orc_paged_attention.restype = ctypes.c_int
-    lib.orc_paged_attention.argtypes = [c_vp, c_vp, c_i32, c_vp, c_vp, c_i32, c_i64, c_vp, c_i64,
-                                        c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_dbl, c_i32]
+    lib.orc_paged_attention.argtypes = [c_vp, c_vp, c_i32, c_vp, c_vp, c_i32, c_vp, c_vp, c_i64,
+                                        c_vp, c_i64, c_vp, c_i32, c_i32, c_i32, c_i32, c_i32,
+                                        c_dbl, c_i32]
+    lib.orc_reshape_and_cache_e4m3.restype = ctypes.c_int
+    lib.orc_reshape_and_cache_e4m3.argtypes = [c_vp, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                               c_i64, c_i32, c_i32, c_i32, c_i64]
+    lib.orc_e4m3_to_f64.restype = c_dbl
+    lib.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+    lib.orc_f32_to_e4m3.restype = ctypes.c_uint8
+    lib.orc_f32_to_e4m3.argtypes = [ctypes.c_float]
     lib.orc_reshape_and_cache.restype = ctypes.c_int
     lib.orc_reshape_and_cache.argtypes = [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i32, c_i32,
                                           c_i32, c_i64, c_i32]
@@ -86,6 +94,8 @@ def load_library(path: str | None = None):
 
 def _dtype_code(x) -> int:
     name = str(x.dtype)
+    if name in ("torch.float8_e4m3fn", "torch.uint8", "uint8"):
+        return E4M3
     if name in ("torch.float32", "float32"):
         return F32
     if name in ("torch.float16", "float16"):
@@ -108,6 +118,8 @@ def _raw(x, inplace: bool = False) -> np.ndarray:
             x = x.contiguous()
             if x.dtype in (torch.float16, torch.bfloat16):
                 return x.view(torch.int16).numpy()
+            if x.dtype == torch.float8_e4m3fn:
+                return x.view(torch.uint8).numpy()
             return x.numpy()
     except ImportError:
         pass
@@ -126,13 +138,19 @@ def max_threads() -> int:
 
 def paged_attention(q, k_cache, v_cache, block_tables, context_lens, scale: float,
                     num_kv_heads: int, block_size: int, num_threads: int = 1,
-                    lib=None) -> np.ndarray:
+                    lib=None, k_scale=None, v_scale=None) -> np.ndarray:
     """Decode attention through block tables, fp64.  Returns out[S][Hq][D] as float64.
 
     q: [S, Hq, D]; k_cache, v_cache: [N, Hkv, B, D]; block_tables: [S, W] int32;
-    context_lens: [S] int32 (current token included).
+    context_lens: [S] int32 (current token included).  An E4M3 cache (torch
+    float8_e4m3fn or uint8 codes) needs k_scale, v_scale: [Hkv] per-head scales.
     """
     lib = lib or load_library()
+    ks = vs = None
+    if k_scale is not None:
+        ks = np.ascontiguousarray(_raw(k_scale), dtype=np.float32)
+        vs = np.ascontiguousarray(_raw(v_scale), dtype=np.float32)
+        assert ks.shape == (num_kv_heads,) and vs.shape == (num_kv_heads,)
     qa, ka, va = _raw(q), _raw(k_cache), _raw(v_cache)
     bt = np.ascontiguousarray(_raw(block_tables), dtype=np.int32)
     cl = np.ascontiguousarray(_raw(context_lens), dtype=np.int32)
@@ -141,9 +159,13 @@ def paged_attention(q, k_cache, v_cache, block_tables, context_lens, scale: floa
     assert ka.shape == (N, num_kv_heads, block_size, D), ka.shape
     assert bt.ndim == 2 and bt.shape[0] == S and cl.shape == (S,)
     out = np.zeros((S, Hq, D), dtype=np.float64)
+    if _dtype_code(k_cache) == E4M3 and ks is None:
+        raise ValueError("an E4M3 cache needs k_scale and v_scale")
     rc = lib.orc_paged_attention(_ptr(out), _ptr(qa), _dtype_code(q), _ptr(ka), _ptr(va),
-                                 _dtype_code(k_cache), N, _ptr(bt), bt.shape[1], _ptr(cl), S, Hq,
-                                 num_kv_heads, D, block_size, float(scale), int(num_threads))
+                                 _dtype_code(k_cache), None if ks is None else _ptr(ks),
+                                 None if vs is None else _ptr(vs), N, _ptr(bt), bt.shape[1],
+                                 _ptr(cl), S, Hq, num_kv_heads, D, block_size, float(scale),
+                                 int(num_threads))
     if rc != 0:
         raise ValueError(f"oracle paged_attention rejected its inputs (status {rc})")
     return out
@@ -162,6 +184,33 @@ def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, block_size: int, lib
                                    block_size, kc.shape[0], _dtype_code(k))
     if rc != 0:
         raise ValueError(f"oracle reshape_and_cache rejected its inputs (status {rc})")
+
+
+def reshape_and_cache_e4m3(k, v, k_cache, v_cache, slot_mapping, block_size: int, k_scale,
+                           v_scale, lib=None) -> None:
+    """Quantising cache write: codes e4m3(fp32(k) / k_scale[h]) into E4M3 caches
+    (torch float8_e4m3fn or uint8, in place)."""
+    lib = lib or load_library()
+    ka, va = _raw(k), _raw(v)
+    kc, vc = _raw(k_cache, inplace=True), _raw(v_cache, inplace=True)
+    sm = np.ascontiguousarray(_raw(slot_mapping), dtype=np.int64)
+    ks = np.ascontiguousarray(_raw(k_scale), dtype=np.float32)
+    vs = np.ascontiguousarray(_raw(v_scale), dtype=np.float32)
+    T, Hkv, D = ka.shape
+    assert ks.shape == (Hkv,) and vs.shape == (Hkv,)
+    rc = lib.orc_reshape_and_cache_e4m3(_ptr(ka), _ptr(va), _dtype_code(k), _ptr(kc), _ptr(vc),
+                                        _ptr(ks), _ptr(vs), _ptr(sm), T, Hkv, D, block_size,
+                                        kc.shape[0])
+    if rc != 0:
+        raise ValueError(f"oracle reshape_and_cache_e4m3 rejected its inputs (status {rc})")
+
+
+def e4m3_to_f64(code: int) -> float:
+    return load_library().orc_e4m3_to_f64(code)
+
+
+def f32_to_e4m3(x: float) -> int:
+    return int(load_library().orc_f32_to_e4m3(x))
 
 
 def copy_blocks(caches, pairs, lib=None) -> None:

@@ -45,7 +45,7 @@
 #include <omp.h>
 #endif
 
-enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2 };
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_E4M3 = 3 };
 
 /* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
 double orc_f16_to_f64(uint16_t h)
@@ -72,9 +72,50 @@ double orc_bf16_to_f64(uint16_t b)
     return (double)f;
 }
 
+/* OCP FP8 E4M3 ("e4m3fn"): 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits;
+ * exponent field 0 is subnormal (fraction x 2^-9), the all-ones code S.1111.111 is
+ * NaN, there are no infinities, and the largest finite magnitude is 448. */
+double orc_e4m3_to_f64(uint8_t c)
+{
+    int sign = c >> 7;
+    int expo = (c >> 3) & 0xf;
+    int frac = c & 0x7;
+    double mag;
+    if (expo == 15 && frac == 7)
+        return NAN;
+    if (expo == 0)
+        mag = ldexp((double)frac, -9);
+    else
+        mag = ldexp((double)(8 + frac), expo - 10);      /* 1.frac * 2^(e-7) */
+    return sign ? -mag : mag;
+}
+
+/* The e4m3 code nearest to x, ties to the even code (even fraction), saturating:
+ * magnitudes of 448 and above (infinity included) give +-448, NaN gives 0x7f.
+ * Found by comparing x with every finite code's value. */
+uint8_t orc_f32_to_e4m3(float x)
+{
+    if (isnan(x))
+        return 0x7f;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    if (a >= 448.0)
+        return sign | 0x7e;
+    int best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c <= 0x7e; ++c) {
+        const double d = fabs(a - orc_e4m3_to_f64((uint8_t)c));
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return sign | (uint8_t)best;
+}
+
 static size_t orc_elem_size(int dtype)
 {
-    return dtype == ORC_F32 ? 4 : 2;
+    return dtype == ORC_F32 ? 4 : (dtype == ORC_E4M3 ? 1 : 2);
 }
 
 static double orc_load(const void* base, int dtype, int64_t idx)
@@ -84,6 +125,8 @@ static double orc_load(const void* base, int dtype, int64_t idx)
         memcpy(&f, (const char*)base + 4 * idx, 4);
         return (double)f;
     }
+    if (dtype == ORC_E4M3)
+        return orc_e4m3_to_f64(((const uint8_t*)base)[idx]);
     uint16_t bits;
     memcpy(&bits, (const char*)base + 2 * idx, 2);
     return dtype == ORC_F16 ? orc_f16_to_f64(bits) : orc_bf16_to_f64(bits);
@@ -101,7 +144,8 @@ static int64_t orc_row(int64_t block, int head, int offset, int num_kv_heads,
  * Returns 0, or -1 when a block id read from the table lies outside the pool.
  */
 static int orc_one_head(double* o, const void* q, int q_dtype, const void* k_cache,
-                        const void* v_cache, int kv_dtype, int64_t num_blocks,
+                        const void* v_cache, int kv_dtype, const float* k_scale,
+                        const float* v_scale, int64_t num_blocks,
                         const int32_t* table_row, int s, int h, int L, int num_q_heads,
                         int num_kv_heads, int head_dim, int block_size, double scale)
 {
@@ -128,9 +172,12 @@ static int orc_one_head(double* o, const void* q, int q_dtype, const void* k_cac
             return -1;
         }
         int64_t r = orc_row(blk, hk, off, num_kv_heads, block_size, head_dim);
+        /* a quantised cache holds codes; the value is code * the kv head's scale */
+        const double ks = k_scale ? (double)k_scale[hk] : 1.0;
+        const double vs = v_scale ? (double)v_scale[hk] : 1.0;
         for (int d = 0; d < head_dim; ++d) {
-            K[(size_t)t * head_dim + d] = orc_load(k_cache, kv_dtype, r + d);
-            V[(size_t)t * head_dim + d] = orc_load(v_cache, kv_dtype, r + d);
+            K[(size_t)t * head_dim + d] = orc_load(k_cache, kv_dtype, r + d) * ks;
+            V[(size_t)t * head_dim + d] = orc_load(v_cache, kv_dtype, r + d) * vs;
         }
     }
 
@@ -167,13 +214,15 @@ static int orc_one_head(double* o, const void* q, int q_dtype, const void* k_cac
 
 /*
  * Paged decode attention: out[s][h][:] for every sequence s and query head h.
- * context_lens[s] tokens are attended (the current token included).
+ * context_lens[s] tokens are attended (the current token included).  For an
+ * E4M3 cache, k_scale / v_scale give each kv head's scale (NULL otherwise).
  * Returns 0; -1 for a block id outside [0, num_blocks); -3 for a context
  * longer than the table row (bt_stride * block_size) or negative; -2 on
  * allocation failure; -4 for bad sizes.
  */
 int orc_paged_attention(double* out, const void* q, int q_dtype, const void* k_cache,
-                        const void* v_cache, int kv_dtype, int64_t num_blocks,
+                        const void* v_cache, int kv_dtype, const float* k_scale,
+                        const float* v_scale, int64_t num_blocks,
                         const int32_t* block_tables, int64_t bt_stride,
                         const int32_t* context_lens, int num_seqs, int num_q_heads,
                         int num_kv_heads, int head_dim, int block_size, double scale,
@@ -197,7 +246,8 @@ int orc_paged_attention(double* out, const void* q, int q_dtype, const void* k_c
         int s = (int)(i / num_q_heads);
         int h = (int)(i % num_q_heads);
         int rc = orc_one_head(out + i * head_dim, q, q_dtype, k_cache, v_cache, kv_dtype,
-                              num_blocks, block_tables + (int64_t)s * bt_stride, s, h,
+                              k_scale, v_scale, num_blocks,
+                              block_tables + (int64_t)s * bt_stride, s, h,
                               context_lens[s], num_q_heads, num_kv_heads, head_dim,
                               block_size, scale);
         if (rc != 0) {
@@ -237,6 +287,40 @@ int orc_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_c
             size_t dst = (size_t)orc_row(blk, h, off, num_kv_heads, block_size, head_dim) * esz;
             memcpy((char*)k_cache + dst, (const char*)k + src, row);
             memcpy((char*)v_cache + dst, (const char*)v + src, row);
+        }
+    }
+    return 0;
+}
+
+/*
+ * reshape_and_cache into an E4M3 cache: for every new token i with a slot >= 0 and
+ * every kv head h, k_cache[slot / B][h][slot % B][d] = e4m3(fp32(k[i][h][d]) / k_scale[h])
+ * (fp32 division, rounded to the nearest code, ties to even, saturating), likewise v.
+ * Returns 0, or -1 if a slot lies beyond the pool (nothing is written then).
+ */
+int orc_reshape_and_cache_e4m3(const void* k, const void* v, int src_dtype, uint8_t* k_cache,
+                               uint8_t* v_cache, const float* k_scale, const float* v_scale,
+                               const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads,
+                               int head_dim, int block_size, int64_t num_blocks)
+{
+    for (int64_t i = 0; i < num_tokens; ++i)
+        if (slot_mapping[i] >= num_blocks * block_size)
+            return -1;
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        int64_t slot = slot_mapping[i];
+        if (slot < 0)
+            continue;
+        int64_t block = slot / block_size;
+        int offset = (int)(slot % block_size);
+        for (int h = 0; h < num_kv_heads; ++h) {
+            int64_t src = ((int64_t)i * num_kv_heads + h) * head_dim;
+            int64_t dst = orc_row(block, h, offset, num_kv_heads, block_size, head_dim);
+            for (int d = 0; d < head_dim; ++d) {
+                float kx = (float)orc_load(k, src_dtype, src + d);
+                float vx = (float)orc_load(v, src_dtype, src + d);
+                k_cache[dst + d] = orc_f32_to_e4m3(kx / k_scale[h]);
+                v_cache[dst + d] = orc_f32_to_e4m3(vx / v_scale[h]);
+            }
         }
     }
     return 0;

@@ -402,4 +402,101 @@ def pin_reshape_bytes(lib):
         assert torch.equal(vc.view(ib), exp_v.view(ib))
 
 
+def pin_e4m3_decoder(lib):
+    """Every OCP E4M3 code decodes as PyTorch's float8_e4m3fn decodes it."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([lib.orc_e4m3_to_f64(i) for i in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got)) and nan.sum() == 2
+    assert np.array_equal(ref[~nan], got[~nan])
+    assert np.array_equal(np.signbit(ref[~nan]), np.signbit(got[~nan]))
+
+
+def _e4m3_probe_values():
+    """fp32 values spanning E4M3's range: every code value, every midpoint between
+    neighbours (ties), the midpoints nudged up and down, subnormals, both signs."""
+    pos = torch.arange(0, 127, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn)
+    vals = pos.double()
+    mids = (vals[1:] + vals[:-1]) / 2
+    pts = torch.cat([vals, mids, mids * (1 + 2 ** -20), mids * (1 - 2 ** -20),
+                     torch.linspace(0, 448, 2001, dtype=torch.float64)])
+    pts = torch.cat([pts, -pts]).float()
+    return pts[pts.abs() <= 448]
+
+
+def pin_e4m3_encoder_rounds_to_nearest_even(lib):
+    """In range, the encoder equals PyTorch's round-to-nearest-even cast, ties included."""
+    x = _e4m3_probe_values()
+    ref = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([lib.orc_f32_to_e4m3(float(v)) for v in x.tolist()], dtype=np.uint8)
+    assert np.array_equal(ref, got)
+
+
+def pin_e4m3_encoder_saturates(lib):
+    """Beyond the largest finite magnitude (448) the encoder saturates (the reading for
+    quantised caches); NaN stays NaN."""
+    for x, code in [(449.0, 0x7E), (464.0, 0x7E), (1e6, 0x7E), (float("inf"), 0x7E),
+                    (-449.0, 0xFE), (-1e30, 0xFE), (float("-inf"), 0xFE)]:
+        assert lib.orc_f32_to_e4m3(x) == code, x
+    assert lib.orc_f32_to_e4m3(float("nan")) & 0x7F == 0x7F
+
+
+def _fp8_case(seed, S, Hq, Hkv, D, B, max_len):
+    rng = np.random.default_rng(seed)
+    c = random_case(rng, S, Hq, Hkv, D, B, torch.float32, max_len)
+    g = torch.Generator().manual_seed(seed)
+    ks = (torch.rand(Hkv, generator=g) * 0.02 + 0.005).float()      # per-head scales
+    vs = (torch.rand(Hkv, generator=g) * 0.02 + 0.005).float()
+    kq = torch.randint(0, 256, c["kc"].shape, generator=g, dtype=torch.int32).to(torch.uint8)
+    vq = torch.randint(0, 256, c["vc"].shape, generator=g, dtype=torch.int32).to(torch.uint8)
+    kq[(kq & 0x7F) == 0x7F] = 0x3F                                   # no NaN codes
+    vq[(vq & 0x7F) == 0x7F] = 0x38
+    return c, kq, vq, ks, vs
+
+
+def pin_e4m3_attention_equals_dequantized_sdpa(lib):
+    """Attention over an E4M3 cache equals PyTorch float64 SDPA over the dequantised
+    (code value x the kv head's own scale) unpaged K and V."""
+    for seed, (S, Hq, Hkv, D, B, max_len) in enumerate([(3, 4, 2, 16, 4, 23), (2, 8, 4, 32, 16, 60)]):
+        c, kq, vq, ks, vs = _fp8_case(seed + 31, S, Hq, Hkv, D, B, max_len)
+        out = oracle.paged_attention(c["q"], kq, vq, table_tensor(c["tables"]),
+                                     torch.tensor(c["lens"], dtype=torch.int32), 0.3, Hkv, B,
+                                     lib=lib, k_scale=ks, v_scale=vs)
+        kd = kq.view(torch.float8_e4m3fn).double() * ks.double()[None, :, None, None]
+        vd = vq.view(torch.float8_e4m3fn).double() * vs.double()[None, :, None, None]
+        for s, L in enumerate(c["lens"]):
+            tab = c["tables"][s]
+            K = torch.stack([kd[tab[t // B], :, t % B] for t in range(L)])
+            V = torch.stack([vd[tab[t // B], :, t % B] for t in range(L)])
+            np.testing.assert_allclose(out[s], dense_reference(c["q"][s], K, V, 0.3),
+                                       rtol=1e-12, atol=1e-12)
+
+
+def pin_e4m3_cache_write(lib):
+    """The quantising cache write stores PyTorch's nearest-even code of fp32(x) / scale[h]
+    (IEEE fp32 division) at each token's slot, per head; other bytes are untouched."""
+    Hkv, D, B, N = 3, 16, 4, 6
+    g = torch.Generator().manual_seed(77)
+    for dtype in (torch.float32, torch.float16, torch.bfloat16):
+        k = (torch.randn(5, Hkv, D, generator=g) * 3).to(dtype)
+        v = (torch.randn(5, Hkv, D, generator=g) * 3).to(dtype)
+        ks = torch.tensor([0.01, 0.02, 0.05])
+        vs = torch.tensor([0.03, 0.015, 0.04])
+        kc = torch.full((N, Hkv, B, D), 0xAB, dtype=torch.uint8)
+        vc = kc.clone()
+        slots = torch.tensor([21, -1, 2, 9, 15])
+        oracle.reshape_and_cache_e4m3(k, v, kc, vc, slots, B, ks, vs, lib=lib)
+        want_k = torch.full_like(kc, 0xAB)
+        want_v = torch.full_like(vc, 0xAB)
+        for i, sl in enumerate(slots.tolist()):
+            if sl < 0:
+                continue
+            qk = (k[i].float() / ks[:, None]).clamp(-448, 448)
+            qv = (v[i].float() / vs[:, None]).clamp(-448, 448)
+            want_k[sl // B, :, sl % B] = qk.to(torch.float8_e4m3fn).view(torch.uint8)
+            want_v[sl // B, :, sl % B] = qv.to(torch.float8_e4m3fn).view(torch.uint8)
+        assert torch.equal(kc, want_k) and torch.equal(vc, want_v)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

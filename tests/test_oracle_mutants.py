@@ -40,6 +40,19 @@ MUTANTS = {
         "memcpy(pool + pairs[2 * p + 1] * block_bytes, pool + pairs[2 * p] * block_bytes,"),
     "reshape_wrong_block": ("int64_t blk = slot / block_size;\n",
                             "int64_t blk = (slot / block_size) ^ 1;\n"),
+    "e4m3_bias": ("mag = ldexp((double)(8 + frac), expo - 10);",
+                  "mag = ldexp((double)(8 + frac), expo - 9);"),
+    "e4m3_subnormal": ("mag = ldexp((double)frac, -9);", "mag = ldexp((double)frac, -10);"),
+    "e4m3_ties_away": ("if (d < best_d || (d == best_d && (c & 1) == 0)) {",
+                       "if (d <= best_d) {"),
+    "e4m3_nan_saturates": ("    if (isnan(x))\n        return 0x7f;\n",
+                           "    if (isnan(x))\n        return 0x7e;\n"),
+    "e4m3_scale_multiplied": ("k_cache[dst + d] = orc_f32_to_e4m3(kx / k_scale[h]);",
+                              "k_cache[dst + d] = orc_f32_to_e4m3(kx * k_scale[h]);"),
+    "dequant_scale_dropped": ("const double ks = k_scale ? (double)k_scale[hk] : 1.0;",
+                              "const double ks = 1.0;"),
+    "dequant_wrong_head_scale": ("const double vs = v_scale ? (double)v_scale[hk] : 1.0;",
+                                 "const double vs = v_scale ? (double)v_scale[0] : 1.0;"),
 }
 
 
