@@ -44,7 +44,12 @@ WORKLOADS = {
     "prefix": "shared-prefix decode: 16 groups x 8 seqs, 32 q / 8 kv heads, head_dim 128, bf16, "
               "block_size 16, 1024-token shared prefix, CoW tail copies each step",
 }
-DTYPE_NAME = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}
+# the same shapes over E4M3 caches with per-kv-head scales (queries and new K/V in the
+# model dtype; the step's cache write quantises)
+for _name in ("llama13b", "opt13b", "long16", "long32", "prefix"):
+    WORKLOADS[_name + "_fp8"] = WORKLOADS[_name] + "; KV cache in FP8 E4M3 with per-head scales"
+DTYPE_NAME = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32",
+              torch.float8_e4m3fn: "fp8_e4m3"}
 METRIC = "paged decode attention KV GB/s"
 KERNEL_SRC = os.path.join(ROOT, "paged_kv_cache_119_gb300", "csrc", "decode_kernel.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.md")
@@ -130,16 +135,17 @@ def recorded_traffic(config: str):
 
 def algorithmic_bytes(w) -> dict:
     """Bytes a decode step must move at minimum (each cached K/V byte read once)."""
-    esz = torch.tensor([], dtype=w.dtype).element_size()
+    esz = torch.tensor([], dtype=w.dtype).element_size()       # q, out, new K/V
+    csz = w.k_cache.element_size()                              # cache elements
     lens = w.context_lens.tolist()
     kv = w.kv_bytes()
     qo = 2 * w.num_seqs * w.num_q_heads * w.head_dim * esz
     tables = 4 * sum(math.ceil(L / w.block_size) for L in lens) + 4 * w.num_seqs
     T = w.slot_mapping.numel()
-    reshape = 2 * 2 * T * w.num_kv_heads * w.head_dim * esz + 8 * T
+    reshape = 2 * T * w.num_kv_heads * w.head_dim * (esz + csz) + 8 * T
     copies = 0
     if w.copy_pairs is not None:
-        copies = 2 * 2 * len(w.copy_pairs) * w.num_kv_heads * w.block_size * w.head_dim * esz
+        copies = 2 * 2 * len(w.copy_pairs) * w.num_kv_heads * w.block_size * w.head_dim * csz
     return {"kv": kv, "decode": kv + qo + tables, "reshape": reshape, "copy": copies,
             "step": kv + qo + tables + reshape + copies}
 
@@ -195,7 +201,32 @@ class ClockSampler:
 def make_workload(config: str, device, num_seqs=None):
     from paged_kv_cache_119_gb300 import workloads
     kw = {} if num_seqs is None else {"num_seqs": num_seqs}
+    if config.endswith("_fp8"):
+        return workloads.to_fp8(workloads.make(config[:-4], device=device, **kw))
     return workloads.make(config, device=device, **kw)
+
+
+def step_ops(pa, w):
+    """(cache write, decode) callables of the library for this workload's cache type."""
+    if w.fp8:
+        ks, vs = w.meta["k_scale"], w.meta["v_scale"]
+
+        def write(k, v, slots):
+            pa.pa_reshape_and_cache_fp8(k, v, w.k_cache, w.v_cache, slots, ks, vs)
+
+        def decode(out, q, bt, cl, part, ws):
+            pa.pa_decode_fp8(out, q, w.k_cache, w.v_cache, ks, vs, bt, cl, w.scale,
+                             w.num_kv_heads, w.block_size, max_context_len=w.max_context_len,
+                             partition_size=part, workspace=ws)
+    else:
+        def write(k, v, slots):
+            pa.pa_reshape_and_cache(k, v, w.k_cache, w.v_cache, slots)
+
+        def decode(out, q, bt, cl, part, ws):
+            pa.pa_decode(out, q, w.k_cache, w.v_cache, bt, cl, w.scale, w.num_kv_heads,
+                         w.block_size, max_context_len=w.max_context_len, partition_size=part,
+                         workspace=ws)
+    return write, decode
 
 
 # ------------------------------------------------------------------------------ our arm
@@ -225,17 +256,17 @@ def run_ours(args, rank, world, local):
         pa.pa_copy_blocks([w.k_cache], [w.v_cache], w.copy_pairs)
         cow_src = w.copy_pairs.copy()
 
+    write, decode = step_ops(pa, w)
+
     def step(e=None):
         if cow_src is not None:
             pa.pa_copy_blocks([w.k_cache], [w.v_cache], cow_src)
         if e is not None:
             e[0].record()
-        pa.pa_reshape_and_cache(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping)
+        write(w.k_new, w.v_new, w.slot_mapping)
         if e is not None:
             e[1].record()
-        pa.pa_decode(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale,
-                     w.num_kv_heads, w.block_size, max_context_len=w.max_context_len,
-                     partition_size=part, workspace=ws)
+        decode(out, w.q, w.block_tables, w.context_lens, part, ws)
         if e is not None:
             e[2].record()
 
@@ -296,7 +327,7 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[w.dtype],
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[w.k_cache.dtype],
         "data": "synthetic",
         "config": {"workload": WORKLOADS[args.config], "name": args.config,
                    "num_seqs": w.num_seqs, "kv_bytes_per_step": nbytes["kv"],
@@ -338,14 +369,13 @@ def measure_e2e(args, pa, w, out, ws, part, dev):
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_host.numel() * out_host.element_size()
 
+    write, decode = step_ops(pa, w)
+
     def step():
         for n in names:
             devb[n].copy_(host[n], non_blocking=True)
-        pa.pa_reshape_and_cache(devb["k_new"], devb["v_new"], w.k_cache, w.v_cache,
-                                devb["slot_mapping"])
-        pa.pa_decode(out, devb["q"], w.k_cache, w.v_cache, devb["block_tables"],
-                     devb["context_lens"], w.scale, w.num_kv_heads, w.block_size,
-                     max_context_len=w.max_context_len, partition_size=part, workspace=ws)
+        write(devb["k_new"], devb["v_new"], devb["slot_mapping"])
+        decode(out, devb["q"], devb["block_tables"], devb["context_lens"], part, ws)
         out_host.copy_(out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
@@ -365,23 +395,29 @@ def measure_e2e(args, pa, w, out, ws, part, dev):
 # ------------------------------------------------------------------------------ oracle arms
 
 def _host_inputs(w):
-    return {n: getattr(w, n).cpu() for n in ("q", "k_cache", "v_cache", "k_new", "v_new",
-                                             "slot_mapping", "block_tables", "context_lens")}
+    h = {n: getattr(w, n).cpu() for n in ("q", "k_cache", "v_cache", "k_new", "v_new",
+                                          "slot_mapping", "block_tables", "context_lens")}
+    if w.fp8:
+        h["k_scale"], h["v_scale"] = w.meta["k_scale"].cpu(), w.meta["v_scale"].cpu()
+    return h
 
 
 def _oracle_step(h, w, seqs, threads):
     """The oracle's step on sequences [0, seqs): reshape of their new tokens, then decode."""
     import oracle
     nt = sum(1 for (s, _) in w.meta["new_tokens"] if s < seqs)
-    oracle.reshape_and_cache(h["k_new"][:nt], h["v_new"][:nt], h["k_cache"], h["v_cache"],
-                             h["slot_mapping"][:nt], w.block_size)
-    oracle.paged_attention(h["q"][:seqs], h["k_cache"], h["v_cache"], h["block_tables"][:seqs],
-                           h["context_lens"][:seqs], w.scale, w.num_kv_heads, w.block_size,
-                           num_threads=threads)
+    if w.fp8:
+        oracle.reshape_and_cache_e4m3(h["k_new"][:nt], h["v_new"][:nt], h["k_cache"],
+                                      h["v_cache"], h["slot_mapping"][:nt], w.block_size,
+                                      h["k_scale"], h["v_scale"])
+    else:
+        oracle.reshape_and_cache(h["k_new"][:nt], h["v_new"][:nt], h["k_cache"], h["v_cache"],
+                                 h["slot_mapping"][:nt], w.block_size)
+    _decode_slice(h, w, 0, seqs, threads)
 
 
 def _sample_bytes(w, seqs):
-    esz = torch.tensor([], dtype=w.dtype).element_size()
+    esz = w.k_cache.element_size()
     return int(sum(w.context_lens.tolist()[:seqs])) * w.num_kv_heads * 2 * w.head_dim * esz
 
 
@@ -417,7 +453,8 @@ def _decode_slice(h, w, s0, s1, threads):
     import oracle
     oracle.paged_attention(h["q"][s0:s1], h["k_cache"], h["v_cache"], h["block_tables"][s0:s1],
                            h["context_lens"][s0:s1], w.scale, w.num_kv_heads, w.block_size,
-                           num_threads=threads)
+                           num_threads=threads, k_scale=h.get("k_scale"),
+                           v_scale=h.get("v_scale"))
 
 
 def run_reference(args, rank, world):

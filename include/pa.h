@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_FP8_E4M3 = 3 } pa_dtype;
 
 typedef enum {
     PA_OK = 0,
@@ -181,6 +181,43 @@ int pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_ca
 int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
                    const int64_t* src_dst_pairs_host, int64_t num_pairs, int64_t block_bytes,
                    int64_t num_blocks, void* stream);
+
+/*
+ * FP8 KV cache (OCP E4M3: 4 exponent bits, bias 7, 3 fraction bits, largest finite
+ * magnitude 448, no infinities).  A cache element is a one-byte code c; its value is
+ * e4m3(c) * scale[h], with one fp32 scale per kv head for K (k_scale[Hkv]) and one
+ * for V (v_scale[Hkv]), both DEVICE arrays owned by the caller.  Quantising halves
+ * the bytes of the bandwidth-bound decode (the write-ups list FP8 KV caches among
+ * the later vLLM optimisations: "PagedAttention 完全拆解", section 局限与未解决的问题,
+ * item 6).  Layouts are those of pa.h's 16-bit caches with one byte per element.
+ *
+ * pa_reshape_and_cache_fp8: for each token i with slot = slot_mapping[i] >= 0 and each
+ * kv head h, k_cache[slot / B][h][slot % B][d] = e4m3(fp32(k[i][h][d]) / k_scale[h]),
+ * likewise v: IEEE fp32 division, round to the nearest code with ties to even,
+ * magnitudes beyond 448 saturate to +-448, NaN stays NaN.  src_dtype: PA_F32, PA_F16
+ * or PA_BF16 (the type of k and v).  head_dim must be a multiple of 16.  Errors and
+ * slot checks as in pa_reshape_and_cache.
+ */
+int pa_reshape_and_cache_fp8(const void* k, const void* v, pa_dtype src_dtype, void* k_cache,
+                             void* v_cache, const float* k_scale, const float* v_scale,
+                             const int64_t* slot_mapping, int64_t num_tokens,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                             int64_t num_blocks, void* stream);
+
+/*
+ * pa_decode_fp8: pa_decode over E4M3 caches.  q (and a native-dtype out) have
+ * q_dtype, PA_F16 or PA_BF16; out_dtype is PA_F32 or q_dtype.  Scores use the
+ * dequantised keys (q . (c_k * k_scale[h])) and the output the dequantised values;
+ * accumulation is fp32 as in pa_decode.  All other arguments, the split rules and
+ * the workspace are those of pa_decode (pa_decode_workspace_bytes gives the size).
+ */
+int pa_decode_fp8(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
+                  const void* k_cache, const void* v_cache, const float* k_scale,
+                  const float* v_scale, int64_t num_blocks, const int32_t* block_tables,
+                  int64_t block_table_stride, const int32_t* context_lens,
+                  int32_t max_context_len, int32_t num_seqs, int32_t num_q_heads,
+                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size, float scale,
+                  int32_t partition_size, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Reads and clears the calling device's error word (PA_DEVERR_* bits).

@@ -15,7 +15,8 @@ into the library raises if ``libpa.so`` is missing.
 """
 __version__ = "0.1.0"
 
-_API = ("pa_decode", "pa_decode_noalloc", "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_workspace_bytes",
+_API = ("pa_decode", "pa_decode_noalloc", "pa_decode_fp8", "pa_reshape_and_cache",
+        "pa_reshape_and_cache_fp8", "pa_copy_blocks", "pa_decode_workspace_bytes",
         "pa_get_device_error", "pa_version")
 
 __all__ = list(_API) + ["workloads", "build"]

@@ -11,7 +11,7 @@ from . import build as _build
 _lock = threading.Lock()
 _lib = None
 
-PA_F32, PA_F16, PA_BF16 = 0, 1, 2
+PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2, 3
 PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0, -1, -2, -3, -4
 PA_DEVERR_BLOCK_ID, PA_DEVERR_CONTEXT_LEN, PA_DEVERR_SLOT, PA_DEVERR_TIMEOUT = 1, 2, 4, 8
 PA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -27,6 +27,11 @@ SIGNATURES = {
     "pa_decode_noalloc": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp, _vp, ctypes.c_int, _i64, _vp,
                                          _i64, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32,
                                          _i32, _vp]),
+    "pa_decode_fp8": (ctypes.c_int, [_vp, ctypes.c_int, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _i64,
+                                     _vp, _i64, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32,
+                                     _vp, _sz, _vp]),
+    "pa_reshape_and_cache_fp8": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp,
+                                                _i64, _i32, _i32, _i32, _i64, _vp]),
     "pa_reshape_and_cache": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i64,
                                             ctypes.c_int, _vp]),
     "pa_copy_blocks": (ctypes.c_int, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32,

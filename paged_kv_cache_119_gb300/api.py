@@ -179,6 +179,83 @@ def pa_copy_blocks(k_caches, v_caches, src_dst_pairs, stream=None) -> None:
     N.check("pa_copy_blocks", status)
 
 
+def _fp8_cache(name: str, t: torch.Tensor) -> None:
+    _cuda(name, t)
+    if t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+        raise TypeError(f"{name} must hold E4M3 codes (torch.float8_e4m3fn or uint8)")
+
+
+def _scales(k_scale, v_scale, num_kv_heads):
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        _cuda(name, t)
+        if t.dtype != torch.float32 or t.shape != (num_kv_heads,):
+            raise ValueError(f"{name} must be float32 [num_kv_heads]")
+
+
+def pa_reshape_and_cache_fp8(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
+                             v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                             k_scale: torch.Tensor, v_scale: torch.Tensor, stream=None) -> None:
+    """Quantising cache write: k_cache[slot / B][h][slot % B] = e4m3(fp32(k[i][h]) / k_scale[h])
+    (round to nearest even, saturating at +-448), likewise v.  k, v [T, Hkv, D] in fp32 /
+    fp16 / bf16; caches [N, Hkv, B, D] of E4M3 codes; scales float32 [Hkv]."""
+    for name, t in (("k", k), ("v", v), ("slot_mapping", slot_mapping)):
+        _cuda(name, t)
+    _fp8_cache("k_cache", k_cache)
+    _fp8_cache("v_cache", v_cache)
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    T, Hkv, D = k.shape
+    if v.shape != k.shape or v.dtype != k.dtype or k_cache.shape != v_cache.shape or \
+            k_cache.dim() != 4 or (k_cache.shape[1], k_cache.shape[3]) != (Hkv, D):
+        raise ValueError("k, v must be [T, Hkv, D] and caches [N, Hkv, B, D]")
+    _scales(k_scale, v_scale, Hkv)
+    status = N.load().pa_reshape_and_cache_fp8(
+        k.data_ptr(), v.data_ptr(), _dtype(k), k_cache.data_ptr(), v_cache.data_ptr(),
+        k_scale.data_ptr(), v_scale.data_ptr(), slot_mapping.data_ptr(), T, Hkv, D,
+        k_cache.shape[2], k_cache.shape[0], _stream(stream))
+    N.check("pa_reshape_and_cache_fp8", status)
+
+
+def pa_decode_fp8(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                  v_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+                  block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                  num_kv_heads: int, block_size: int, max_context_len: int | None = None,
+                  partition_size: int = 0, workspace: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """pa_decode over E4M3 caches with per-kv-head scales (value = code * scale[h]).
+    q [S, Hq, D] fp16 / bf16; out fp32 or q's dtype."""
+    for name, t in (("out", out), ("q", q), ("block_tables", block_tables),
+                    ("context_lens", context_lens)):
+        _cuda(name, t)
+    _fp8_cache("k_cache", k_cache)
+    _fp8_cache("v_cache", v_cache)
+    _scales(k_scale, v_scale, num_kv_heads)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    if q.dim() != 3 or out.shape != q.shape:
+        raise ValueError("q and out must be [S, Hq, D] of one shape")
+    S, Hq, D = q.shape
+    if k_cache.shape != v_cache.shape or tuple(k_cache.shape[1:]) != (num_kv_heads, block_size, D):
+        raise ValueError("caches must be [N, Hkv, B, D]")
+    if max_context_len is None:
+        max_context_len = block_tables.shape[1] * block_size
+    ws_need = pa_decode_workspace_bytes(S, Hq, D, max_context_len, block_size,
+                                        max(partition_size, 0)) if partition_size >= 0 else 0
+    if ws_need and workspace is None:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
+    ws_ptr, ws_bytes = (0, 0) if workspace is None else (workspace.data_ptr(),
+                                                         workspace.numel() *
+                                                         workspace.element_size())
+    status = N.load().pa_decode_fp8(
+        out.data_ptr(), _dtype(out), q.data_ptr(), _dtype(q), k_cache.data_ptr(),
+        v_cache.data_ptr(), k_scale.data_ptr(), v_scale.data_ptr(), k_cache.shape[0],
+        block_tables.data_ptr(), block_tables.stride(0), context_lens.data_ptr(),
+        int(max_context_len), S, Hq, num_kv_heads, D, block_size, float(scale),
+        int(partition_size), ws_ptr, ws_bytes, _stream(stream))
+    N.check("pa_decode_fp8", status)
+    return out
+
+
 def pa_get_device_error(stream=None) -> int:
     """Read and clear the device error word (PA_DEVERR_* bits).  Synchronises."""
     flags = ctypes.c_uint32(0)

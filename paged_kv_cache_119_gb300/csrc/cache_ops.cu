@@ -61,6 +61,75 @@ cudaError_t launch_reshape_and_cache(const ReshapeParams& p, cudaStream_t stream
     return cudaGetLastError();
 }
 
+// Quantising cache write: one thread per 16 consecutive elements of a (token, head)
+// row, for K and for V; each element becomes e4m3(fp32(x) / scale[head]) (IEEE fp32
+// division, round to nearest even, saturating at +-448) and the 16 codes are stored
+// with one 16-byte store.
+template <typename TS>
+__global__ void __launch_bounds__(256) reshape_and_cache_fp8_kernel(const ReshapeFp8Params p)
+{
+    const int groups = p.head_dim / 16;
+    const int64_t per_tensor = p.num_tokens * p.num_kv_heads * groups;
+    const int64_t total = 2 * per_tensor;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const bool is_v = i >= per_tensor;
+        const int64_t j = is_v ? i - per_tensor : i;
+        const int grp = (int)(j % groups);
+        const int64_t th = j / groups;                       // token * num_kv_heads + head
+        const int h = (int)(th % p.num_kv_heads);
+        const int64_t tok = th / p.num_kv_heads;
+        const int64_t slot = p.slot_mapping[tok];
+        if (slot < 0)
+            continue;
+        if (slot >= p.num_blocks * p.block_size) {
+            if (grp == 0 && h == 0 && !is_v)
+                atomicOr(p.err, PA_DEVERR_SLOT);
+            continue;
+        }
+        const TS* src = reinterpret_cast<const TS*>(is_v ? p.v : p.k) + th * p.head_dim + grp * 16;
+        const float scale = (is_v ? p.v_scale : p.k_scale)[h];
+        float x[16];
+        Load<TS, 4>::run(src, *reinterpret_cast<float(*)[4]>(&x[0]));
+        Load<TS, 4>::run(src + 4, *reinterpret_cast<float(*)[4]>(&x[4]));
+        Load<TS, 4>::run(src + 8, *reinterpret_cast<float(*)[4]>(&x[8]));
+        Load<TS, 4>::run(src + 12, *reinterpret_cast<float(*)[4]>(&x[12]));
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+                make_float2(x[4 * k] / scale, x[4 * k + 1] / scale), __NV_SATFINITE, __NV_E4M3);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+                make_float2(x[4 * k + 2] / scale, x[4 * k + 3] / scale), __NV_SATFINITE, __NV_E4M3);
+            w[k] = lo | (hi << 16);
+        }
+        const int64_t blk = slot / p.block_size;
+        const int64_t off = slot - blk * p.block_size;
+        unsigned char* dst = (is_v ? p.v_cache : p.k_cache) +
+                             ((blk * p.num_kv_heads + h) * p.block_size + off) * p.head_dim + grp * 16;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+cudaError_t launch_reshape_and_cache_fp8(const ReshapeFp8Params& p, pa_dtype src_dtype,
+                                         cudaStream_t stream)
+{
+    const int64_t total = 2 * p.num_tokens * p.num_kv_heads * (p.head_dim / 16);
+    if (total == 0)
+        return cudaSuccess;
+    const int sms = device_sm_count();
+    const int64_t want = (total + 255) / 256;
+    const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 16;
+    const int blocks = (int)(want < cap ? want : cap);
+    switch (src_dtype) {
+    case PA_F32: reshape_and_cache_fp8_kernel<float><<<blocks, 256, 0, stream>>>(p); break;
+    case PA_F16: reshape_and_cache_fp8_kernel<__half><<<blocks, 256, 0, stream>>>(p); break;
+    case PA_BF16: reshape_and_cache_fp8_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(p); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
 // grid = (pairs, 2 * layers, splits): CTA (p, l2, s) copies the s-th slice of
 // block pairs[p].src of pool l2 (K pools first, then V pools) to pairs[p].dst.
 __global__ void __launch_bounds__(256) copy_blocks_kernel(const CopyParams p)

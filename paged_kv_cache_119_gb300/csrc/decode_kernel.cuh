@@ -109,11 +109,14 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, int64_t idx, fl
         store_as(reinterpret_cast<T*>(p.out) + idx, x);
 }
 
-template <typename T, int D, int BS, int GC, int NSTAGE>
+// T: query / native output type.  TK: cache element type (T itself, or
+// __nv_fp8_e4m3 for a quantised cache whose value is code * per-kv-head scale).
+template <typename T, typename TK, int D, int BS, int GC, int NSTAGE>
 __global__ void __launch_bounds__(kDecodeThreads)
     decode_kernel(const DecodeParams p)
 {
-    using Smem = DecodeSmem<T, D, BS, GC, NSTAGE>;
+    using Smem = DecodeSmem<TK, D, BS, GC, NSTAGE>;
+    constexpr bool kFp8 = sizeof(TK) == 1;
     constexpr int NCW = kDecodeConsumerWarps;
     constexpr int E = D / 32;                  // head dims per lane
     constexpr int TC = BS < 8 ? BS : 8;        // tokens per butterfly
@@ -123,10 +126,10 @@ __global__ void __launch_bounds__(kDecodeThreads)
     static_assert(D % 32 == 0 && (E == 2 || E == 4), "head_dim must be 64 or 128");
     static_assert(NSTAGE % NCW == 0, "each ring stage must belong to one consumer warp");
     // copy a tile to registers and release its stage early when K + V take <= 64 registers
-    constexpr bool kEarlyRelease = 2 * BS * E * (int)sizeof(T) / 4 <= 64;
+    constexpr bool kEarlyRelease = 2 * BS * E * (int)sizeof(TK) / 4 <= 64;
 
     extern __shared__ __align__(128) unsigned char smem[];
-    T* ring = reinterpret_cast<T*>(smem);
+    TK* ring = reinterpret_cast<TK*>(smem);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Smem::kBarOffset);
     uint64_t* empty = full + NSTAGE;
     int* stage_ok = reinterpret_cast<int*>(smem + Smem::kOkOffset);
@@ -178,8 +181,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
     if (warp == NCW) {
         // ------------------------------------------------------------------ producer
         const int32_t* bt_row = p.block_tables + (int64_t)seq * p.bt_stride + jb;
-        const T* kpool = reinterpret_cast<const T*>(p.k_cache) + (int64_t)kvh * kTile;
-        const T* vpool = reinterpret_cast<const T*>(p.v_cache) + (int64_t)kvh * kTile;
+        const TK* kpool = reinterpret_cast<const TK*>(p.k_cache) + (int64_t)kvh * kTile;
+        const TK* vpool = reinterpret_cast<const TK*>(p.v_cache) + (int64_t)kvh * kTile;
         const int64_t blk_stride = (int64_t)p.num_kv_heads * kTile;
         const uint64_t policy = l2_evict_first_policy();
         int next = (lane < ntiles) ? __ldg(bt_row + lane) : 0;
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
                         stage_ok[stage] = valid ? 1 : 0;
                         if (valid) {
                             const int64_t off = (int64_t)pbn * blk_stride;
-                            T* dst = ring + stage * 2 * kTile;
+                            TK* dst = ring + stage * 2 * kTile;
                             mbar_arrive_expect_tx(&full[stage], 2u * Smem::kTileBytes);
                             bulk_g2s(dst, kpool + off, Smem::kTileBytes, &full[stage], policy);
                             bulk_g2s(dst + kTile, vpool + off, Smem::kTileBytes, &full[stage], policy);
@@ -224,6 +227,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
     }
 
     // ---------------------------------------------------------------------- consumers
+    // q carries the softmax scale (base 2) and, for a quantised cache, the K scale
+    const float qscale = kFp8 ? p.scale_log2 * p.k_scale[kvh] : p.scale_log2;
     float qf[GC][E];
 #pragma unroll
     for (int g = 0; g < GC; ++g) {
@@ -232,7 +237,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
         Load<T, E>::run(qp, qf[g]);
 #pragma unroll
         for (int e = 0; e < E; ++e)
-            qf[g][e] *= p.scale_log2;
+            qf[g][e] *= qscale;
     }
     float m[GC], lsum[GC], acc[GC][E];
 #pragma unroll
@@ -262,19 +267,19 @@ __global__ void __launch_bounds__(kDecodeThreads)
                 mbar_arrive(&empty[stage]);
             continue;
         }
-        const T* Ks = ring + stage * 2 * kTile;
-        const T* Vs = Ks + kTile;
+        const TK* Ks = ring + stage * 2 * kTile;
+        const TK* Vs = Ks + kTile;
         const int nvalid = min(BS, t1 - (jb + it) * BS);
 
         // Small tiles are copied to registers and the stage is released at once, so
         // the producer refills it while this warp computes (the stage would
         // otherwise be held through the whole tile's arithmetic).
-        Raw<T, E> kr[kEarlyRelease ? BS : 1], vr[kEarlyRelease ? BS : 1];
+        Raw<TK, E> kr[kEarlyRelease ? BS : 1], vr[kEarlyRelease ? BS : 1];
         if constexpr (kEarlyRelease) {
 #pragma unroll
             for (int t = 0; t < BS; ++t) {
-                load_raw<T, E>(Ks + t * D + lane * E, kr[t]);
-                load_raw<T, E>(Vs + t * D + lane * E, vr[t]);
+                load_raw<TK, E>(Ks + t * D + lane * E, kr[t]);
+                load_raw<TK, E>(Vs + t * D + lane * E, vr[t]);
             }
             __syncwarp();
             if (lane == 0)
@@ -282,15 +287,15 @@ __global__ void __launch_bounds__(kDecodeThreads)
         }
         auto k_row = [&](int t, float (&f)[E]) {
             if constexpr (kEarlyRelease)
-                raw_to_float<T, E>(kr[t], f);
+                raw_to_float<TK, E>(kr[t], f);
             else
-                Load<T, E>::run(Ks + t * D + lane * E, f);
+                Load<TK, E>::run(Ks + t * D + lane * E, f);
         };
         auto v_row = [&](int t, float (&f)[E]) {
             if constexpr (kEarlyRelease)
-                raw_to_float<T, E>(vr[t], f);
+                raw_to_float<TK, E>(vr[t], f);
             else
-                Load<T, E>::run(Vs + t * D + lane * E, f);
+                Load<TK, E>::run(Vs + t * D + lane * E, f);
         };
 
         // scores s[g][c] for token c * TC + mytok, base-2 units
@@ -405,6 +410,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
     named_barrier(1, NCW * 32);
 
     const bool bad = *poison != 0;
+    const float oscale = kFp8 ? p.v_scale[kvh] : 1.f;     // V scale of a quantised cache
     for (int idx = threadIdx.x; idx < GC * D; idx += NCW * 32) {
         const int g = idx / D;
         const int d = idx - g * D;
@@ -422,6 +428,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
             }
         }
         float o = den > 0.f ? num / den : 0.f;
+        if constexpr (kFp8)
+            o *= oscale;
         if (bad)
             o = __int_as_float(0x7fc00000);
         const int64_t row = (int64_t)seq * p.num_q_heads + h0 + g;
@@ -478,7 +486,7 @@ __global__ void __launch_bounds__(D) reduce_kernel(const DecodeParams p)
 // a parity wait can succeed a full phase early.)
 template <typename T, int D, int BS>
 struct DecodeStages {
-    static constexpr int kStageBytes = 2 * BS * D * (int)sizeof(T);
+    static constexpr int kStageBytes = 2 * BS * D * (int)sizeof(T);   // T: cache element type
     static constexpr int kPerWarp = 65536 / (kDecodeConsumerWarps * kStageBytes);
     static constexpr int value =
         kDecodeConsumerWarps * (kPerWarp < 1 ? 1 : (kPerWarp > 3 ? 3 : kPerWarp));
@@ -513,11 +521,11 @@ inline int kernel_occupancy(const void* kernel, int smem_bytes)
     return n;
 }
 
-template <typename T, int D, int BS, int GC>
+template <typename T, typename TK, int D, int BS, int GC>
 struct CoreVariant {
-    static constexpr int kStages = DecodeStages<T, D, BS>::value;
-    using Smem = DecodeSmem<T, D, BS, GC, kStages>;
-    static constexpr auto kernel() { return decode_kernel<T, D, BS, GC, kStages>; }
+    static constexpr int kStages = DecodeStages<TK, D, BS>::value;
+    using Smem = DecodeSmem<TK, D, BS, GC, kStages>;
+    static constexpr auto kernel() { return decode_kernel<T, TK, D, BS, GC, kStages>; }
     static cudaError_t configure()
     {
         return configure_once(reinterpret_cast<const void*>(kernel()), Smem::kBytes);
@@ -543,29 +551,53 @@ struct CoreVariant {
     X(128, 32, 4) X(128, 32, 8) X(64, 16, 1) X(64, 16, 2) X(64, 16, 4) X(64, 16, 8)     \
     X(64, 32, 1) X(64, 32, 2) X(64, 32, 4) X(64, 32, 8)
 
-template <typename T>
+// Whether the CUDA-core kernel serves this many heads per CTA for cache type TK:
+// 16-bit and E4M3 caches use the tensor-core kernel from kMmaMinHeads heads on,
+// so those variants are never built.
+template <typename TK, int GC>
+constexpr bool core_serves() { return sizeof(TK) == 4 || GC < kMmaMinHeads; }
+
+template <typename T, typename TK, int D, int BS, int GC>
+cudaError_t launch_core(const DecodeParams& p, cudaStream_t stream)
+{
+    if constexpr (core_serves<TK, GC>())
+        return CoreVariant<T, TK, D, BS, GC>::launch(p, stream);
+    else
+        return cudaErrorInvalidValue;
+}
+
+template <typename T, typename TK, int D, int BS, int GC>
+int occupancy_core()
+{
+    if constexpr (core_serves<TK, GC>()) {
+        using V = CoreVariant<T, TK, D, BS, GC>;
+        return V::configure() == cudaSuccess
+                   ? kernel_occupancy(reinterpret_cast<const void*>(V::kernel()), V::Smem::kBytes)
+                   : 0;
+    } else {
+        return 0;
+    }
+}
+
+template <typename T, typename TK = T>
 cudaError_t launch_decode_typed(const DecodeParams& p, int head_dim, int block_size, int gc,
                                 cudaStream_t stream)
 {
 #define PA_CORE_CASE(D_, BS_, GC_)                                   \
     if (head_dim == D_ && block_size == BS_ && gc == GC_)            \
-        return CoreVariant<T, D_, BS_, GC_>::launch(p, stream);
+        return launch_core<T, TK, D_, BS_, GC_>(p, stream);
     PA_CORE_VARIANTS(PA_CORE_CASE)
 #undef PA_CORE_CASE
     return cudaErrorInvalidValue;
 }
 
 // Resident CTAs per SM of the CUDA-core kernel for this shape (0 if unknown).
-template <typename T>
+template <typename T, typename TK = T>
 int occupancy_decode_typed(int head_dim, int block_size, int gc)
 {
 #define PA_CORE_OCC(D_, BS_, GC_)                                    \
-    if (head_dim == D_ && block_size == BS_ && gc == GC_) {          \
-        using V = CoreVariant<T, D_, BS_, GC_>;                      \
-        return V::configure() == cudaSuccess                         \
-                   ? kernel_occupancy(reinterpret_cast<const void*>(V::kernel()), V::Smem::kBytes) \
-                   : 0;                                              \
-    }
+    if (head_dim == D_ && block_size == BS_ && gc == GC_)            \
+        return occupancy_core<T, TK, D_, BS_, GC_>();
     PA_CORE_VARIANTS(PA_CORE_OCC)
 #undef PA_CORE_OCC
     return 0;

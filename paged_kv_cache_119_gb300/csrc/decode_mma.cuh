@@ -118,30 +118,86 @@ struct Mma<__half> {
     }
 };
 
-template <typename T, int D, int BS, int NSTAGE>
+// Converts one raw E4M3 tile [B][D] (row-major bytes) into the 128-byte-swizzled
+// 16-bit layout the tensor-map TMA produces: D/64 regions of B rows x 128 bytes,
+// the 16-byte chunk j of row r stored at chunk position j ^ (r & 7).  One lane per
+// 64-element half row; E4M3 -> f16 is exact and so is f16 -> bf16 for these values.
+template <typename T, int D, int BS>
+__device__ __forceinline__ void convert_e4m3_tile(const unsigned char* src, unsigned char* dst,
+                                                  int lane)
+{
+    constexpr int HALVES = D / 64;
+#pragma unroll
+    for (int hr = lane; hr < BS * HALVES; hr += 32) {
+        const int r = hr / HALVES;
+        const int h = hr - r * HALVES;
+        const uint4* in = reinterpret_cast<const uint4*>(src + r * D + h * 64);
+        unsigned char* out_row = dst + h * (BS * 128) + r * 128;
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+            const uint4 w = in[q];                         // 16 codes -> chunks 2q, 2q+1
+            const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+            uint32_t packed[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {                  // 2 codes per packed 32-bit word
+                const __half2_raw hv =
+                    __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(words[i / 2] >> (16 * (i % 2))),
+                                               __NV_E4M3);
+                if constexpr (DType<T>::id == PA_F16) {
+                    packed[i] = *reinterpret_cast<const uint32_t*>(&hv);
+                } else {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hv));
+                    __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+                    packed[i] = *reinterpret_cast<const uint32_t*>(&b);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int j = 2 * q + k;
+                *reinterpret_cast<uint4*>(out_row + ((j ^ (r & 7)) << 4)) =
+                    make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
+            }
+        }
+    }
+}
+
+// Shared memory of the tensor-core kernel.  16-bit caches: the ring holds the
+// swizzled K and V tiles the tensor-map TMA writes.  E4M3 caches: the ring holds
+// the raw one-byte tiles (1-D bulk copies) and each consumer warp owns a staging
+// pair of 16-bit swizzled tiles, in the same layout, that it converts them into.
+template <typename TK, int D, int BS, int NSTAGE>
 struct MmaSmem {
+    static constexpr bool kFp8 = sizeof(TK) == 1;
     static constexpr int kHalfBytes = BS * 128;                // one 64-dim box: B rows x 128 B
-    static constexpr int kTileBytes = (D / 64) * kHalfBytes;   // K (or V) of one block
-    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kTileBytes = (D / 64) * kHalfBytes;   // one 16-bit K (or V) tile
+    static constexpr int kScratchBytes = kFp8 ? kDecodeConsumerWarps * 2 * kTileBytes : 0;
+    static constexpr int kFp8TileBytes = BS * D;               // one E4M3 K (or V) tile
+    static constexpr int kStageBytes = kFp8 ? 2 * kFp8TileBytes : 2 * kTileBytes;
+    static constexpr int kRingOffset = kScratchBytes;
     static constexpr int kRingBytes = NSTAGE * kStageBytes;
-    static constexpr int kBarOffset = kRingBytes;
+    static constexpr int kBarOffset = kRingOffset + kRingBytes;
     static constexpr int kOkOffset = kBarOffset + 2 * NSTAGE * 8;
     static constexpr int kFlagOffset = kOkOffset + NSTAGE * 4;
     static constexpr int kBytes = kFlagOffset + 16;
     static constexpr int kAlloc = kBytes + 1024;                 // room to align the ring to 1 KB
-    // merge area, aliased onto the ring once every tile is consumed
+    // merge area at offset 0 (the ring, or the staging tiles), reused once every tile
+    // is consumed
     static constexpr int kMergeAcc = kDecodeConsumerWarps * 8 * D * 4;
     static constexpr int kMergeBytes = kMergeAcc + kDecodeConsumerWarps * 8 * 2 * 4;
-    static_assert(kMergeBytes <= kRingBytes, "merge area must fit in the ring");
+    static_assert(kMergeBytes <= (kFp8 ? kScratchBytes : kRingBytes), "merge area must fit");
     static_assert(kHalfBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
 };
 
-template <typename T, int D, int BS, int NH, int NSTAGE>
+// T: query / native output type (the mma operand type).  TK: cache element type,
+// T itself (tiles by tensor-map TMA) or __nv_fp8_e4m3 (raw tiles by 1-D bulk copy,
+// converted exactly to T in shared memory; the value is code * per-kv-head scale).
+template <typename T, typename TK, int D, int BS, int NH, int NSTAGE>
 __global__ void __launch_bounds__(kDecodeThreads)
     decode_mma_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv)
 {
-    using Sm = MmaSmem<T, D, BS, NSTAGE>;
+    using Sm = MmaSmem<TK, D, BS, NSTAGE>;
+    constexpr bool kFp8 = Sm::kFp8;
     constexpr int NCW = kDecodeConsumerWarps;
     constexpr int KS = D / 16;        // k-steps of the score product / m-blocks of P.V
     constexpr int MB = BS / 16;       // 16-token row blocks per tile
@@ -195,7 +251,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
         *poison = 0;
         fence_mbar_init();
     }
-    if (warp == NCW && lane == 0) {
+    if (!kFp8 && warp == NCW && lane == 0) {
         prefetch_tensormap(&tk);
         prefetch_tensormap(&tv);
     }
@@ -226,15 +282,25 @@ __global__ void __launch_bounds__(kDecodeThreads)
                         const bool valid = pbn >= 0 && (int64_t)pbn < p.num_blocks;
                         stage_ok[stage] = valid ? 1 : 0;
                         if (valid) {
-                            unsigned char* dst = smem + stage * Sm::kStageBytes;
-                            const int z = pbn * p.num_kv_heads + kvh;   // < 2^31: N * Hkv rows of tiles
+                            unsigned char* dst = smem + Sm::kRingOffset + stage * Sm::kStageBytes;
                             mbar_arrive_expect_tx(&full[stage], Sm::kStageBytes);
+                            if constexpr (kFp8) {
+                                const int64_t off =
+                                    ((int64_t)pbn * p.num_kv_heads + kvh) * Sm::kFp8TileBytes;
+                                bulk_g2s(dst, reinterpret_cast<const unsigned char*>(p.k_cache) + off,
+                                         Sm::kFp8TileBytes, &full[stage], policy);
+                                bulk_g2s(dst + Sm::kFp8TileBytes,
+                                         reinterpret_cast<const unsigned char*>(p.v_cache) + off,
+                                         Sm::kFp8TileBytes, &full[stage], policy);
+                            } else {
+                                const int z = pbn * p.num_kv_heads + kvh;   // < 2^31 (checked on the host)
 #pragma unroll
-                            for (int h = 0; h < D / 64; ++h) {
-                                tma_load_3d(dst + h * Sm::kHalfBytes, &tk, 64 * h, 0, z, &full[stage],
-                                            policy);
-                                tma_load_3d(dst + Sm::kTileBytes + h * Sm::kHalfBytes, &tv, 64 * h, 0,
-                                            z, &full[stage], policy);
+                                for (int h = 0; h < D / 64; ++h) {
+                                    tma_load_3d(dst + h * Sm::kHalfBytes, &tk, 64 * h, 0, z,
+                                                &full[stage], policy);
+                                    tma_load_3d(dst + Sm::kTileBytes + h * Sm::kHalfBytes, &tv, 64 * h,
+                                                0, z, &full[stage], policy);
+                                }
                             }
                         } else {
                             atomicOr(p.err, PA_DEVERR_BLOCK_ID);
@@ -276,7 +342,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
         for (int j = 0; j < 4; ++j)
             o[i][j] = 0.f;
     bool poisoned = false;
-    const float sl2 = p.scale_log2;
+    // scores carry the softmax scale (base 2) and, for a quantised cache, the K scale
+    const float sl2 = kFp8 ? p.scale_log2 * p.k_scale[kvh] : p.scale_log2;
 
     for (int it = warp; it < ntiles; it += NCW) {
         const int stage = it % NSTAGE;
@@ -293,8 +360,24 @@ __global__ void __launch_bounds__(kDecodeThreads)
                 mbar_arrive(&empty[stage]);
             continue;
         }
-        const uint32_t kbase = smem_addr(smem + stage * Sm::kStageBytes);
-        const uint32_t vbase = kbase + Sm::kTileBytes;
+        uint32_t kbase, vbase;
+        if constexpr (kFp8) {
+            // convert the raw tiles into this warp's swizzled 16-bit staging tiles
+            // (E4M3 -> T is exact), then hand the stage back to the producer
+            unsigned char* stg = smem + warp * 2 * Sm::kTileBytes;
+            const unsigned char* raw = smem + Sm::kRingOffset + stage * Sm::kStageBytes;
+            __syncwarp();                      // the previous tile's ldmatrix reads are done
+            convert_e4m3_tile<T, D, BS>(raw, stg, lane);
+            convert_e4m3_tile<T, D, BS>(raw + Sm::kFp8TileBytes, stg + Sm::kTileBytes, lane);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[stage]);
+            kbase = smem_addr(stg);
+            vbase = kbase + Sm::kTileBytes;
+        } else {
+            kbase = smem_addr(smem + stage * Sm::kStageBytes);
+            vbase = kbase + Sm::kTileBytes;
+        }
         const int nvalid = min(BS, t1 - (jb + it) * BS);
 
 #pragma unroll
@@ -378,13 +461,15 @@ __global__ void __launch_bounds__(kDecodeThreads)
                 Mma<T>::run(o[i], a, bl0, bl1);
             }
         }
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&empty[stage]);
+        if constexpr (!kFp8) {
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[stage]);
+        }
     }
 
     // ------------------------------------------------------------- merge the warps
-    named_barrier(1, NCW * 32);            // every tile consumed: the ring is free
+    named_barrier(1, NCW * 32);            // every tile consumed: the ring / staging is free
     float* mrg_acc = reinterpret_cast<float*>(smem);                    // [NCW][8][D]
     float* mrg_ml = mrg_acc + NCW * 8 * D;                               // [NCW][8][2]
 #pragma unroll
@@ -428,6 +513,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
             }
         }
         float out = den > 0.f ? num / den : 0.f;
+        if constexpr (kFp8)
+            out *= p.v_scale[kvh];
         if (bad)
             out = __int_as_float(0x7fc00000);
         const int64_t row = (int64_t)seq * p.num_q_heads + h0 + h;
@@ -444,20 +531,21 @@ __global__ void __launch_bounds__(kDecodeThreads)
     }
 }
 
-// Ring depth of the tensor-core kernel: one stage per consumer warp.  The
-// consumers need little time per tile, so a shallow ring and more resident CTAs
-// per SM beat a deeper ring (measured on GB300: 75 vs 95 us for the shared-prefix
-// decode, 175 vs 194 us for the 8 x 32768-token decode at 2048-token partitions).
-template <typename T, int D, int BS>
+// Ring depth of the tensor-core kernel: one stage per consumer warp for 16-bit
+// caches (the consumers need little time per tile, so a shallow ring and more
+// resident CTAs per SM beat a deeper ring: measured on GB300, 75 vs 95 us for the
+// shared-prefix decode and 175 vs 194 us for the 8 x 32768-token decode), two for
+// E4M3 caches, whose stages are half the size.
+template <typename TK, int D, int BS>
 struct MmaStages {
-    static constexpr int value = kDecodeConsumerWarps;
+    static constexpr int value = kDecodeConsumerWarps * (sizeof(TK) == 1 ? 2 : 1);
 };
 
-template <typename T, int D, int BS, int NH>
+template <typename T, typename TK, int D, int BS, int NH>
 struct MmaVariant {
-    static constexpr int kStages = MmaStages<T, D, BS>::value;
-    using Sm = MmaSmem<T, D, BS, kStages>;
-    static constexpr auto kernel() { return decode_mma_kernel<T, D, BS, NH, kStages>; }
+    static constexpr int kStages = MmaStages<TK, D, BS>::value;
+    using Sm = MmaSmem<TK, D, BS, kStages>;
+    static constexpr auto kernel() { return decode_mma_kernel<T, TK, D, BS, NH, kStages>; }
     static cudaError_t configure()
     {
         return configure_once(reinterpret_cast<const void*>(kernel()), Sm::kAlloc);
@@ -479,39 +567,42 @@ struct MmaVariant {
     }
 };
 
-// Tensor-core path for 16-bit caches (1, 2, 4 or 8 query heads per CTA).
+// Tensor-core path (4 or 8 query heads per CTA; the kernel also takes 1 or 2, but
+// the CUDA-core kernel serves those, as measured faster for MHA).  T: the 16-bit query type;
+// TK: T, or __nv_fp8_e4m3 for a quantised cache (no tensor maps needed then).
 #define PA_MMA_VARIANTS(X)                                                                    \
-    X(128, 16, 8) X(128, 16, 4) X(128, 16, 2) X(128, 16, 1) X(128, 32, 8) X(128, 32, 4)         \
-    X(128, 32, 2) X(128, 32, 1) X(64, 16, 8) X(64, 16, 4) X(64, 16, 2) X(64, 16, 1) X(64, 32, 8) \
-    X(64, 32, 4) X(64, 32, 2) X(64, 32, 1)
+    X(128, 16, 8) X(128, 16, 4) X(128, 32, 8) X(128, 32, 4) X(64, 16, 8) X(64, 16, 4)           \
+    X(64, 32, 8) X(64, 32, 4)
 
-template <typename T>
+template <typename T, typename TK = T>
 cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, int block_size, int gc,
                               cudaStream_t stream)
 {
-    CUtensorMap tk, tv;
-    cudaError_t e = kv_tensor_map(&tk, p.k_cache, p.num_blocks, p.num_kv_heads, block_size,
-                                  head_dim, DType<T>::id);
-    if (e == cudaSuccess)
-        e = kv_tensor_map(&tv, p.v_cache, p.num_blocks, p.num_kv_heads, block_size, head_dim,
-                          DType<T>::id);
-    if (e != cudaSuccess)
-        return e;
+    CUtensorMap tk{}, tv{};
+    if constexpr (sizeof(TK) == 2) {
+        cudaError_t e = kv_tensor_map(&tk, p.k_cache, p.num_blocks, p.num_kv_heads, block_size,
+                                      head_dim, DType<TK>::id);
+        if (e == cudaSuccess)
+            e = kv_tensor_map(&tv, p.v_cache, p.num_blocks, p.num_kv_heads, block_size, head_dim,
+                              DType<TK>::id);
+        if (e != cudaSuccess)
+            return e;
+    }
 #define PA_MMA_CASE(D_, BS_, NH_)                                  \
     if (head_dim == D_ && block_size == BS_ && gc == NH_)          \
-        return MmaVariant<T, D_, BS_, NH_>::launch(p, tk, tv, stream);
+        return MmaVariant<T, TK, D_, BS_, NH_>::launch(p, tk, tv, stream);
     PA_MMA_VARIANTS(PA_MMA_CASE)
 #undef PA_MMA_CASE
     return cudaErrorInvalidValue;
 }
 
 // Resident CTAs per SM of the tensor-core kernel for this shape (0 if unknown).
-template <typename T>
+template <typename T, typename TK = T>
 int occupancy_decode_mma(int head_dim, int block_size, int gc)
 {
 #define PA_MMA_OCC(D_, BS_, NH_)                                   \
     if (head_dim == D_ && block_size == BS_ && gc == NH_) {        \
-        using V = MmaVariant<T, D_, BS_, NH_>;                     \
+        using V = MmaVariant<T, TK, D_, BS_, NH_>;                 \
         return V::configure() == cudaSuccess                       \
                    ? kernel_occupancy(reinterpret_cast<const void*>(V::kernel()), V::Sm::kAlloc) \
                    : 0;                                            \

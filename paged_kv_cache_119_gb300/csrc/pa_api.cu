@@ -25,7 +25,7 @@ int g_sm_count[kMaxDevices] = {};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-size_t elem_size(int dt) { return dt == PA_F32 ? 4 : 2; }
+size_t elem_size(int dt) { return dt == PA_F32 ? 4 : (dt == PA_FP8_E4M3 ? 1 : 2); }
 
 bool valid_dtype(int dt) { return dt == PA_F32 || dt == PA_F16 || dt == PA_BF16; }
 
@@ -231,15 +231,23 @@ size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t 
     return workspace_layout((int64_t)num_seqs * num_q_heads, max_parts, head_dim, nullptr);
 }
 
-int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
-              const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
-              const int32_t* block_tables, int64_t block_table_stride,
-              const int32_t* context_lens, int32_t max_context_len, int32_t num_seqs,
-              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-              float scale, int32_t partition_size, void* workspace, size_t workspace_bytes,
-              void* stream)
+}  // extern "C"
+
+namespace {
+
+// Shared body of pa_decode and pa_decode_fp8.  q_dtype is the type of q (and of a
+// native out); kv_dtype the cache's, PA_FP8_E4M3 with k_scale / v_scale.
+int decode_impl(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
+                const void* k_cache, const void* v_cache, pa_dtype kv_dtype,
+                const float* k_scale, const float* v_scale, int64_t num_blocks,
+                const int32_t* block_tables, int64_t block_table_stride,
+                const int32_t* context_lens, int32_t max_context_len, int32_t num_seqs,
+                int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                float scale, int32_t partition_size, void* workspace, size_t workspace_bytes,
+                void* stream)
 {
-    if (!valid_dtype(kv_dtype) || !(out_dtype == PA_F32 || out_dtype == kv_dtype))
+    const bool fp8 = kv_dtype == PA_FP8_E4M3;
+    if (!valid_dtype(q_dtype) || !(out_dtype == PA_F32 || out_dtype == q_dtype))
         return PA_ERR_INVALID;
     if (num_seqs < 0 || num_seqs > 65535 || num_q_heads <= 0 || num_kv_heads <= 0 ||
         num_q_heads % num_kv_heads != 0)
@@ -256,6 +264,8 @@ int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
         return PA_OK;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
         return PA_ERR_INVALID;
+    if (fp8 && (!k_scale || !v_scale))
+        return PA_ERR_INVALID;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
         return PA_ERR_INVALID;
 
@@ -264,10 +274,10 @@ int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
     const int chunks = group / gc;
     if ((int64_t)num_kv_heads * chunks > 65535)
         return PA_ERR_INVALID;
-    const size_t esz = elem_size(kv_dtype);
-    const size_t q_bytes = (size_t)num_seqs * num_q_heads * head_dim * esz;
+    const size_t q_bytes = (size_t)num_seqs * num_q_heads * head_dim * elem_size(q_dtype);
     const size_t out_bytes = (size_t)num_seqs * num_q_heads * head_dim * elem_size(out_dtype);
-    const size_t pool_bytes = (size_t)num_blocks * num_kv_heads * block_size * head_dim * esz;
+    const size_t pool_bytes =
+        (size_t)num_blocks * num_kv_heads * block_size * head_dim * elem_size(kv_dtype);
     if (overlaps(out, out_bytes, q, q_bytes) || overlaps(out, out_bytes, k_cache, pool_bytes) ||
         overlaps(out, out_bytes, v_cache, pool_bytes))
         return PA_ERR_INVALID;
@@ -279,6 +289,7 @@ int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
         case PA_F32: occ = occupancy_decode_f32(head_dim, block_size, gc); break;
         case PA_F16: occ = occupancy_decode_f16(head_dim, block_size, gc); break;
         case PA_BF16: occ = occupancy_decode_bf16(head_dim, block_size, gc); break;
+        case PA_FP8_E4M3: occ = occupancy_decode_fp8(q_dtype, head_dim, block_size, gc); break;
         }
     }
     const int P = choose_partition(partition_size, max_context_len,
@@ -291,6 +302,8 @@ int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
     p.v_cache = v_cache;
     p.block_tables = block_tables;
     p.context_lens = context_lens;
+    p.k_scale = fp8 ? k_scale : nullptr;
+    p.v_scale = fp8 ? v_scale : nullptr;
     p.num_blocks = num_blocks;
     p.bt_stride = block_table_stride;
     p.num_seqs = num_seqs;
@@ -325,8 +338,87 @@ int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
     case PA_F32: e = launch_decode_f32(p, head_dim, block_size, gc, st); break;
     case PA_F16: e = launch_decode_f16(p, head_dim, block_size, gc, st); break;
     case PA_BF16: e = launch_decode_bf16(p, head_dim, block_size, gc, st); break;
+    case PA_FP8_E4M3: e = launch_decode_fp8(p, q_dtype, head_dim, block_size, gc, st); break;
     }
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
+              const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
+              const int32_t* block_tables, int64_t block_table_stride,
+              const int32_t* context_lens, int32_t max_context_len, int32_t num_seqs,
+              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+              float scale, int32_t partition_size, void* workspace, size_t workspace_bytes,
+              void* stream)
+{
+    if (!valid_dtype(kv_dtype))
+        return PA_ERR_INVALID;
+    return decode_impl(out, out_dtype, q, kv_dtype, k_cache, v_cache, kv_dtype, nullptr, nullptr,
+                       num_blocks, block_tables, block_table_stride, context_lens,
+                       max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                       block_size, scale, partition_size, workspace, workspace_bytes, stream);
+}
+
+int pa_decode_fp8(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
+                  const void* k_cache, const void* v_cache, const float* k_scale,
+                  const float* v_scale, int64_t num_blocks, const int32_t* block_tables,
+                  int64_t block_table_stride, const int32_t* context_lens,
+                  int32_t max_context_len, int32_t num_seqs, int32_t num_q_heads,
+                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size, float scale,
+                  int32_t partition_size, void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (!(q_dtype == PA_F16 || q_dtype == PA_BF16))
+        return PA_ERR_UNSUPPORTED;
+    return decode_impl(out, out_dtype, q, q_dtype, k_cache, v_cache, PA_FP8_E4M3, k_scale,
+                       v_scale, num_blocks, block_tables, block_table_stride, context_lens,
+                       max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                       block_size, scale, partition_size, workspace, workspace_bytes, stream);
+}
+
+int pa_reshape_and_cache_fp8(const void* k, const void* v, pa_dtype src_dtype, void* k_cache,
+                             void* v_cache, const float* k_scale, const float* v_scale,
+                             const int64_t* slot_mapping, int64_t num_tokens,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                             int64_t num_blocks, void* stream)
+{
+    if (!valid_dtype(src_dtype) || num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        block_size <= 0 || num_blocks <= 0)
+        return PA_ERR_INVALID;
+    if (head_dim % 16 != 0)
+        return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0)
+        return PA_OK;
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping || !k_scale || !v_scale)
+        return PA_ERR_INVALID;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID;
+    const size_t pool_bytes = (size_t)num_blocks * num_kv_heads * block_size * head_dim;
+    if (overlaps(k_cache, pool_bytes, v_cache, pool_bytes))
+        return PA_ERR_INVALID;
+    ReshapeFp8Params p{};
+    p.k = k;
+    p.v = v;
+    p.k_cache = static_cast<unsigned char*>(k_cache);
+    p.v_cache = static_cast<unsigned char*>(v_cache);
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.slot_mapping = slot_mapping;
+    p.err = device_error_word();
+    if (!p.err)
+        return PA_ERR_CUDA;
+    p.num_tokens = num_tokens;
+    p.num_blocks = num_blocks;
+    p.num_kv_heads = num_kv_heads;
+    p.head_dim = head_dim;
+    p.block_size = block_size;
+    return launch_reshape_and_cache_fp8(p, src_dtype, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
 }
 
 int pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,

@@ -4,6 +4,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "pa.h"
@@ -133,6 +134,17 @@ template <>
 struct DType<__nv_bfloat16> {
     static constexpr pa_dtype id = PA_BF16;
 };
+template <>
+struct DType<__nv_fp8_e4m3> {
+    static constexpr pa_dtype id = PA_FP8_E4M3;
+};
+
+// Two E4M3 codes (low byte first) as two fp32 values; exact.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes)
+{
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two_codes, __NV_E4M3);
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -192,18 +204,24 @@ struct Load<float, 2> {
     }
 };
 
+template <int N>
+struct Load<__nv_fp8_e4m3, N>;   // defined after Raw below
+
 // N consecutive elements of T held as raw 32-bit words (N * sizeof(T) / 4 of them),
 // loaded with one vector load and converted to fp32 later.
 template <typename T, int N>
 struct Raw {
-    static constexpr int W = N * (int)sizeof(T) / 4;
+    static constexpr int kBytes = N * (int)sizeof(T);
+    static constexpr int W = (kBytes + 3) / 4;
     uint32_t w[W];
 };
 
 template <typename T, int N>
 __device__ __forceinline__ void load_raw(const T* p, Raw<T, N>& r)
 {
-    if constexpr (Raw<T, N>::W == 4) {
+    if constexpr (Raw<T, N>::kBytes == 2) {
+        r.w[0] = *reinterpret_cast<const uint16_t*>(p);
+    } else if constexpr (Raw<T, N>::W == 4) {
         const uint4 v = *reinterpret_cast<const uint4*>(p);
         r.w[0] = v.x; r.w[1] = v.y; r.w[2] = v.z; r.w[3] = v.w;
     } else if constexpr (Raw<T, N>::W == 2) {
@@ -221,6 +239,13 @@ __device__ __forceinline__ void raw_to_float(const Raw<T, N>& r, float (&f)[N])
 #pragma unroll
         for (int i = 0; i < N; ++i)
             f[i] = __uint_as_float(r.w[i]);
+    } else if constexpr (sizeof(T) == 1) {
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            const float2 v = e4m3x2_to_float2(r.w[i / 2] >> (16 * (i % 2)));
+            f[2 * i] = v.x;
+            f[2 * i + 1] = v.y;
+        }
     } else if constexpr (DType<T>::id == PA_BF16) {
 #pragma unroll
         for (int i = 0; i < N / 2; ++i) {
@@ -236,6 +261,16 @@ __device__ __forceinline__ void raw_to_float(const Raw<T, N>& r, float (&f)[N])
         }
     }
 }
+
+template <int N>
+struct Load<__nv_fp8_e4m3, N> {
+    __device__ __forceinline__ static void run(const __nv_fp8_e4m3* p, float (&f)[N])
+    {
+        Raw<__nv_fp8_e4m3, N> r;
+        load_raw<__nv_fp8_e4m3, N>(p, r);
+        raw_to_float<__nv_fp8_e4m3, N>(r, f);
+    }
+};
 
 // Stores one fp32 value as T, rounding to nearest even.
 __device__ __forceinline__ void store_as(float* p, float x) { *p = x; }

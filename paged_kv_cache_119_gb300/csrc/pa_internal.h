@@ -28,6 +28,8 @@ struct DecodeParams {
     const int32_t* context_lens;
     float* part_o;       // [S][Hq][max_parts][D] normalised partial outputs (split only)
     float* part_ml;      // [S][Hq][max_parts][2] (running max in log2 units, sum)
+    const float* k_scale;  // [Hkv] per-head scales of a quantised (E4M3) cache, else null
+    const float* v_scale;
     unsigned* err;       // device error word
     int64_t num_blocks;
     int64_t bt_stride;
@@ -53,6 +55,11 @@ cudaError_t launch_decode_f16(const DecodeParams& p, int head_dim, int block_siz
 cudaError_t launch_decode_bf16(const DecodeParams& p, int head_dim, int block_size, int gc,
                                cudaStream_t stream);
 
+// E4M3 caches (decode_fp8.cu): q_dtype PA_F16 or PA_BF16; p.k_scale / p.v_scale set.
+cudaError_t launch_decode_fp8(const DecodeParams& p, pa_dtype q_dtype, int head_dim,
+                              int block_size, int gc, cudaStream_t stream);
+int occupancy_decode_fp8(pa_dtype q_dtype, int head_dim, int block_size, int gc);
+
 // Resident decode CTAs per SM for this dtype / shape / heads-per-CTA (0 if unknown).
 int occupancy_decode_f32(int head_dim, int block_size, int gc);
 int occupancy_decode_f16(int head_dim, int block_size, int gc);
@@ -72,6 +79,25 @@ struct ReshapeParams {
     int block_size;
 };
 cudaError_t launch_reshape_and_cache(const ReshapeParams& p, cudaStream_t stream);
+
+// Quantising cache write into E4M3 caches: codes e4m3(fp32(x) / scale[h]).
+struct ReshapeFp8Params {
+    const void* k;
+    const void* v;
+    unsigned char* k_cache;
+    unsigned char* v_cache;
+    const float* k_scale;
+    const float* v_scale;
+    const int64_t* slot_mapping;
+    unsigned* err;
+    int64_t num_tokens;
+    int64_t num_blocks;
+    int num_kv_heads;
+    int head_dim;       // a multiple of 16
+    int block_size;
+};
+cudaError_t launch_reshape_and_cache_fp8(const ReshapeFp8Params& p, pa_dtype src_dtype,
+                                         cudaStream_t stream);
 
 // One copy_blocks launch covers up to kCopyMaxLayers layers and kCopyMaxPairs
 // pairs; the parameter block stays under the classic 4 KB kernel-parameter limit.

@@ -60,9 +60,13 @@ class Workload:
     def max_context_len(self) -> int:
         return int(self.meta["max_context_len"])
 
+    @property
+    def fp8(self) -> bool:
+        return self.k_cache.dtype == torch.float8_e4m3fn
+
     def kv_bytes(self) -> int:
         """Bytes of K and V that one decode step must read (every cached token once)."""
-        esz = torch.tensor([], dtype=self.dtype).element_size()
+        esz = self.k_cache.element_size()
         return int(self.meta["total_tokens"]) * self.num_kv_heads * 2 * self.head_dim * esz
 
 
@@ -143,6 +147,34 @@ def _assemble(name, rng, device, *, lens, Hq, Hkv, D, B, dtype, std, pool_slack=
         k_new=k_new, v_new=v_new, slot_mapping=slot_mapping,
         copy_pairs=None if copy_pairs is None else np.asarray(copy_pairs, dtype=np.int64),
         partition_size=partition_size, meta=meta)
+
+
+def to_fp8(w: Workload, headroom: float = 8.0) -> Workload:
+    """The same workload over E4M3 caches.  Each kv head gets its own scale,
+    headroom * std / 448 * (1 + head / Hkv), so values up to `headroom` standard
+    deviations stay in range and heads differ; the cached tokens become
+    e4m3(fp32(x) / scale) by PyTorch's round-to-nearest-even cast (NaN stays NaN).
+    q and the step's new K/V keep the model dtype; the step's cache write
+    quantises them."""
+    std = float(w.meta["std"])
+    heads = torch.arange(w.num_kv_heads, dtype=torch.float32)
+    base = headroom * std / 448.0 * (1.0 + heads / w.num_kv_heads)
+    k_scale = base.to(w.k_cache.device)
+    v_scale = (base * 0.75).to(w.k_cache.device)
+
+    def quant(pool, sc):
+        return (pool.float() / sc[None, :, None, None]).to(torch.float8_e4m3fn)
+
+    meta = dict(w.meta)
+    meta["kv_dtype"] = "fp8_e4m3"
+    return Workload(
+        name=w.name + "_fp8", num_seqs=w.num_seqs, num_q_heads=w.num_q_heads,
+        num_kv_heads=w.num_kv_heads, head_dim=w.head_dim, block_size=w.block_size,
+        dtype=w.dtype, scale=w.scale, num_blocks=w.num_blocks, context_lens=w.context_lens,
+        block_tables=w.block_tables, q=w.q, k_cache=quant(w.k_cache, k_scale),
+        v_cache=quant(w.v_cache, v_scale), k_new=w.k_new, v_new=w.v_new,
+        slot_mapping=w.slot_mapping, copy_pairs=w.copy_pairs,
+        partition_size=w.partition_size, meta=dict(meta, k_scale=k_scale, v_scale=v_scale))
 
 
 def tiny(device="cpu", seed=None, **kw) -> Workload:
