@@ -1,6 +1,6 @@
 // decode_fp8.cu -- paged decode attention over E4M3 (FP8) caches with per-kv-head
 // scales; queries and native outputs are fp16 or bf16.  The tensor-core kernel
-// (decode_mma.cuh) serves at least kMmaMinHeads query heads per CTA, the CUDA-core
+// (decode_mma.cuh) serves at least kMmaMinHeadsFp8 query heads per CTA, the CUDA-core
 // kernel (decode_kernel.cuh) the rest; both read one byte per cached element.
 #include "decode_mma.cuh"
 
@@ -12,7 +12,7 @@ template <typename T>
 cudaError_t launch_fp8(const DecodeParams& p, int head_dim, int block_size, int gc,
                        cudaStream_t stream)
 {
-    if (gc >= kMmaMinHeads)
+    if (gc >= kMmaMinHeadsFp8)
         return launch_decode_mma<T, __nv_fp8_e4m3>(p, head_dim, block_size, gc, stream);
     return launch_decode_typed<T, __nv_fp8_e4m3>(p, head_dim, block_size, gc, stream);
 }
@@ -20,7 +20,7 @@ cudaError_t launch_fp8(const DecodeParams& p, int head_dim, int block_size, int 
 template <typename T>
 int occupancy_fp8(int head_dim, int block_size, int gc)
 {
-    if (gc >= kMmaMinHeads)
+    if (gc >= kMmaMinHeadsFp8)
         return occupancy_decode_mma<T, __nv_fp8_e4m3>(head_dim, block_size, gc);
     return occupancy_decode_typed<T, __nv_fp8_e4m3>(head_dim, block_size, gc);
 }

@@ -28,6 +28,8 @@
 
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "decode_kernel.cuh"
 
 namespace pa {
@@ -61,6 +63,21 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4])
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+// Two E4M3 codes (low 16 bits, low byte first) as an f16x2 operand word; exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
+{
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xffffu),
+                                                     __NV_E4M3);
+    return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
@@ -168,9 +185,13 @@ __device__ __forceinline__ void convert_e4m3_tile(const unsigned char* src, unsi
 template <typename TK, int D, int BS, int NSTAGE>
 struct MmaSmem {
     static constexpr bool kFp8 = sizeof(TK) == 1;
+    // E4M3 with head_dim 128: a tile row is 128 bytes, so the raw tile arrives by
+    // tensor-map TMA with 128-byte swizzle and fragments are read from it directly
+    static constexpr bool kDirect = kFp8 && D == 128;
     static constexpr int kHalfBytes = BS * 128;                // one 64-dim box: B rows x 128 B
     static constexpr int kTileBytes = (D / 64) * kHalfBytes;   // one 16-bit K (or V) tile
-    static constexpr int kScratchBytes = kFp8 ? kDecodeConsumerWarps * 2 * kTileBytes : 0;
+    static constexpr int kScratchBytes =
+        (kFp8 && !kDirect) ? kDecodeConsumerWarps * 2 * kTileBytes : 0;
     static constexpr int kFp8TileBytes = BS * D;               // one E4M3 K (or V) tile
     static constexpr int kStageBytes = kFp8 ? 2 * kFp8TileBytes : 2 * kTileBytes;
     static constexpr int kRingOffset = kScratchBytes;
@@ -184,7 +205,8 @@ struct MmaSmem {
     // is consumed
     static constexpr int kMergeAcc = kDecodeConsumerWarps * 8 * D * 4;
     static constexpr int kMergeBytes = kMergeAcc + kDecodeConsumerWarps * 8 * 2 * 4;
-    static_assert(kMergeBytes <= (kFp8 ? kScratchBytes : kRingBytes), "merge area must fit");
+    static_assert(kMergeBytes <= ((kFp8 && !kDirect) ? kScratchBytes : kRingBytes),
+                  "merge area must fit");
     static_assert(kHalfBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
 };
 
@@ -198,6 +220,10 @@ __global__ void __launch_bounds__(kDecodeThreads)
 {
     using Sm = MmaSmem<TK, D, BS, NSTAGE>;
     constexpr bool kFp8 = Sm::kFp8;
+    // tensor-core operand type: the query type for 16-bit caches; f16 for E4M3 caches
+    // (an E4M3 code converts to f16 exactly in one instruction per pair)
+    using TM = std::conditional_t<kFp8, __half, T>;
+    constexpr bool kDirect = Sm::kDirect;
     constexpr int NCW = kDecodeConsumerWarps;
     constexpr int KS = D / 16;        // k-steps of the score product / m-blocks of P.V
     constexpr int MB = BS / 16;       // 16-token row blocks per tile
@@ -251,7 +277,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
         *poison = 0;
         fence_mbar_init();
     }
-    if (!kFp8 && warp == NCW && lane == 0) {
+    if ((!kFp8 || kDirect) && warp == NCW && lane == 0) {
         prefetch_tensormap(&tk);
         prefetch_tensormap(&tv);
     }
@@ -284,7 +310,12 @@ __global__ void __launch_bounds__(kDecodeThreads)
                         if (valid) {
                             unsigned char* dst = smem + Sm::kRingOffset + stage * Sm::kStageBytes;
                             mbar_arrive_expect_tx(&full[stage], Sm::kStageBytes);
-                            if constexpr (kFp8) {
+                            if constexpr (kDirect) {
+                                const int z = pbn * p.num_kv_heads + kvh;
+                                tma_load_3d(dst, &tk, 0, 0, z, &full[stage], policy);
+                                tma_load_3d(dst + Sm::kFp8TileBytes, &tv, 0, 0, z, &full[stage],
+                                            policy);
+                            } else if constexpr (kFp8) {
                                 const int64_t off =
                                     ((int64_t)pbn * p.num_kv_heads + kvh) * Sm::kFp8TileBytes;
                                 bulk_g2s(dst, reinterpret_cast<const unsigned char*>(p.k_cache) + off,
@@ -322,14 +353,48 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const int c = lane & 3;           // fragment column pair
     // Q^T fragments: b0 = q[head g][16ks + 2c, +1], b1 = q[head g][16ks + 2c + 8, +9]
     uint32_t qb[KS][2];
+    float q_unscale = 1.f;            // for E4M3 caches: q was scaled by 2^-e to fit f16
     {
         const bool live = g < NH;
         const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
             reinterpret_cast<const T*>(p.q) + ((int64_t)seq * p.num_q_heads + h0 + (live ? g : 0)) * D);
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-            qb[ks][0] = live ? __ldg(qrow + (16 * ks + 2 * c) / 2) : 0u;
-            qb[ks][1] = live ? __ldg(qrow + (16 * ks + 2 * c + 8) / 2) : 0u;
+            // k-indices 2c, 2c+1 | 2c+8, 2c+9 of step ks are head dims 16ks + 2c.. | +8..,
+            // or, reading E4M3 bytes directly, 16ks + 4c, +1 | +2, +3 (the same
+            // permutation of the summed dimension is applied to K)
+            const int d0 = kDirect ? 16 * ks + 4 * c : 16 * ks + 2 * c;
+            const int d1 = kDirect ? d0 + 2 : d0 + 8;
+            qb[ks][0] = live ? __ldg(qrow + d0 / 2) : 0u;
+            qb[ks][1] = live ? __ldg(qrow + d1 / 2) : 0u;
+        }
+        if constexpr (kFp8 && !std::is_same_v<T, __half>) {
+            // bf16 queries become f16 operands: scale by a power of two 2^-e so that the
+            // largest |q| of the CTA's heads stays below 2^15 (no overflow; the scaling
+            // is exact), and fold 2^e back into the scores
+            float amax = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float2 f = Mma<T>::unpack(qb[ks][j]);
+                    amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+                }
+#pragma unroll
+            for (int msk = 16; msk >= 1; msk >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, msk));
+            int e = 0;
+            if (amax >= 32768.f)
+                e = ((__float_as_int(amax) >> 23) & 0xff) - 127 - 14;   // 2^-e * amax < 2^15
+            const float down = __int_as_float((127 - e) << 23);
+            q_unscale = __int_as_float((127 + e) << 23);
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float2 f = Mma<T>::unpack(qb[ks][j]);
+                    qb[ks][j] = Mma<__half>::pack(f.x * down, f.y * down);
+                }
         }
     }
     // per-thread statistics for heads 2c and 2c+1 (base-2 units)
@@ -343,7 +408,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
             o[i][j] = 0.f;
     bool poisoned = false;
     // scores carry the softmax scale (base 2) and, for a quantised cache, the K scale
-    const float sl2 = kFp8 ? p.scale_log2 * p.k_scale[kvh] : p.scale_log2;
+    const float sl2 = kFp8 ? p.scale_log2 * p.k_scale[kvh] * q_unscale : p.scale_log2;
 
     for (int it = warp; it < ntiles; it += NCW) {
         const int stage = it % NSTAGE;
@@ -361,14 +426,17 @@ __global__ void __launch_bounds__(kDecodeThreads)
             continue;
         }
         uint32_t kbase, vbase;
-        if constexpr (kFp8) {
+        if constexpr (kDirect) {
+            kbase = smem_addr(smem + Sm::kRingOffset + stage * Sm::kStageBytes);
+            vbase = kbase + Sm::kFp8TileBytes;
+        } else if constexpr (kFp8) {
             // convert the raw tiles into this warp's swizzled 16-bit staging tiles
             // (E4M3 -> T is exact), then hand the stage back to the producer
             unsigned char* stg = smem + warp * 2 * Sm::kTileBytes;
             const unsigned char* raw = smem + Sm::kRingOffset + stage * Sm::kStageBytes;
             __syncwarp();                      // the previous tile's ldmatrix reads are done
-            convert_e4m3_tile<T, D, BS>(raw, stg, lane);
-            convert_e4m3_tile<T, D, BS>(raw + Sm::kFp8TileBytes, stg + Sm::kTileBytes, lane);
+            convert_e4m3_tile<TM, D, BS>(raw, stg, lane);
+            convert_e4m3_tile<TM, D, BS>(raw + Sm::kFp8TileBytes, stg + Sm::kTileBytes, lane);
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&empty[stage]);
@@ -386,7 +454,19 @@ __global__ void __launch_bounds__(kDecodeThreads)
                 break;                         // the rest of the tile lies past the context
             // ---- S^T = K . Q^T for tokens 16mb .. 16mb+15
             float s[4] = {0.f, 0.f, 0.f, 0.f};
-            {
+            if constexpr (kDirect) {
+                // rows 16mb+g and +8; the 4 codes at head dims 16ks + 4c .. +3 of a row
+                // (16-byte chunk ks, swizzled by row) give a0 / a2 (and a1 / a3)
+                const int r0 = 16 * mb + g, r1 = r0 + 8;
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const uint32_t w0 = lds_u32(kbase + r0 * 128 + ((ks ^ (r0 & 7)) << 4) + 4 * c);
+                    const uint32_t w1 = lds_u32(kbase + r1 * 128 + ((ks ^ (r1 & 7)) << 4) + 4 * c);
+                    const uint32_t a[4] = {e4m3x2_to_f16x2(w0), e4m3x2_to_f16x2(w1),
+                                           e4m3x2_to_f16x2(w0 >> 16), e4m3x2_to_f16x2(w1 >> 16)};
+                    Mma<TM>::run(s, a, qb[ks][0], qb[ks][1]);
+                }
+            } else {
                 const int r = 16 * mb + (lane & 7) + 8 * ((lane >> 3) & 1);   // token row
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
@@ -395,7 +475,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
                                           (((chunk & 7) ^ (r & 7)) << 4);
                     uint32_t a[4];
                     ldsm_x4(addr, a);
-                    Mma<T>::run(s, a, qb[ks][0], qb[ks][1]);
+                    Mma<TM>::run(s, a, qb[ks][0], qb[ks][1]);
                 }
             }
             // ---- online softmax: s[0], s[1] = token 16mb+g; s[2], s[3] = token 16mb+g+8
@@ -429,23 +509,60 @@ __global__ void __launch_bounds__(kDecodeThreads)
                 o[i][3] *= alpha[1];
             }
             // ---- P^T (hi + lo) into B fragments: transpose each 8x8 block in registers
-            const uint32_t hi_a = Mma<T>::pack(x[0], x[1]);
-            const uint32_t hi_b = Mma<T>::pack(x[2], x[3]);
-            const float2 fa = Mma<T>::unpack(hi_a), fb = Mma<T>::unpack(hi_b);
-            const uint32_t lo_a = Mma<T>::pack(x[0] - fa.x, x[1] - fa.y);
-            const uint32_t lo_b = Mma<T>::pack(x[2] - fb.x, x[3] - fb.y);
+            const uint32_t hi_a = Mma<TM>::pack(x[0], x[1]);
+            const uint32_t hi_b = Mma<TM>::pack(x[2], x[3]);
+            const float2 fa = Mma<TM>::unpack(hi_a), fb = Mma<TM>::unpack(hi_b);
+            const uint32_t lo_a = Mma<TM>::pack(x[0] - fa.x, x[1] - fa.y);
+            const uint32_t lo_b = Mma<TM>::pack(x[2] - fb.x, x[3] - fb.y);
             const uint32_t bh0 = movmatrix_trans(hi_a), bh1 = movmatrix_trans(hi_b);
             const uint32_t bl0 = movmatrix_trans(lo_a), bl1 = movmatrix_trans(lo_b);
             // ---- O^T += V^T . P^T over tokens 16mb .. 16mb+15
             const int vr = 16 * mb + (lane & 7) + 8 * (lane >> 4);            // token row
             const bool ragged = nvalid < 16 * (mb + 1);
+            uint32_t vpair[8];   // direct E4M3: the two m-blocks 2j, 2j+1 read together
 #pragma unroll
             for (int i = 0; i < KS; ++i) {
-                const int chunk = 2 * i + ((lane >> 3) & 1);
-                const uint32_t addr = vbase + (chunk >> 3) * Sm::kHalfBytes + vr * 128 +
-                                      (((chunk & 7) ^ (vr & 7)) << 4);
                 uint32_t a[4];
-                ldsm_x4_trans(addr, a);
+                if constexpr (kDirect) {
+                    // m-block i = 2j + q holds head dims 32j + 4g + 2q (m = g) and +1
+                    // (m = g + 8): token pairs (2c, 2c+1) and (2c+8, 2c+9) of those dims
+                    // come from 4-byte loads of the four rows, interleaved by byte_perm
+                    if (i % 2 == 0) {
+                        const int j = i / 2;
+                        const int t0 = 16 * mb + 2 * c;
+                        const int chunk = 2 * j + (g >> 2);
+                        const int off = 4 * (g & 3);
+                        const uint32_t w0 = lds_u32(vbase + t0 * 128 + ((chunk ^ (t0 & 7)) << 4) + off);
+                        const uint32_t w1 = lds_u32(vbase + (t0 + 1) * 128 +
+                                                    ((chunk ^ ((t0 + 1) & 7)) << 4) + off);
+                        const uint32_t w8 = lds_u32(vbase + (t0 + 8) * 128 +
+                                                    ((chunk ^ ((t0 + 8) & 7)) << 4) + off);
+                        const uint32_t w9 = lds_u32(vbase + (t0 + 9) * 128 +
+                                                    ((chunk ^ ((t0 + 9) & 7)) << 4) + off);
+                        const uint32_t e01 = __byte_perm(w0, w1, 0x5140);   // dims +0, +1
+                        const uint32_t e23 = __byte_perm(w0, w1, 0x7362);   // dims +2, +3
+                        const uint32_t f01 = __byte_perm(w8, w9, 0x5140);
+                        const uint32_t f23 = __byte_perm(w8, w9, 0x7362);
+                        vpair[0] = e4m3x2_to_f16x2(e01);
+                        vpair[1] = e4m3x2_to_f16x2(e01 >> 16);
+                        vpair[2] = e4m3x2_to_f16x2(f01);
+                        vpair[3] = e4m3x2_to_f16x2(f01 >> 16);
+                        vpair[4] = e4m3x2_to_f16x2(e23);
+                        vpair[5] = e4m3x2_to_f16x2(e23 >> 16);
+                        vpair[6] = e4m3x2_to_f16x2(f23);
+                        vpair[7] = e4m3x2_to_f16x2(f23 >> 16);
+                    }
+                    const int b = 4 * (i % 2);
+                    a[0] = vpair[b];
+                    a[1] = vpair[b + 1];
+                    a[2] = vpair[b + 2];
+                    a[3] = vpair[b + 3];
+                } else {
+                    const int chunk = 2 * i + ((lane >> 3) & 1);
+                    const uint32_t addr = vbase + (chunk >> 3) * Sm::kHalfBytes + vr * 128 +
+                                          (((chunk & 7) ^ (vr & 7)) << 4);
+                    ldsm_x4_trans(addr, a);
+                }
                 if (ragged) {
                     // a0, a1 hold tokens 16mb + 2c, +1; a2, a3 tokens 16mb + 2c + 8, +9
                     const int t = 16 * mb + 2 * c;
@@ -457,11 +574,11 @@ __global__ void __launch_bounds__(kDecodeThreads)
                     a[2] &= m23;
                     a[3] &= m23;
                 }
-                Mma<T>::run(o[i], a, bh0, bh1);
-                Mma<T>::run(o[i], a, bl0, bl1);
+                Mma<TM>::run(o[i], a, bh0, bh1);
+                Mma<TM>::run(o[i], a, bl0, bl1);
             }
         }
-        if constexpr (!kFp8) {
+        if constexpr (!kFp8 || kDirect) {
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&empty[stage]);
@@ -485,11 +602,13 @@ __global__ void __launch_bounds__(kDecodeThreads)
     }
 #pragma unroll
     for (int i = 0; i < KS; ++i) {
-        const int d = 16 * i + g;
+        // head dims of m-block i's rows g and g + 8
+        const int d = kDirect ? 32 * (i / 2) + 4 * g + 2 * (i % 2) : 16 * i + g;
+        const int d8 = kDirect ? d + 1 : d + 8;
         mrg_acc[(warp * 8 + 2 * c) * D + d] = o[i][0];
         mrg_acc[(warp * 8 + 2 * c + 1) * D + d] = o[i][1];
-        mrg_acc[(warp * 8 + 2 * c) * D + d + 8] = o[i][2];
-        mrg_acc[(warp * 8 + 2 * c + 1) * D + d + 8] = o[i][3];
+        mrg_acc[(warp * 8 + 2 * c) * D + d8] = o[i][2];
+        mrg_acc[(warp * 8 + 2 * c + 1) * D + d8] = o[i][3];
     }
     if (poisoned)
         *poison = 1;
@@ -573,13 +692,15 @@ struct MmaVariant {
 #define PA_MMA_VARIANTS(X)                                                                    \
     X(128, 16, 8) X(128, 16, 4) X(128, 32, 8) X(128, 32, 4) X(64, 16, 8) X(64, 16, 4)           \
     X(64, 32, 8) X(64, 32, 4)
+#define PA_MMA_VARIANTS_SMALL(X) \
+    X(128, 16, 2) X(128, 16, 1) X(128, 32, 2) X(128, 32, 1) X(64, 16, 2) X(64, 16, 1) X(64, 32, 2) X(64, 32, 1)
 
 template <typename T, typename TK = T>
 cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, int block_size, int gc,
                               cudaStream_t stream)
 {
     CUtensorMap tk{}, tv{};
-    if constexpr (sizeof(TK) == 2) {
+    if (sizeof(TK) == 2 || head_dim == 128) {      // 16-bit tiles, or direct E4M3 tiles
         cudaError_t e = kv_tensor_map(&tk, p.k_cache, p.num_blocks, p.num_kv_heads, block_size,
                                       head_dim, DType<TK>::id);
         if (e == cudaSuccess)
@@ -592,6 +713,9 @@ cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, int block_siz
     if (head_dim == D_ && block_size == BS_ && gc == NH_)          \
         return MmaVariant<T, TK, D_, BS_, NH_>::launch(p, tk, tv, stream);
     PA_MMA_VARIANTS(PA_MMA_CASE)
+    if constexpr (sizeof(TK) == 1) {
+        PA_MMA_VARIANTS_SMALL(PA_MMA_CASE)
+    }
 #undef PA_MMA_CASE
     return cudaErrorInvalidValue;
 }
@@ -608,6 +732,9 @@ int occupancy_decode_mma(int head_dim, int block_size, int gc)
                    : 0;                                            \
     }
     PA_MMA_VARIANTS(PA_MMA_OCC)
+    if constexpr (sizeof(TK) == 1) {
+        PA_MMA_VARIANTS_SMALL(PA_MMA_OCC)
+    }
 #undef PA_MMA_OCC
     return 0;
 }

@@ -145,19 +145,21 @@ cudaError_t kv_tensor_map(CUtensorMap* map, const void* base, int64_t num_blocks
             return cudaSuccess;
         }
     EncodeTiledFn fn = encode_tiled_fn();
-    if (!fn || elem_size(dtype) != 2)
+    const bool fp8 = dtype == PA_FP8_E4M3;
+    if (!fn || (!fp8 && elem_size(dtype) != 2) || (fp8 && head_dim != 128))
         return cudaErrorNotSupported;
     if (num_blocks * (int64_t)num_kv_heads >= (int64_t(1) << 31))
         return cudaErrorInvalidValue;           // the TMA z coordinate is a signed 32-bit int
-    const cuuint64_t esz = 2;
+    const cuuint64_t esz = fp8 ? 1 : 2;
     const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)block_size,
                                 (cuuint64_t)num_blocks * (cuuint64_t)num_kv_heads};
     const cuuint64_t strides[2] = {head_dim * esz, (cuuint64_t)block_size * head_dim * esz};
-    const cuuint32_t box[3] = {64, (cuuint32_t)block_size, 1};
+    const cuuint32_t box[3] = {fp8 ? 128u : 64u, (cuuint32_t)block_size, 1};   // 128-byte rows
     const cuuint32_t estride[3] = {1, 1, 1};
     CUtensorMap m;
-    const CUresult r = fn(&m, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+    const CUresult r = fn(&m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                  : (dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT16),
                           3, const_cast<void*>(base), dims, strides, box, estride,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

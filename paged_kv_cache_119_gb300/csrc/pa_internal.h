@@ -16,6 +16,9 @@ constexpr int kDecodeThreads = (kDecodeConsumerWarps + 1) * 32;
 // 16-bit caches use the tensor-core decode when a CTA serves at least this many
 // query heads, else the CUDA-core decode.
 constexpr int kMmaMinHeads = 4;
+// E4M3 caches: the same threshold (the tensor-core kernel's exact one-instruction
+// E4M3 -> f16 conversion is measured against the CUDA-core kernel's E4M3 -> f32).
+constexpr int kMmaMinHeadsFp8 = 4;
 // Partition length the automatic split uses (a multiple of every block size).
 constexpr int kAutoPartitionTokens = 512;
 
@@ -113,10 +116,11 @@ struct CopyParams {
 };
 cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);
 
-// Tensor map over a [num_blocks][num_kv_heads][block_size][head_dim] cache of a
-// 16-bit dtype, as 3-D (head_dim, block_size, num_blocks * num_kv_heads) with a
-// box of 64 dims x block_size tokens and 128-byte swizzle.  Encoded maps are
-// cached per (base, shape, dtype).
+// Tensor map over a [num_blocks][num_kv_heads][block_size][head_dim] cache, as
+// 3-D (head_dim, block_size, num_blocks * num_kv_heads) with 128-byte swizzle and
+// a box of 128-byte rows x block_size tokens (64 dims of a 16-bit dtype, or 128
+// E4M3 codes; E4M3 needs head_dim 128).  Encoded maps are cached per (base,
+// shape, dtype).
 cudaError_t kv_tensor_map(CUtensorMap* map, const void* base, int64_t num_blocks, int num_kv_heads,
                           int block_size, int head_dim, pa_dtype dtype);
 
