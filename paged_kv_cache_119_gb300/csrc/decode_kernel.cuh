@@ -311,11 +311,14 @@ __global__ void __launch_bounds__(kDecodeThreads)
                 float part_dot[TC];
 #pragma unroll
                 for (int tt = 0; tt < TC; ++tt) {
-                    float a = qf[g][0] * kf[tt][0];
+                    // pairs of head dims accumulate in packed fp32, then the two halves add
+                    float2 a2 = fmul2(make_float2(qf[g][0], qf[g][1]),
+                                      make_float2(kf[tt][0], kf[tt][1]));
 #pragma unroll
-                    for (int e = 1; e < E; ++e)
-                        a = fmaf(qf[g][e], kf[tt][e], a);
-                    part_dot[tt] = a;
+                    for (int e = 2; e < E; e += 2)
+                        a2 = ffma2(make_float2(qf[g][e], qf[g][e + 1]),
+                                   make_float2(kf[tt][e], kf[tt][e + 1]), a2);
+                    part_dot[tt] = a2.x + a2.y;
                 }
                 s[g][c] = butterfly_sum<TC>(part_dot, lane);
             }
@@ -349,8 +352,12 @@ __global__ void __launch_bounds__(kDecodeThreads)
             }
             lsum[g] = fmaf(lsum[g], alpha, psum);
 #pragma unroll
-            for (int e = 0; e < E; ++e)
-                acc[g][e] *= alpha;
+            for (int e = 0; e < E; e += 2) {
+                const float2 r = fmul2(make_float2(acc[g][e], acc[g][e + 1]),
+                                       make_float2(alpha, alpha));
+                acc[g][e] = r.x;
+                acc[g][e + 1] = r.y;
+            }
             if ((lane & ((1 << TOK_SHIFT) - 1)) == 0) {
 #pragma unroll
                 for (int c = 0; c < NCH; ++c)
@@ -376,8 +383,13 @@ __global__ void __launch_bounds__(kDecodeThreads)
                         for (int g = 0; g < GC; ++g) {
                             const float pt = u == 0 ? pv[g].x : u == 1 ? pv[g].y : u == 2 ? pv[g].z : pv[g].w;
 #pragma unroll
-                            for (int e = 0; e < E; ++e)
-                                acc[g][e] = fmaf(pt, vf[e], acc[g][e]);
+                            for (int e = 0; e < E; e += 2) {
+                                const float2 r = ffma2(make_float2(pt, pt),
+                                                       make_float2(vf[e], vf[e + 1]),
+                                                       make_float2(acc[g][e], acc[g][e + 1]));
+                                acc[g][e] = r.x;
+                                acc[g][e + 1] = r.y;
+                            }
                         }
                     }
                 }
