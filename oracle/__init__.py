@@ -55,6 +55,10 @@ def _declare(lib):
     lib.orc_paged_attention.argtypes = [c_vp, c_vp, c_i32, c_vp, c_vp, c_i32, c_vp, c_vp, c_i64,
                                         c_vp, c_i64, c_vp, c_i32, c_i32, c_i32, c_i32, c_i32,
                                         c_dbl, c_i32]
+    lib.orc_chunk_attention.restype = ctypes.c_int
+    lib.orc_chunk_attention.argtypes = [c_vp, c_vp, c_i32, c_vp, c_vp, c_i32, c_vp, c_vp, c_i64,
+                                        c_vp, c_i64, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32,
+                                        c_i32, c_dbl, c_i32]
     lib.orc_reshape_and_cache_e4m3.restype = ctypes.c_int
     lib.orc_reshape_and_cache_e4m3.argtypes = [c_vp, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
                                                c_i64, c_i32, c_i32, c_i32, c_i64]
@@ -168,6 +172,45 @@ def paged_attention(q, k_cache, v_cache, block_tables, context_lens, scale: floa
                                  int(num_threads))
     if rc != 0:
         raise ValueError(f"oracle paged_attention rejected its inputs (status {rc})")
+    return out
+
+
+def chunk_attention(q, k_cache, v_cache, block_tables, context_lens, query_start,
+                    scale: float, num_kv_heads: int, block_size: int, num_threads: int = 1,
+                    lib=None, k_scale=None, v_scale=None) -> np.ndarray:
+    """Causal attention of each sequence's chunk of new query tokens, fp64.
+
+    q: [R, Hq, D] query rows, sequence s owning rows query_start[s] ..
+    query_start[s+1]-1 (query_start: [S+1] int32, starting at 0); the chunk is the
+    last n_s of the context_lens[s] cached tokens and its token j attends to cached
+    tokens 0 .. L_s - n_s + j.  Returns out[R][Hq][D] as float64.
+    """
+    lib = lib or load_library()
+    ks = vs = None
+    if k_scale is not None:
+        ks = np.ascontiguousarray(_raw(k_scale), dtype=np.float32)
+        vs = np.ascontiguousarray(_raw(v_scale), dtype=np.float32)
+        assert ks.shape == (num_kv_heads,) and vs.shape == (num_kv_heads,)
+    qa, ka, va = _raw(q), _raw(k_cache), _raw(v_cache)
+    bt = np.ascontiguousarray(_raw(block_tables), dtype=np.int32)
+    cl = np.ascontiguousarray(_raw(context_lens), dtype=np.int32)
+    qs = np.ascontiguousarray(_raw(query_start), dtype=np.int32)
+    R, Hq, D = qa.shape
+    S = cl.shape[0]
+    N = ka.shape[0]
+    assert ka.shape == (N, num_kv_heads, block_size, D), ka.shape
+    assert bt.ndim == 2 and bt.shape[0] == S and qs.shape == (S + 1,)
+    assert int(qs[-1]) == R, "query_start[-1] must equal the number of query rows"
+    if _dtype_code(k_cache) == E4M3 and ks is None:
+        raise ValueError("an E4M3 cache needs k_scale and v_scale")
+    out = np.zeros((R, Hq, D), dtype=np.float64)
+    rc = lib.orc_chunk_attention(_ptr(out), _ptr(qa), _dtype_code(q), _ptr(ka), _ptr(va),
+                                 _dtype_code(k_cache), None if ks is None else _ptr(ks),
+                                 None if vs is None else _ptr(vs), N, _ptr(bt), bt.shape[1],
+                                 _ptr(cl), _ptr(qs), S, Hq, num_kv_heads, D, block_size,
+                                 float(scale), int(num_threads))
+    if rc != 0:
+        raise ValueError(f"oracle chunk_attention rejected its inputs (status {rc})")
     return out
 
 

@@ -16,6 +16,9 @@
  *    block, only the last block partially filled) and "原理详解（三）：kernel 实现"
  *    items 1 and 3 (fused reshape + block write; fused block copy).
  *  - same page, "内存共享" Figure 8 (copy-on-write copies one block src -> dst).
+ *  - same page, "局限与未解决的问题" item 6, and "PagedAttention 与 vLLM 推理加速"
+ *    section "一图总结" (chunked prefill and speculative verification: several
+ *    new query tokens of one sequence attend to the paged cache causally).
  *  - iaim.asia/ai-infra/182, section "KV Cache 如何按块分配" (zero-based table:
  *    tokens 0..15 -> block_table[0], 16..31 -> block_table[1], ...; the in-block
  *    layout is the backend's choice and K, V may be two tensors).
@@ -250,6 +253,78 @@ int orc_paged_attention(double* out, const void* q, int q_dtype, const void* k_c
                               block_tables + (int64_t)s * bt_stride, s, h,
                               context_lens[s], num_q_heads, num_kv_heads, head_dim,
                               block_size, scale);
+        if (rc != 0) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+            status = rc;
+        }
+    }
+    (void)num_threads;
+    return status;
+}
+
+/*
+ * Attention of a chunk of consecutive new query tokens per sequence: chunked
+ * prefill and speculative verification, the later uses of the paged cache named
+ * in "PagedAttention 完全拆解", section "局限与未解决的问题" item 6 (Chunked Prefill
+ * on top of the paged KV cache) and in "PagedAttention 与 vLLM 推理加速", section
+ * "一图总结" (a large model verifying a small model's guesses).
+ *
+ * Sequence s owns query rows query_start[s] .. query_start[s+1]-1 of q and out
+ * ([rows][num_q_heads][head_dim]); with n = that count and L = context_lens[s],
+ * the chunk's tokens are the last n of the L cached ones, so chunk token j sits at
+ * position L - n + j and, causally, attends to cached tokens 0 .. L - n + j: the
+ * decode attention of section "背景" over a context of L - n + j + 1 tokens.
+ * Rows of a sequence whose chunk is longer than its context (n > L) are NaN.
+ * Returns 0; -1 for a block id outside the pool; -3 for a context longer than
+ * the table row or negative; -4 for bad sizes or a decreasing query_start.
+ */
+int orc_chunk_attention(double* out, const void* q, int q_dtype, const void* k_cache,
+                        const void* v_cache, int kv_dtype, const float* k_scale,
+                        const float* v_scale, int64_t num_blocks,
+                        const int32_t* block_tables, int64_t bt_stride,
+                        const int32_t* context_lens, const int32_t* query_start, int num_seqs,
+                        int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                        double scale, int num_threads)
+{
+    if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || head_dim <= 0 ||
+        block_size <= 0 || num_q_heads % num_kv_heads != 0 || query_start[0] != 0)
+        return -4;
+    for (int s = 0; s < num_seqs; ++s) {
+        if (query_start[s + 1] < query_start[s])
+            return -4;
+        if (context_lens[s] < 0 || (int64_t)context_lens[s] > bt_stride * block_size)
+            return -3;
+    }
+
+    int status = 0;
+    const int64_t rows = query_start[num_seqs];
+    const int64_t work = rows * num_q_heads;
+#ifdef _OPENMP
+    if (num_threads < 1)
+        num_threads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads)
+#endif
+    for (int64_t i = 0; i < work; ++i) {
+        const int64_t row = i / num_q_heads;            /* query token row of q / out */
+        const int h = (int)(i % num_q_heads);
+        int s = 0;                                      /* the sequence owning the row */
+        while (query_start[s + 1] <= row)
+            ++s;
+        const int n = query_start[s + 1] - query_start[s];
+        const int L = context_lens[s];
+        double* o = out + i * head_dim;
+        if (n > L) {
+            for (int d = 0; d < head_dim; ++d)
+                o[d] = NAN;
+            continue;
+        }
+        const int j = (int)(row - query_start[s]);      /* index within the chunk */
+        const int visible = L - n + j + 1;              /* tokens 0 .. L - n + j */
+        int rc = orc_one_head(o, q, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale,
+                              num_blocks, block_tables + (int64_t)s * bt_stride, (int)row, h,
+                              visible, num_q_heads, num_kv_heads, head_dim, block_size, scale);
         if (rc != 0) {
 #ifdef _OPENMP
 #pragma omp critical

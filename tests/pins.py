@@ -499,4 +499,129 @@ def pin_e4m3_cache_write(lib):
         assert torch.equal(kc, want_k) and torch.equal(vc, want_v)
 
 
+# ----------------------------------------------------------------------------- chunks
+
+def chunk_case(rng, S, Hq, Hkv, D, B, dtype, max_len, full_prefill=False):
+    """A paged case plus a chunk of n_s <= L_s query rows per sequence."""
+    c = random_case(rng, S, Hq, Hkv, D, B, dtype, max_len)
+    ns = [L if full_prefill else int(rng.integers(1, L + 1)) for L in c["lens"]]
+    qs = np.concatenate([[0], np.cumsum(ns)]).astype(np.int32)
+    g = torch.Generator().manual_seed(int(rng.integers(0, 2**31)))
+    c["ns"] = ns
+    c["query_start"] = torch.from_numpy(qs)
+    c["qc"] = torch.randn(int(qs[-1]), Hq, D, generator=g).to(dtype)
+    return c
+
+
+def run_chunk(lib, c, scale, Hkv, B, query_start=None, lens=None, q=None):
+    lens = c["lens"] if lens is None else lens
+    return oracle.chunk_attention(c["qc"] if q is None else q, c["kc"], c["vc"],
+                                  table_tensor(c["tables"]), torch.tensor(lens, dtype=torch.int32),
+                                  c["query_start"] if query_start is None else query_start,
+                                  scale, Hkv, B, lib=lib)
+
+
+def pin_chunk_hand_case(lib):
+    """Two sequences with chunks of 2 and 1 tokens, evaluated by hand
+    (tests/golden/chunk_causal_hand.json)."""
+    g = golden("chunk_causal_hand.json")
+    B, D, N = g["block_size"], g["head_dim"], g["num_blocks"]
+    kc = torch.full((N, 1, B, D), float("nan"))
+    vc = kc.clone()
+    q, tables, lens = [], [], []
+    for sq in g["sequences"]:
+        for t, (k, v) in enumerate(zip(sq["k"], sq["v"])):
+            kc[sq["block_table"][t // B], 0, t % B] = torch.tensor(k)
+            vc[sq["block_table"][t // B], 0, t % B] = torch.tensor(v)
+        q += sq["q"]
+        tables.append(sq["block_table"])
+        lens.append(sq["context_len"])
+    out = oracle.chunk_attention(torch.tensor(q)[:, None, :], kc, vc, table_tensor(tables),
+                                 torch.tensor(lens, dtype=torch.int32),
+                                 torch.tensor(g["query_start"], dtype=torch.int32), g["scale"],
+                                 1, B, lib=lib)
+    np.testing.assert_allclose(out[:, 0], g["expected"], rtol=1e-14, atol=0)
+
+
+def pin_chunk_full_prefill_is_causal_sdpa(lib):
+    """A chunk that is the whole context (n = L) is ordinary causal self-attention:
+    PyTorch's float64 SDPA with is_causal=True on the unpaged arrays, MHA and GQA."""
+    rng = np.random.default_rng(21)
+    for S, Hq, Hkv, D, B, dtype, max_len in [(3, 4, 4, 16, 4, torch.float32, 23),
+                                             (2, 8, 2, 32, 16, torch.bfloat16, 40),
+                                             (2, 6, 3, 64, 8, torch.float16, 19)]:
+        c = chunk_case(rng, S, Hq, Hkv, D, B, dtype, max_len, full_prefill=True)
+        scale = 1.0 / math.sqrt(D)
+        out = run_chunk(lib, c, scale, Hkv, B)
+        qs = c["query_start"].tolist()
+        for s in range(S):
+            q64 = c["qc"][qs[s]:qs[s + 1]].double().permute(1, 0, 2)[None]
+            k64 = c["K"][s].double().permute(1, 0, 2)[None]
+            v64 = c["V"][s].double().permute(1, 0, 2)[None]
+            ref = F.scaled_dot_product_attention(q64, k64, v64, scale=scale, is_causal=True,
+                                                 enable_gqa=Hq != Hkv)[0].permute(1, 0, 2)
+            np.testing.assert_allclose(out[qs[s]:qs[s + 1]], ref.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def pin_chunk_rows_see_their_prefix(lib):
+    """Chunk row j of a sequence (n < L) equals unmasked SDPA over the first
+    L - n + j + 1 cached tokens; the last row sees the whole context."""
+    rng = np.random.default_rng(22)
+    c = chunk_case(rng, 4, 4, 2, 32, 8, torch.bfloat16, 45)
+    scale = 1.0 / math.sqrt(32)
+    out = run_chunk(lib, c, scale, 2, 8)
+    qs = c["query_start"].tolist()
+    for s, (L, n) in enumerate(zip(c["lens"], c["ns"])):
+        for j in range(n):
+            vis = L - n + j + 1
+            ref = dense_reference(c["qc"][qs[s] + j], c["K"][s][:vis], c["V"][s][:vis], scale)
+            np.testing.assert_allclose(out[qs[s] + j], ref, rtol=1e-12, atol=1e-13)
+
+
+def pin_chunking_invariance(lib):
+    """Chunked prefill: attending a chunk at once equals attending it as two
+    consecutive chunks, the first over the shorter context it had then."""
+    rng = np.random.default_rng(23)
+    c = chunk_case(rng, 3, 4, 4, 16, 4, torch.float32, 40, full_prefill=True)
+    whole = run_chunk(lib, c, 0.25, 4, 4)
+    qs = c["query_start"].tolist()
+    for s, L in enumerate(c["lens"]):
+        n1 = L // 2
+        rows = c["qc"][qs[s]:qs[s + 1]]
+        one = dict(c, tables=[c["tables"][s]])
+        first = run_chunk(lib, one, 0.25, 4, 4, torch.tensor([0, n1], dtype=torch.int32),
+                          [n1], rows[:n1]) if n1 > 0 else np.zeros((0,) + whole.shape[1:])
+        second = run_chunk(lib, one, 0.25, 4, 4, torch.tensor([0, L - n1], dtype=torch.int32),
+                           [L], rows[n1:])
+        assert np.array_equal(np.concatenate([first, second]), whole[qs[s]:qs[s + 1]])
+
+
+def pin_chunk_of_one_is_decode_sdpa(lib):
+    """One new token per sequence (n = 1) is plain decode attention over the whole
+    context (SDPA on the unpaged arrays), as in the single-query kernel."""
+    rng = np.random.default_rng(24)
+    c = random_case(rng, 5, 8, 2, 64, 16, torch.bfloat16, 70)
+    c["query_start"] = torch.arange(6, dtype=torch.int32)
+    c["qc"] = c["q"]
+    out = run_chunk(lib, c, 0.125, 2, 16)
+    for s in range(5):
+        np.testing.assert_allclose(out[s], dense_reference(c["q"][s], c["K"][s], c["V"][s], 0.125),
+                                   rtol=1e-12, atol=1e-13)
+
+
+def pin_chunk_longer_than_context_is_nan(lib):
+    """A chunk longer than its context is malformed: its rows come back NaN and the
+    other sequences are unaffected."""
+    rng = np.random.default_rng(25)
+    c = random_case(rng, 2, 2, 2, 8, 4, torch.float32, 9)
+    lens = [c["lens"][0], c["lens"][1]]
+    n0 = lens[0] + 1
+    c["query_start"] = torch.tensor([0, n0, n0 + 1], dtype=torch.int32)
+    c["qc"] = torch.randn(n0 + 1, 2, 8)
+    out = run_chunk(lib, c, 0.5, 2, 4)
+    assert np.isnan(out[:n0]).all()
+    ref = dense_reference(c["qc"][n0], c["K"][1], c["V"][1], 0.5)
+    np.testing.assert_allclose(out[n0], ref, rtol=1e-12, atol=1e-13)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

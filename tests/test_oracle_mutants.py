@@ -53,6 +53,14 @@ MUTANTS = {
                               "const double ks = 1.0;"),
     "dequant_wrong_head_scale": ("const double vs = v_scale ? (double)v_scale[hk] : 1.0;",
                                  "const double vs = v_scale ? (double)v_scale[0] : 1.0;"),
+    "chunk_top_left_causal": ("const int visible = L - n + j + 1;", "const int visible = j + 1;"),
+    "chunk_excludes_own_token": ("const int visible = L - n + j + 1;",
+                                 "const int visible = L - n + j;"),
+    "chunk_unmasked": ("const int visible = L - n + j + 1;", "const int visible = L;"),
+    "chunk_query_row_is_sequence": ("block_tables + (int64_t)s * bt_stride, (int)row, h,",
+                                    "block_tables + (int64_t)s * bt_stride, s, h,"),
+    "chunk_row_owner_off_by_one": ("while (query_start[s + 1] <= row)",
+                                   "while (query_start[s + 1] < row)"),
 }
 
 
