@@ -220,6 +220,51 @@ int pa_decode_fp8(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype
                   int32_t partition_size, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Chunk attention: causal attention of several new query tokens per sequence over
+ * the paged cache -- chunked prefill and speculative verification, the later uses
+ * of the paged KV cache named in "PagedAttention 完全拆解", section 局限与未解决的问题
+ * item 6, and in "PagedAttention 与 vLLM 推理加速", section 一图总结.
+ *
+ * Sequence s owns query rows query_start[s] .. query_start[s+1]-1 of q and out
+ * (n_s rows; query_start[0] = 0, query_start[num_seqs] = num_query_tokens).  Its
+ * chunk is the last n_s of its context_lens[s] = L_s cached tokens (write them with
+ * pa_reshape_and_cache first), so chunk token j sits at position L_s - n_s + j and
+ * attends to cached tokens 0 .. L_s - n_s + j:
+ *   out[row][h] = sum_{t <= L_s - n_s + j} a_t v_t,
+ *   a_t = exp(scale q[row][h] . k_t) / sum_{u <= L_s - n_s + j} exp(scale q[row][h] . k_u),
+ * with k_t, v_t read through block_tables[s] as in pa_decode and query head h
+ * reading kv head h / (num_q_heads / num_kv_heads).  n_s = 1 is pa_decode.
+ *
+ *   out        [num_query_tokens][num_q_heads][head_dim], out_dtype PA_F32 or kv_dtype
+ *   q          [num_query_tokens][num_q_heads][head_dim], kv_dtype
+ *   k_cache, v_cache, num_blocks, block_tables, block_table_stride, context_lens: as in
+ *              pa_decode; kv_dtype PA_F16 or PA_BF16
+ *   query_start  DEVICE int32 [num_seqs + 1], non-decreasing
+ *   max_query_len    >= every n_s (sizes the grid); max_context_len >= every L_s
+ *   partition_size   0 = automatic split of long contexts, < 0 never split, > 0 that
+ *                    many tokens per partition (a multiple of 64)
+ *   workspace        DEVICE scratch of pa_chunk_workspace_bytes(...) when a split
+ *                    happens (16-byte aligned, caller-owned), else may be NULL
+ * Supported: head_dim 64 / 128, block_size 16 / 32, num_q_heads / num_kv_heads <= 128.
+ * Accumulation is fp32 on the tensor cores; probabilities enter the P.V product as
+ * hi + lo halves of the 16-bit type, so they keep fp32-level accuracy.
+ * Errors: invalid arguments return a negative pa_status with nothing launched.  On
+ * the device, n_s > L_s, L_s > max_context_len, n_s > max_query_len or rows beyond
+ * query_start[num_seqs] set PA_DEVERR_CONTEXT_LEN (that sequence's rows become NaN);
+ * a block id outside the pool sets PA_DEVERR_BLOCK_ID.
+ */
+size_t pa_chunk_workspace_bytes(int64_t num_query_tokens, int32_t num_q_heads, int32_t head_dim,
+                                int32_t max_context_len, int32_t partition_size);
+int pa_chunk_attention(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
+                       const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
+                       const int32_t* block_tables, int64_t block_table_stride,
+                       const int32_t* context_lens, const int32_t* query_start,
+                       int64_t num_query_tokens, int32_t max_query_len, int32_t max_context_len,
+                       int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, float scale, int32_t partition_size,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Reads and clears the calling device's error word (PA_DEVERR_* bits).
  * Synchronises with `stream` to do so.  flags: host pointer.
  */

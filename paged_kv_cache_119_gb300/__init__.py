@@ -8,6 +8,8 @@ contexts), and this thin binding that passes PyTorch tensors to it:
     pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
               num_kv_heads, block_size)
     pa_copy_blocks(k_caches, v_caches, src_dst_pairs)
+    pa_chunk_attention(out, q, k_cache, v_cache, block_tables, context_lens,
+                       query_start, scale, num_kv_heads, block_size, max_query_len)
 
 ``workloads`` builds seeded synthetic inputs.  The binding is imported lazily
 so the input generator works on machines without the built library; any call
@@ -17,6 +19,7 @@ __version__ = "0.1.0"
 
 _API = ("pa_decode", "pa_decode_noalloc", "pa_decode_fp8", "pa_reshape_and_cache",
         "pa_reshape_and_cache_fp8", "pa_copy_blocks", "pa_decode_workspace_bytes",
+        "pa_chunk_attention", "pa_chunk_workspace_bytes",
         "pa_get_device_error", "pa_version")
 
 __all__ = list(_API) + ["workloads", "build"]

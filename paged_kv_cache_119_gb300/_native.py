@@ -30,6 +30,10 @@ SIGNATURES = {
     "pa_decode_fp8": (ctypes.c_int, [_vp, ctypes.c_int, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _i64,
                                      _vp, _i64, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32,
                                      _vp, _sz, _vp]),
+    "pa_chunk_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32, _i32]),
+    "pa_chunk_attention": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp, _vp, ctypes.c_int, _i64, _vp,
+                                          _i64, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _i32, _i32,
+                                          _i32, _f32, _i32, _vp, _sz, _vp]),
     "pa_reshape_and_cache_fp8": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _vp, _vp, _vp, _vp, _vp,
                                                 _i64, _i32, _i32, _i32, _i64, _vp]),
     "pa_reshape_and_cache": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i64,

@@ -256,6 +256,68 @@ def pa_decode_fp8(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
     return out
 
 
+def pa_chunk_workspace_bytes(num_query_tokens: int, num_q_heads: int, head_dim: int,
+                             max_context_len: int, partition_size: int = 0) -> int:
+    """Workspace bytes pa_chunk_attention needs for a split call (0 when it never splits)."""
+    return int(N.load().pa_chunk_workspace_bytes(num_query_tokens, num_q_heads, head_dim,
+                                                 max_context_len, partition_size))
+
+
+def pa_chunk_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                       v_cache: torch.Tensor, block_tables: torch.Tensor,
+                       context_lens: torch.Tensor, query_start: torch.Tensor, scale: float,
+                       num_kv_heads: int, block_size: int, max_query_len: int,
+                       max_context_len: int | None = None, partition_size: int = 0,
+                       workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Causal attention of each sequence's chunk of new query tokens (chunked prefill,
+    speculative verification) over the paged cache.
+
+    q, out [R, Hq, D] (out float32 or q's dtype; q float16 or bfloat16, the caches'
+    dtype); sequence s owns rows query_start[s] .. query_start[s+1]-1 (query_start
+    [S+1] int32), the last n_s of its context_lens[s] cached tokens, and chunk token j
+    attends to cached tokens 0 .. L_s - n_s + j.  max_query_len bounds every n_s;
+    max_context_len defaults to W * block_size.  A workspace is allocated with torch
+    if the call splits and none is given.
+    """
+    for name, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                    ("block_tables", block_tables), ("context_lens", context_lens),
+                    ("query_start", query_start)):
+        _cuda(name, t)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 or \
+            query_start.dtype != torch.int32:
+        raise TypeError("block_tables, context_lens and query_start must be int32")
+    if q.dim() != 3 or out.shape != q.shape:
+        raise ValueError(f"q and out must be [R, Hq, D] of one shape, got {tuple(q.shape)}, "
+                         f"{tuple(out.shape)}")
+    R, Hq, D = q.shape
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape or \
+            tuple(k_cache.shape[1:]) != (num_kv_heads, block_size, D):
+        raise ValueError(f"k_cache/v_cache must be [N, {num_kv_heads}, {block_size}, {D}], "
+                         f"got {tuple(k_cache.shape)}, {tuple(v_cache.shape)}")
+    if k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise TypeError("q, k_cache and v_cache must share a dtype")
+    S = context_lens.shape[0]
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or query_start.shape != (S + 1,):
+        raise ValueError("block_tables must be [S, W], context_lens [S], query_start [S + 1]")
+    if max_context_len is None:
+        max_context_len = block_tables.shape[1] * block_size
+    ws_need = pa_chunk_workspace_bytes(R, Hq, D, max_context_len, max(partition_size, 0)) \
+        if partition_size >= 0 else 0
+    if ws_need and workspace is None:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
+    ws_ptr, ws_bytes = (0, 0) if workspace is None else (workspace.data_ptr(),
+                                                         workspace.numel() *
+                                                         workspace.element_size())
+    status = N.load().pa_chunk_attention(
+        out.data_ptr(), _dtype(out), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        _dtype(q), k_cache.shape[0], block_tables.data_ptr(), block_tables.stride(0),
+        context_lens.data_ptr(), query_start.data_ptr(), R, int(max_query_len),
+        int(max_context_len), S, Hq, num_kv_heads, D, block_size, float(scale),
+        int(partition_size), ws_ptr, ws_bytes, _stream(stream))
+    N.check("pa_chunk_attention", status)
+    return out
+
+
 def pa_get_device_error(stream=None) -> int:
     """Read and clear the device error word (PA_DEVERR_* bits).  Synchronises."""
     flags = ctypes.c_uint32(0)

@@ -1,0 +1,576 @@
+// chunk_attn.cuh -- causal attention of a chunk of new query tokens per sequence
+// over the paged KV cache, on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// What it computes (the chunked-prefill / speculative-verification use of the
+// paged cache: "PagedAttention 完全拆解", section "局限与未解决的问题" item 6;
+// "PagedAttention 与 vLLM 推理加速", section "一图总结"): sequence s owns query rows
+// query_start[s] .. query_start[s+1]-1; with n of them and context L, chunk token
+// j sits at position L - n + j and attends to cached tokens 0 .. L - n + j, i.e.
+// the softmax attention of section "背景" over that prefix, read through the
+// block table.
+//
+// Organisation.  A CTA owns up to 128 (query token, query head) rows that share a
+// kv head: TT = 128 / G consecutive chunk tokens x the G heads of the group, row
+// r = token * G + head.  K and V are streamed through the block table in tiles of
+// 64 tokens; both products are dense 128-row contractions:
+//   S[128 x 64]  = Q[128 x D] . K_tile^T      (tcgen05.mma kind::f16, fp32 in TMEM)
+//   O[128 x D]  += P[128 x 64] . V_tile        (P = hi + lo halves of the 16-bit type)
+//   * warp 0 (producer): block-table entries and tensor-map TMA of the tile's K
+//     and V boxes (64 dims x B tokens, 128-byte swizzle) into an mbarrier ring;
+//   * warp 1: allocates tensor memory and (one thread) issues the MMAs: S of the
+//     next tile is issued before P.V of the current one, into a second S buffer,
+//     so the tensor core works while the softmax warps read scores;
+//   * warps 2-5 (one thread per row = TMEM lane): read S, mask (causal within the
+//     chunk, end of context), online softmax in base 2, write P to shared memory
+//     in the operand layout, and keep O in tensor memory up to date.
+// Rescaling O is lazy: a row's reference maximum moves only when a tile's maximum
+// exceeds it by more than 2^8 in probability, so p = 2^(x - m_ref) <= 256 and
+// most tiles need no tensor-memory round trip.  The result O / l is exact for any
+// reference, as O and l share it.
+// P is split into hi = rn(p) and lo = rn(p - hi) of the 16-bit operand type
+// (p = hi + lo to ~2^-17 relative) and both halves are multiplied with V, so the
+// probabilities keep fp32-level accuracy (one 8-bit-mantissa rounding of p would
+// cost up to 2^-9 relative per weight).
+// Long contexts with few CTAs are split into partitions merged by
+// chunk_reduce_kernel, as in the decode path.
+#pragma once
+
+#include <cuda.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+#include "tc_device.cuh"
+
+namespace pa {
+
+constexpr int kChunkRows = 128;      // M of the tensor-core tile
+constexpr int kChunkTileTok = 64;    // tokens per K/V tile (N of the score product)
+constexpr int kChunkThreads = 192;   // producer, MMA, four softmax warps
+
+template <int D, int NST>
+struct ChunkSmem {
+    static constexpr int kHalves = D / 64;                       // 128-byte column groups
+    static constexpr int kQHalf = kChunkRows * 128;              // 16 KB
+    static constexpr int kQBytes = kHalves * kQHalf;
+    static constexpr int kPBytes = kChunkRows * 128;             // 128 rows x 64 tokens x 2 B
+    static constexpr int kKVHalf = kChunkTileTok * 128;          // 8 KB
+    static constexpr int kKBytes = kHalves * kKVHalf;
+    static constexpr int kStageBytes = 2 * kKBytes;              // K then V
+    static constexpr int kQOff = 0;
+    static constexpr int kPOff = kQOff + kQBytes;                // [buffer 2][hi, lo][kPBytes]
+    static constexpr int kStageOff = kPOff + 4 * kPBytes;
+    static constexpr int kBarOff = kStageOff + NST * kStageBytes;
+    // full[NST], empty[NST], s_full[2], s_free[2], p_full[2], pv_done[2], q_full, mma_done
+    static constexpr int kNumBars = 2 * NST + 10;
+    static constexpr int kOkOff = kBarOff + 8 * kNumBars;        // stage_ok[NST]
+    static constexpr int kSlotOff = kOkOff + 4 * NST;            // TMEM address
+    static constexpr int kBytes = kSlotOff + 16;
+    static constexpr int kAlloc = kBytes + 1024;                 // 1 KB alignment slack
+    static constexpr int kTmemCols = 256;                        // O at 0, S buffers at 128, 192
+    static constexpr int kSCol = 128;
+    static_assert(D <= 128, "O must fit below the S buffers");
+    static_assert(kAlloc <= 227 * 1024, "shared memory");
+};
+
+// Stores 32 consecutive outputs v[i] * mul (NaN when nan_out) at base + idx as
+// fp32 (which = 0), f16 (1) or bf16 (2); idx is a multiple of 32.
+__device__ __forceinline__ void store_row32(void* base, int64_t idx, const float (&v)[32], float mul,
+                                            bool nan_out, int which)
+{
+    const float qnan = __int_as_float(0x7fc00000);
+    if (which == 0) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(base) + idx);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            dst[i] = nan_out ? make_float4(qnan, qnan, qnan, qnan)
+                             : make_float4(v[4 * i] * mul, v[4 * i + 1] * mul, v[4 * i + 2] * mul,
+                                           v[4 * i + 3] * mul);
+        return;
+    }
+    uint32_t packed[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float a = nan_out ? qnan : v[2 * i] * mul;
+        const float b = nan_out ? qnan : v[2 * i + 1] * mul;
+        if (which == 1) {
+            __half2 h = __floats2half2_rn(a, b);
+            packed[i] = *reinterpret_cast<uint32_t*>(&h);
+        } else {
+            __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+            packed[i] = *reinterpret_cast<uint32_t*>(&h);
+        }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + idx);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float a, float b)
+{
+    if constexpr (DType<T>::id == PA_F16) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ float2 unpack2(uint32_t w)
+{
+    if constexpr (DType<T>::id == PA_F16)
+        return __half22float2(*reinterpret_cast<__half2*>(&w));
+    else
+        return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w));
+}
+
+// grid = (partitions, num_kv_heads * m_tiles, num_seqs); 192 threads.
+template <typename T, int D, int BS, int NST>
+__global__ void __launch_bounds__(kChunkThreads, 1)
+    chunk_attn_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ CUtensorMap tk,
+                      const __grid_constant__ CUtensorMap tv)
+{
+    using Sm = ChunkSmem<D, NST>;
+    constexpr int NT = kChunkTileTok;
+    constexpr int BPT = NT / BS;                 // cache blocks per K/V tile
+    constexpr int KS = D / 16;                   // k-steps of the score product
+    constexpr bool kBf16 = DType<T>::id == PA_BF16;
+    static_assert(NT % BS == 0 && D % 64 == 0, "block_size 16/32, head_dim 64/128");
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sm::kBarOff);
+    uint64_t* empty = full + NST;
+    uint64_t* s_full = empty + NST;
+    uint64_t* s_free = s_full + 2;
+    uint64_t* p_full = s_free + 2;
+    uint64_t* pv_done = p_full + 2;
+    uint64_t* q_full = pv_done + 2;
+    uint64_t* mma_done = q_full + 1;
+    int* stage_ok = reinterpret_cast<int*>(smem + Sm::kOkOff);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Sm::kSlotOff);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int seq = blockIdx.z;
+    const int kvh = blockIdx.y / p.m_tiles;
+    const int mt = blockIdx.y - kvh * p.m_tiles;
+    const int part = blockIdx.x;
+    const bool split = p.partition_tokens > 0;
+    const int G = p.group;
+    const int TT = p.rows_tokens;
+
+    const int qs0 = p.query_start[seq];
+    const int qs1 = p.query_start[seq + 1];
+    const int n = qs1 - qs0;
+    const int L = p.context_lens[seq];
+    const bool rows_sane = qs0 >= 0 && n >= 0 && (int64_t)qs1 <= p.num_rows;
+    if (!rows_sane || L < 0 || L > p.max_context_len || n > L || n > p.max_query_len) {
+        if (part == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+            atomicOr(p.err, PA_DEVERR_CONTEXT_LEN);
+        if (!split && rows_sane && part == 0 && mt == 0) {
+            // the sequence's rows of this kv head's query heads become NaN
+            const int64_t cnt = (int64_t)n * G * D;
+            for (int64_t i = threadIdx.x; i < cnt; i += blockDim.x) {
+                const int64_t tok = i / ((int64_t)G * D);
+                const int rem = (int)(i - tok * G * D);
+                const int64_t idx = ((qs0 + tok) * p.num_q_heads + kvh * G) * D + rem;
+                if (p.out_f32)
+                    store_as(static_cast<float*>(p.out) + idx, __int_as_float(0x7fc00000));
+                else
+                    store_as(static_cast<T*>(p.out) + idx, __int_as_float(0x7fc00000));
+            }
+        }
+        return;
+    }
+    if (seq == p.num_seqs - 1 && part == 0 && blockIdx.y == 0 && (int64_t)qs1 != p.num_rows) {
+        // rows after the last sequence's chunk are owned by nobody
+        if (threadIdx.x == 0)
+            atomicOr(p.err, PA_DEVERR_CONTEXT_LEN);
+    }
+    const int j0 = mt * TT;
+    if (j0 >= n)
+        return;                                  // no chunk token in this row tile
+    const int ntok = min(TT, n - j0);
+    const int pos_first = L - n + j0;            // position of the tile's first token
+    const int t_end = pos_first + ntok;          // tokens [0, t_end) are seen by some row
+    int t0 = 0, t1 = t_end;
+    if (split) {
+        t0 = part * p.partition_tokens;
+        if (t0 >= t_end)
+            return;
+        t1 = min(t_end, t0 + p.partition_tokens);
+    }
+    const int ntiles = (t1 - t0 + NT - 1) / NT;  // >= 1
+
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&s_free[b], 4);
+            mbar_init(&p_full[b], 4);
+            mbar_init(&pv_done[b], 1);
+        }
+        mbar_init(q_full, 4);
+        mbar_init(mma_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, Sm::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tk);
+        prefetch_tensormap(&tv);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ producer
+        const int32_t* bt_row = p.block_tables + (int64_t)seq * p.bt_stride;
+        const uint64_t policy = l2_evict_first_policy();
+        const int blk_end = (t1 + BS - 1) / BS;
+        int issued = 0;
+        for (int it = 0; it < ntiles; ++it) {
+            const int st = it % NST;
+            const int b0 = (t0 + it * NT) / BS;
+            const int nb = min(BPT, blk_end - b0);
+            int pbn = -1;
+            bool valid = false;
+            if (lane < nb) {
+                pbn = __ldg(bt_row + b0 + lane);
+                valid = pbn >= 0 && (int64_t)pbn < p.num_blocks;
+            }
+            const unsigned vmask = __ballot_sync(kFullMask, valid);
+            int ok = 1;
+            if (lane == 0) {
+                if (it >= NST && !mbar_wait(&empty[st], ((it / NST) - 1) & 1)) {
+                    atomicOr(p.err, PA_DEVERR_TIMEOUT);
+                    ok = 0;
+                } else {
+                    const int nvalid = __popc(vmask);
+                    stage_ok[st] = nvalid == nb ? 1 : 0;
+                    if (nvalid != nb)
+                        atomicOr(p.err, PA_DEVERR_BLOCK_ID);
+                    mbar_arrive_expect_tx(&full[st], (uint32_t)nvalid * 2u * Sm::kHalves * BS * 128u);
+                }
+            }
+            if (!__shfl_sync(kFullMask, ok, 0))
+                break;
+            if (valid) {
+                unsigned char* kdst = smem + Sm::kStageOff + st * Sm::kStageBytes + lane * (BS * 128);
+                const int z = pbn * p.num_kv_heads + kvh;     // < 2^31 (checked on the host)
+#pragma unroll
+                for (int h = 0; h < Sm::kHalves; ++h) {
+                    tma_load_3d(kdst + h * Sm::kKVHalf, &tk, 64 * h, 0, z, &full[st], policy);
+                    tma_load_3d(kdst + Sm::kKBytes + h * Sm::kKVHalf, &tv, 64 * h, 0, z, &full[st],
+                                policy);
+                }
+            }
+            issued = it + 1;
+        }
+        // no copy may still be in flight into this CTA's shared memory at exit
+        if (lane == 0)
+            for (int it = max(0, issued - NST); it < issued; ++it)
+                mbar_wait(&full[it % NST], (it / NST) & 1);
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            const uint32_t sq = smem_addr(smem + Sm::kQOff);
+            const uint32_t idesc_s = mma_idesc_f16(kBf16, kChunkRows, NT, false);
+            const uint32_t idesc_o = mma_idesc_f16(kBf16, kChunkRows, D, true);
+            bool ok = mbar_wait(q_full, 0);
+            auto issue_scores = [&](int it) {
+                const uint32_t kb = smem_addr(smem + Sm::kStageOff + (it % NST) * Sm::kStageBytes);
+                const uint32_t dcol = tbase + Sm::kSCol + (it & 1) * NT;
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk) {
+                    const uint64_t a = sw128_desc(sq + (kk / 4) * Sm::kQHalf + (kk % 4) * 32, 16, 1024);
+                    const uint64_t b = sw128_desc(kb + (kk / 4) * Sm::kKVHalf + (kk % 4) * 32, 16, 1024);
+                    tc_mma_f16(dcol, a, b, idesc_s, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(&s_full[it & 1]);
+            };
+            if (ok)
+                ok = mbar_wait(&full[0], 0);
+            if (ok) {
+                tc_fence_after();
+                issue_scores(0);
+            }
+            for (int it = 0; it < ntiles && ok; ++it) {
+                if (it + 1 < ntiles) {
+                    ok = mbar_wait(&full[(it + 1) % NST], ((it + 1) / NST) & 1);
+                    if (ok && it >= 1)        // S buffer (it+1)&1 was read by the softmax of tile it-1
+                        ok = mbar_wait(&s_free[(it + 1) & 1], ((it - 1) >> 1) & 1);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    issue_scores(it + 1);
+                }
+                ok = mbar_wait(&p_full[it & 1], (it >> 1) & 1);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                const uint32_t vb =
+                    smem_addr(smem + Sm::kStageOff + (it % NST) * Sm::kStageBytes + Sm::kKBytes);
+                const uint32_t pb = smem_addr(smem + Sm::kPOff + (it & 1) * 2 * Sm::kPBytes);
+#pragma unroll
+                for (int half = 0; half < 2; ++half)          // hi, then lo
+#pragma unroll
+                    for (int kk = 0; kk < NT / 16; ++kk) {
+                        const uint64_t a = sw128_desc(pb + half * Sm::kPBytes + kk * 32, 16, 1024);
+                        const uint64_t b = sw128_desc(vb + kk * 16 * 128, Sm::kKVHalf, 1024);
+                        tc_mma_f16(tbase, a, b, idesc_o, (it > 0 || half > 0 || kk > 0) ? 1u : 0u);
+                    }
+                tc_commit(&empty[it % NST]);
+                tc_commit(&pv_done[it & 1]);
+            }
+            if (!ok)
+                atomicOr(p.err, PA_DEVERR_TIMEOUT);
+            tc_commit(mma_done);              // every MMA above completes before TMEM is freed
+            mbar_wait(mma_done, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax warps
+        const int wq = warp & 3;                         // TMEM lane quarter of this warp
+        const int r = 32 * wq + lane;                    // tile row = TMEM lane
+        const int tok = r / G;
+        const int g = r - tok * G;
+        const bool row_valid = tok < ntok;               // (r >= TT * G gives tok >= TT)
+        const int pos = pos_first + tok;
+        const int64_t qrow = (int64_t)(qs0 + j0 + tok) * p.num_q_heads + (int64_t)kvh * G + g;
+        {
+            // Q rows into the 128-byte-swizzled operand layout; rows past the chunk are 0
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
+                                                              (row_valid ? qrow : 0) * D);
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                const uint4 v = row_valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(smem + Sm::kQOff + (c / 8) * Sm::kQHalf + r * 128 +
+                                          (((c & 7) ^ (r & 7)) << 4)) = v;
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(q_full);
+
+        const bool warp_live = __any_sync(kFullMask, row_valid);
+        const uint32_t lane_t = tbase + ((uint32_t)(32 * wq) << 16);
+        const float sl2 = p.scale_log2;
+        float m_ref = -INFINITY, lsum = 0.f;
+        bool poisoned = false;
+        for (int it = 0; it < ntiles; ++it) {
+            const int b = it & 1;
+            const int st = it % NST;
+            const int tb = t0 + it * NT;
+            bool ok = mbar_wait(&s_full[b], (it >> 1) & 1);
+            ok = ok && mbar_wait(&full[st], (it / NST) & 1);   // stage_ok and the tile's bytes
+            if (!ok) {
+                if (lane == 0)
+                    atomicOr(p.err, PA_DEVERR_TIMEOUT);
+                poisoned = true;
+                break;
+            }
+            if (!stage_ok[st])
+                poisoned = true;
+            tc_fence_after();
+            float s[NT];
+            if (warp_live) {
+                tmem_ld32(lane_t + Sm::kSCol + b * NT, *reinterpret_cast<float(*)[32]>(&s[0]));
+                tmem_ld32(lane_t + Sm::kSCol + b * NT + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&s_free[b]);
+
+            uint32_t hi[NT / 2], lo[NT / 2];
+            if (warp_live) {
+                const int lim = row_valid ? pos - tb : -1;   // columns c <= lim are visible
+                float tmax = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < NT; ++c) {
+                    s[c] = c <= lim ? s[c] * sl2 : -INFINITY;
+                    tmax = fmaxf(tmax, s[c]);
+                }
+                const bool need = tmax > m_ref + 8.f;
+                if (__any_sync(kFullMask, need && it > 0)) {
+                    // O holds P.V of tiles 0 .. it-1: wait for the last, then rescale the
+                    // rows whose reference maximum moves
+                    if (!mbar_wait(&pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1)) {
+                        if (lane == 0)
+                            atomicOr(p.err, PA_DEVERR_TIMEOUT);
+                        poisoned = true;
+                    }
+                    tc_fence_after();
+                    const float alpha = need ? exp2f(m_ref - tmax) : 1.f;
+#pragma unroll 1
+                    for (int c4 = 0; c4 < D / 32; ++c4) {
+                        float o[32];
+                        tmem_ld32(lane_t + 32 * c4, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            o[i] *= alpha;
+                        tmem_st32(lane_t + 32 * c4, o);
+                    }
+                }
+                if (need) {
+                    lsum *= exp2f(m_ref - tmax);
+                    m_ref = tmax;
+                }
+                float rs = 0.f;
+                const bool any = m_ref != -INFINITY;
+#pragma unroll
+                for (int c = 0; c < NT; c += 2) {
+                    const float p0 = any ? exp2f(s[c] - m_ref) : 0.f;
+                    const float p1 = any ? exp2f(s[c + 1] - m_ref) : 0.f;
+                    rs += p0 + p1;
+                    const uint32_t h2 = pack2<T>(p0, p1);
+                    const float2 hf = unpack2<T>(h2);
+                    hi[c / 2] = h2;
+                    lo[c / 2] = pack2<T>(p0 - hf.x, p1 - hf.y);
+                }
+                lsum += rs;
+            }
+            // P buffer b was last read by P.V of tile it-2
+            if (it >= 2 && !mbar_wait(&pv_done[b], ((it - 2) >> 1) & 1)) {
+                if (lane == 0)
+                    atomicOr(p.err, PA_DEVERR_TIMEOUT);
+                poisoned = true;
+                break;
+            }
+            if (warp_live) {
+                unsigned char* ph = smem + Sm::kPOff + b * 2 * Sm::kPBytes + r * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int off = (c ^ (r & 7)) << 4;
+                    *reinterpret_cast<uint4*>(ph + off) =
+                        make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+                    *reinterpret_cast<uint4*>(ph + Sm::kPBytes + off) =
+                        make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+                }
+            }
+            if (tb + NT > t1) {
+                // V rows past the range may hold anything (unused slots, stale tiles):
+                // zero them so that 0 * V stays 0
+                const int v0 = t1 - tb;
+                const int rows = NT - v0;
+                unsigned char* vbase = smem + Sm::kStageOff + st * Sm::kStageBytes + Sm::kKBytes;
+                const int tid = threadIdx.x - 64;
+                for (int idx = tid; idx < Sm::kHalves * rows * 8; idx += 128) {
+                    const int h = idx / (rows * 8);
+                    const int w = idx - h * rows * 8;
+                    *reinterpret_cast<uint4*>(vbase + h * Sm::kKVHalf + (v0 + w / 8) * 128 +
+                                              (w % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&p_full[b]);
+        }
+
+        // ---------------------------------------------------------------- epilogue
+        if (!mbar_wait(&pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) {
+            if (lane == 0)
+                atomicOr(p.err, PA_DEVERR_TIMEOUT);
+            poisoned = true;
+        }
+        tc_fence_after();
+        if (warp_live) {
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            const int which = split || p.out_f32 ? 0 : (DType<T>::id == PA_F16 ? 1 : 2);
+#pragma unroll 1
+            for (int c4 = 0; c4 < D / 32; ++c4) {
+                float o[32];
+                tmem_ld32(lane_t + 32 * c4, o);
+                if (!row_valid)
+                    continue;
+                if (split) {
+                    const int64_t prow = qrow * p.max_parts + part;
+                    store_row32(p.part_o, prow * D + 32 * c4, o, inv, poisoned, 0);
+                    if (c4 == 0) {
+                        p.part_ml[prow * 2 + 0] = poisoned ? __int_as_float(0x7fc00000) : m_ref;
+                        p.part_ml[prow * 2 + 1] = lsum;
+                    }
+                } else {
+                    store_row32(p.out, qrow * D + 32 * c4, o, inv, poisoned, which);
+                }
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, Sm::kTmemCols);
+    }
+}
+
+// Merges the partitions of a split chunk launch: one CTA of D threads per
+// (query row, query head); grid = (rows, num_q_heads).
+template <typename T, int D>
+__global__ void __launch_bounds__(D) chunk_reduce_kernel(const ChunkParams p)
+{
+    const int64_t row = blockIdx.x;
+    const int h = blockIdx.y;
+    const int d = threadIdx.x;
+    // the sequence owning the row: query_start[s] <= row < query_start[s + 1]
+    int lo = 0, hi = p.num_seqs;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.query_start[mid] <= row)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    const int s = lo;
+    const int qs0 = p.query_start[s], qs1 = p.query_start[s + 1];
+    const int n = qs1 - qs0;
+    const int L = p.context_lens[s];
+    const int64_t idx = (row * p.num_q_heads + h) * D + d;
+    float out;
+    if (row < qs0 || row >= qs1 || n > L || L < 0 || L > p.max_context_len || n > p.max_query_len) {
+        out = __int_as_float(0x7fc00000);
+        if (d == 0 && h == 0)
+            atomicOr(p.err, PA_DEVERR_CONTEXT_LEN);
+    } else {
+        const int pos = L - n + (int)(row - qs0);
+        const int nparts = min(p.max_parts, (pos + p.partition_tokens) / p.partition_tokens);
+        const int64_t prow0 = (row * p.num_q_heads + h) * p.max_parts;
+        float M = -INFINITY;
+        for (int k = 0; k < nparts; ++k)
+            M = fmaxf(M, p.part_ml[(prow0 + k) * 2]);
+        float num = 0.f, den = 0.f;
+        for (int k = 0; k < nparts; ++k) {
+            const float mk = p.part_ml[(prow0 + k) * 2];
+            const float w = mk == -INFINITY ? 0.f : exp2f(mk - M) * p.part_ml[(prow0 + k) * 2 + 1];
+            num = fmaf(w, p.part_o[(prow0 + k) * D + d], num);
+            den += w;
+        }
+        // a poisoned partition (NaN) makes the row NaN; no visible token gives 0
+        out = den > 0.f ? num / den : (den == 0.f ? 0.f : __int_as_float(0x7fc00000));
+    }
+    if (p.out_f32)
+        store_as(static_cast<float*>(p.out) + idx, out);
+    else
+        store_as(static_cast<T*>(p.out) + idx, out);
+}
+
+}  // namespace pa

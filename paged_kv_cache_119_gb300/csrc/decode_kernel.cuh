@@ -504,25 +504,6 @@ struct DecodeStages {
         kDecodeConsumerWarps * (kPerWarp < 1 ? 1 : (kPerWarp > 3 ? 3 : kPerWarp));
 };
 
-// Sets the dynamic shared-memory limit of a kernel once per device and process.
-inline cudaError_t configure_once(const void* kernel, int smem_bytes)
-{
-    static std::mutex mu;
-    static std::vector<std::pair<const void*, int>> done;   // (kernel, device)
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess)
-        return err;
-    std::lock_guard<std::mutex> lock(mu);
-    for (const auto& d : done)
-        if (d.first == kernel && d.second == dev)
-            return cudaSuccess;
-    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-    if (err == cudaSuccess)
-        done.emplace_back(kernel, dev);
-    return err;
-}
-
 // Resident CTAs per SM for a decode kernel with this dynamic shared memory.
 inline int kernel_occupancy(const void* kernel, int smem_bytes)
 {

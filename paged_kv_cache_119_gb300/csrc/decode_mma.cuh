@@ -34,23 +34,6 @@
 
 namespace pa {
 
-__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map)
-{
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-// 3-D tensor-map TMA load (x = head dim, y = token in block, z = block*Hkv + head).
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
-                                            uint64_t* bar, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)),
-        "l"(policy)
-        : "memory");
-}
-
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"

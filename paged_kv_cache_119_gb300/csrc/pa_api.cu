@@ -80,6 +80,30 @@ int choose_partition(int partition_size, int max_context_len, int64_t units, int
     return P >= max_context_len ? 0 : P;
 }
 
+// Partition length of the chunk-attention kernel (a multiple of its 64-token K/V
+// tile), or 0 for one pass; the same one-wave rule as choose_partition.
+int choose_chunk_partition(int partition_size, int max_context_len, int64_t units, int64_t slots)
+{
+    if (partition_size < 0)
+        return 0;
+    if (partition_size > 0)
+        return max_context_len > partition_size ? partition_size : 0;
+    const int pmin = kAutoPartitionTokens;
+    if (max_context_len <= pmin)
+        return 0;
+    if (slots <= 0)
+        slots = 148;
+    if (2 * units > slots)
+        return 0;
+    const int64_t max_parts = (max_context_len + pmin - 1) / pmin;
+    const int64_t parts = std::min<int64_t>(slots / units, max_parts);
+    if (parts <= 1)
+        return 0;
+    const int per = (int)((max_context_len + parts - 1) / parts);
+    const int P = (per + 63) / 64 * 64;
+    return P >= max_context_len ? 0 : P;
+}
+
 size_t workspace_layout(int64_t rows, int max_parts, int head_dim, size_t* ml_offset)
 {
     const size_t o_bytes = align_up((size_t)rows * max_parts * head_dim * sizeof(float), 256);
@@ -379,6 +403,122 @@ int pa_decode_fp8(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype
                        v_scale, num_blocks, block_tables, block_table_stride, context_lens,
                        max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
                        block_size, scale, partition_size, workspace, workspace_bytes, stream);
+}
+
+size_t pa_chunk_workspace_bytes(int64_t num_query_tokens, int32_t num_q_heads, int32_t head_dim,
+                                int32_t max_context_len, int32_t partition_size)
+{
+    if (num_query_tokens < 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0 ||
+        partition_size < 0)
+        return 0;
+    const int P = partition_size > 0 ? partition_size : kAutoPartitionTokens;
+    if (max_context_len <= P)
+        return 0;
+    const int max_parts = (max_context_len + P - 1) / P;
+    return workspace_layout(num_query_tokens * num_q_heads, max_parts, head_dim, nullptr);
+}
+
+int pa_chunk_attention(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
+                       const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
+                       const int32_t* block_tables, int64_t block_table_stride,
+                       const int32_t* context_lens, const int32_t* query_start,
+                       int64_t num_query_tokens, int32_t max_query_len, int32_t max_context_len,
+                       int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, float scale, int32_t partition_size,
+                       void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (!(kv_dtype == PA_F16 || kv_dtype == PA_BF16)) {
+        return (kv_dtype == PA_F32 || kv_dtype == PA_FP8_E4M3) ? PA_ERR_UNSUPPORTED
+                                                               : PA_ERR_INVALID;
+    }
+    if (!(out_dtype == PA_F32 || out_dtype == kv_dtype))
+        return PA_ERR_INVALID;
+    if (num_seqs < 0 || num_seqs > 65535 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > 128)
+        return PA_ERR_INVALID;
+    if (!(head_dim == 64 || head_dim == 128) || !(block_size == 16 || block_size == 32))
+        return PA_ERR_UNSUPPORTED;
+    if (num_blocks <= 0 || num_blocks > INT32_MAX || block_table_stride <= 0 ||
+        max_context_len < 0 || (int64_t)max_context_len > block_table_stride * block_size ||
+        max_query_len < 0 || max_query_len > max_context_len || num_query_tokens < 0 ||
+        num_query_tokens > INT32_MAX || !std::isfinite(scale))
+        return PA_ERR_INVALID;
+    if (partition_size > 0 && partition_size % 64 != 0)
+        return PA_ERR_INVALID;
+    if (num_seqs == 0 || num_query_tokens == 0 || max_query_len == 0)
+        return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start)
+        return PA_ERR_INVALID;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID;
+    const int group = num_q_heads / num_kv_heads;
+    const int rows_tokens = 128 / group;
+    const int m_tiles = (max_query_len + rows_tokens - 1) / rows_tokens;
+    if ((int64_t)num_kv_heads * m_tiles > 65535)
+        return PA_ERR_INVALID;
+    const size_t row_elems = (size_t)num_query_tokens * num_q_heads * head_dim;
+    const size_t q_bytes = row_elems * elem_size(kv_dtype);
+    const size_t out_bytes = row_elems * elem_size(out_dtype);
+    const size_t pool_bytes =
+        (size_t)num_blocks * num_kv_heads * block_size * head_dim * elem_size(kv_dtype);
+    if (overlaps(out, out_bytes, q, q_bytes) || overlaps(out, out_bytes, k_cache, pool_bytes) ||
+        overlaps(out, out_bytes, v_cache, pool_bytes))
+        return PA_ERR_INVALID;
+
+    int occ = 0;
+    if (partition_size == 0)
+        occ = occupancy_chunk_attention(kv_dtype, head_dim, block_size);
+    const int P = choose_chunk_partition(partition_size, max_context_len,
+                                         (int64_t)num_seqs * num_kv_heads * m_tiles,
+                                         (int64_t)device_sm_count() * occ);
+    ChunkParams p{};
+    p.out = out;
+    p.q = q;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.query_start = query_start;
+    p.num_blocks = num_blocks;
+    p.bt_stride = block_table_stride;
+    p.num_rows = num_query_tokens;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = group;
+    p.rows_tokens = rows_tokens;
+    p.m_tiles = m_tiles;
+    p.max_query_len = max_query_len;
+    p.max_context_len = max_context_len;
+    p.partition_tokens = P;
+    p.max_parts = 1;
+    p.out_f32 = out_dtype == PA_F32 ? 1 : 0;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);  // log2(e)
+    if (P > 0) {
+        p.max_parts = (max_context_len + P - 1) / P;
+        size_t ml_off = 0;
+        const size_t need = workspace_layout(num_query_tokens * num_q_heads, p.max_parts,
+                                             head_dim, &ml_off);
+        if (!workspace || workspace_bytes < need || !aligned16(workspace))
+            return PA_ERR_WORKSPACE;
+        if (overlaps(out, out_bytes, workspace, need))
+            return PA_ERR_INVALID;
+        p.part_o = static_cast<float*>(workspace);
+        p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ml_off);
+    }
+    p.err = device_error_word();
+    if (!p.err)
+        return PA_ERR_CUDA;
+    CUtensorMap tk{}, tv{};
+    cudaError_t e = kv_tensor_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim,
+                                  kv_dtype);
+    if (e == cudaSuccess)
+        e = kv_tensor_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim, kv_dtype);
+    if (e == cudaErrorInvalidValue)
+        return PA_ERR_INVALID;
+    if (e != cudaSuccess)
+        return PA_ERR_CUDA;
+    e = launch_chunk_attention(p, kv_dtype, head_dim, block_size, tk, tv,
+                               static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 int pa_reshape_and_cache_fp8(const void* k, const void* v, pa_dtype src_dtype, void* k_cache,

@@ -6,6 +6,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <utility>
+#include <vector>
+
 #include "pa.h"
 
 namespace pa {
@@ -123,6 +127,59 @@ cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);
 // shape, dtype).
 cudaError_t kv_tensor_map(CUtensorMap* map, const void* base, int64_t num_blocks, int num_kv_heads,
                           int block_size, int head_dim, pa_dtype dtype);
+
+// Causal attention of chunks of new query tokens over the paged cache (the
+// tensor-core kernel of chunk_attn.cuh).  Rows of q / out are (query token, query
+// head) pairs, [num_rows][num_q_heads][head_dim].
+struct ChunkParams {
+    void* out;                   // [num_rows][Hq][D], fp32 or the cache dtype
+    const void* q;               // [num_rows][Hq][D], the cache dtype
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    const int32_t* query_start;  // [num_seqs + 1]
+    float* part_o;               // [num_rows][Hq][max_parts][D] (split only)
+    float* part_ml;              // [num_rows][Hq][max_parts][2]
+    unsigned* err;
+    int64_t num_blocks;
+    int64_t bt_stride;
+    int64_t num_rows;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;                   // num_q_heads / num_kv_heads (<= 128)
+    int rows_tokens;             // chunk tokens per CTA row tile: 128 / group
+    int m_tiles;                 // row tiles per (sequence, kv head)
+    int max_query_len;
+    int max_context_len;
+    int partition_tokens;        // 0: one pass; else a multiple of 64
+    int max_parts;
+    int out_f32;
+    float scale_log2;
+};
+cudaError_t launch_chunk_attention(const ChunkParams& p, pa_dtype dtype, int head_dim,
+                                   int block_size, const CUtensorMap& tk, const CUtensorMap& tv,
+                                   cudaStream_t stream);
+// Resident chunk-attention CTAs per SM (0 if unknown).
+int occupancy_chunk_attention(pa_dtype dtype, int head_dim, int block_size);
+
+// Sets the dynamic shared-memory limit of a kernel once per device and process.
+inline cudaError_t configure_once(const void* kernel, int smem_bytes)
+{
+    static std::mutex mu;
+    static std::vector<std::pair<const void*, int>> done;   // (kernel, device)
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const auto& d : done)
+        if (d.first == kernel && d.second == dev)
+            return cudaSuccess;
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (err == cudaSuccess)
+        done.emplace_back(kernel, dev);
+    return err;
+}
 
 // The calling device's error word (device address), or nullptr on failure.
 unsigned* device_error_word();

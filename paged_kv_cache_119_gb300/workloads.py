@@ -16,6 +16,10 @@ tensors stand in for them.
 Conventions:
   * context_lens[s] counts the current token; the pool holds tokens
     0 .. L-2 before the step and the step's reshape_and_cache writes token L-1.
+  * chunk workloads (``query_len`` > 1: chunked prefill, speculative
+    verification) give sequence s n_s = min(query_len, L) new tokens: the pool
+    holds tokens 0 .. L-n_s-1, the step writes the last n_s, and q has one row
+    per new token ([sum n_s, Hq, D], rows of sequence s at query_start[s] ..).
   * block_tables rows are padded with -1 past ceil(L/B) entries.
   * every pool slot that holds no cached token is NaN, so a kernel that reads
     outside a context produces NaN instead of a plausible number.
@@ -54,11 +58,16 @@ class Workload:
     slot_mapping: torch.Tensor      # int64 [T]
     copy_pairs: np.ndarray | None = None   # int64 [P, 2] (src, dst), host
     partition_size: int = 0
+    query_start: torch.Tensor | None = None   # int32 [S+1] for chunk workloads
     meta: dict = field(default_factory=dict)
 
     @property
     def max_context_len(self) -> int:
         return int(self.meta["max_context_len"])
+
+    @property
+    def max_query_len(self) -> int:
+        return int(self.meta.get("max_query_len", 1))
 
     @property
     def fp8(self) -> bool:
@@ -85,7 +94,7 @@ def _normal(shape, std: float, dtype: torch.dtype, device, gen_seed: int) -> tor
 
 def _assemble(name, rng, device, *, lens, Hq, Hkv, D, B, dtype, std, pool_slack=1.1,
               tables=None, num_blocks=None, filled=None, new_tokens=None, scale=None,
-              copy_pairs=None, partition_size=0, extra_meta=None) -> Workload:
+              copy_pairs=None, partition_size=0, extra_meta=None, chunk=None) -> Workload:
     """Common tail: pools, q, new rows, slot mapping.
 
     lens        : context lengths (current token included), list[int]
@@ -94,6 +103,9 @@ def _assemble(name, rng, device, *, lens, Hq, Hkv, D, B, dtype, std, pool_slack=
                   from tables, tokens 0..L-2 of each sequence)
     new_tokens  : optional list of (seq, position) pairs whose K/V rows the step
                   writes (default: position L-1 of every sequence with L > 0)
+    chunk       : optional list of per-sequence new-token counts n_s <= L_s: the
+                  pool then holds tokens 0 .. L-n_s-1, the step writes the rest and
+                  q gets one row per new token
     """
     S = len(lens)
     if tables is None:
@@ -109,14 +121,15 @@ def _assemble(name, rng, device, *, lens, Hq, Hkv, D, B, dtype, std, pool_slack=
     bt = np.full((S, W), -1, dtype=np.int32)
     for s, t in enumerate(tables):
         bt[s, :len(t)] = t
+    cached = [L - (1 if chunk is None else chunk[s]) for s, L in enumerate(lens)]
     if filled is None:
         filled = {}
         for s, L in enumerate(lens):
             for j, b in enumerate(tables[s]):
-                n_old = max(0, min(B, (L - 1) - j * B))
+                n_old = max(0, min(B, cached[s] - j * B))
                 filled[b] = max(filled.get(b, 0), n_old)
     if new_tokens is None:
-        new_tokens = [(s, L - 1) for s, L in enumerate(lens) if L > 0]
+        new_tokens = [(s, p) for s, L in enumerate(lens) for p in range(max(cached[s], 0), L)]
     seed0 = int(rng.integers(0, 2**31 - 1))
 
     count = torch.zeros(num_blocks, dtype=torch.int64)
@@ -129,7 +142,8 @@ def _assemble(name, rng, device, *, lens, Hq, Hkv, D, B, dtype, std, pool_slack=
     shape = (num_blocks, Hkv, B, D)
     k_cache = _normal(shape, std, dtype, device, seed0 + 1).masked_fill_(empty, float("nan"))
     v_cache = _normal(shape, std, dtype, device, seed0 + 2).masked_fill_(empty, float("nan"))
-    q = _normal((S, Hq, D), std, dtype, device, seed0 + 3)
+    rows = S if chunk is None else int(sum(chunk))
+    q = _normal((rows, Hq, D), std, dtype, device, seed0 + 3)
     T = len(new_tokens)
     k_new = _normal((T, Hkv, D), std, dtype, device, seed0 + 4)
     v_new = _normal((T, Hkv, D), std, dtype, device, seed0 + 5)
@@ -137,6 +151,12 @@ def _assemble(name, rng, device, *, lens, Hq, Hkv, D, B, dtype, std, pool_slack=
     slot_mapping = torch.tensor(slots, dtype=torch.int64).to(device)
     meta = {"total_tokens": int(sum(lens)), "max_context_len": int(max(lens, default=0)),
             "std": std, "new_tokens": new_tokens, "filled_blocks": len(filled)}
+    query_start = None
+    if chunk is not None:
+        meta["max_query_len"] = int(max(chunk, default=0))
+        meta["query_tokens"] = rows
+        query_start = torch.tensor(np.concatenate([[0], np.cumsum(chunk)]),
+                                   dtype=torch.int32).to(device)
     meta.update(extra_meta or {})
     return Workload(
         name=name, num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=B,
@@ -146,7 +166,7 @@ def _assemble(name, rng, device, *, lens, Hq, Hkv, D, B, dtype, std, pool_slack=
         block_tables=torch.from_numpy(bt).to(device), q=q, k_cache=k_cache, v_cache=v_cache,
         k_new=k_new, v_new=v_new, slot_mapping=slot_mapping,
         copy_pairs=None if copy_pairs is None else np.asarray(copy_pairs, dtype=np.int64),
-        partition_size=partition_size, meta=meta)
+        partition_size=partition_size, meta=meta, query_start=query_start)
 
 
 def to_fp8(w: Workload, headroom: float = 8.0) -> Workload:
@@ -204,15 +224,18 @@ def opt13b(device="cpu", seed=None, num_seqs=64, max_len=2048, dtype=torch.float
                      dtype=dtype, std=1.0, **kw)
 
 
-def llama13b(device="cpu", seed=None, num_seqs=256, dtype=torch.bfloat16, **kw):
+def llama13b(device="cpu", seed=None, num_seqs=256, dtype=torch.bfloat16, query_len=1,
+             name="llama13b", **kw):
     """LLaMA-13B-shaped batched decode: 40 MHA heads, head_dim 128, bf16, block_size 16,
     lengths lognormal (median 400, sigma 0.8) rounded and clipped to [16, 2048],
-    N(0, 0.5) values, one new token per sequence."""
+    N(0, 0.5) values, one new token per sequence (``query_len`` > 1: that many new
+    tokens per sequence, attended causally, as in speculative verification)."""
     rng = _rng("llama13b", seed)
     raw = rng.lognormal(mean=math.log(400.0), sigma=0.8, size=num_seqs)
     lens = [int(min(2048, max(16, round(x)))) for x in raw]
-    return _assemble("llama13b", rng, device, lens=lens, Hq=40, Hkv=40, D=128, B=16,
-                     dtype=dtype, std=0.5, **kw)
+    chunk = None if query_len == 1 else [min(query_len, L) for L in lens]
+    return _assemble(name, rng, device, lens=lens, Hq=40, Hkv=40, D=128, B=16,
+                     dtype=dtype, std=0.5, chunk=chunk, **kw)
 
 
 def prefix(device="cpu", seed=None, num_groups=16, group_size=8, prefix_blocks=64,
@@ -277,15 +300,18 @@ def prefix(device="cpu", seed=None, num_groups=16, group_size=8, prefix_blocks=6
 
 
 def long_context(device="cpu", seed=None, block_size=16, num_seqs=8, context=32768,
-                 dtype=torch.bfloat16, partition_size=512, **kw):
+                 dtype=torch.bfloat16, partition_size=512, query_len=1, name=None, **kw):
     """Long-context split-context decode: 64 query / 8 kv heads, head_dim 128, bf16,
     ``num_seqs`` sequences of ``context`` tokens, block_size 16 or 32, randomly
-    permuted pool, N(0,1), split into ``partition_size``-token partitions."""
-    name = "long16" if block_size == 16 else "long32"
-    rng = _rng(name, seed)
+    permuted pool, N(0,1), split into ``partition_size``-token partitions.
+    ``query_len`` > 1: the last ``query_len`` tokens of each context are new and
+    attended causally (a chunked-prefill step)."""
+    base = "long16" if block_size == 16 else "long32"
+    rng = _rng(base, seed)
     lens = [int(context)] * num_seqs
-    return _assemble(name, rng, device, lens=lens, Hq=64, Hkv=8, D=128, B=block_size,
-                     dtype=dtype, std=1.0, partition_size=partition_size, **kw)
+    chunk = None if query_len == 1 else [min(query_len, L) for L in lens]
+    return _assemble(name or base, rng, device, lens=lens, Hq=64, Hkv=8, D=128, B=block_size,
+                     dtype=dtype, std=1.0, partition_size=partition_size, chunk=chunk, **kw)
 
 
 CONFIGS = {
@@ -295,6 +321,13 @@ CONFIGS = {
     "prefix": prefix,
     "long16": lambda device="cpu", seed=None, **kw: long_context(device, seed, 16, **kw),
     "long32": lambda device="cpu", seed=None, **kw: long_context(device, seed, 32, **kw),
+    # multi-token queries: speculative verification of 4 tokens per sequence on the
+    # LLaMA-13B batch, and a 512-token chunked-prefill step on the long contexts
+    "llama13b_verify4": lambda device="cpu", seed=None, **kw: llama13b(
+        device, seed, **{"query_len": 4, "name": "llama13b_verify4", **kw}),
+    "long16_chunk512": lambda device="cpu", seed=None, **kw: long_context(
+        device, seed, 16, **{"query_len": 512, "name": "long16_chunk512", "partition_size": 0,
+                             **kw}),
 }
 
 

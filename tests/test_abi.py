@@ -155,3 +155,51 @@ def test_noalloc_rejects_oversized_and_unsplit_requests(lib):
     args = decode_args(part=-1)
     del args[18:20]
     assert lib.pa_decode_noalloc(*args) == N.PA_ERR_INVALID
+
+
+def chunk_args(**kw):
+    a = dict(out=FAKE, out_dtype=N.PA_F32, q=FAKE * 16, k=FAKE * 48, v=FAKE * 96,
+             kv_dtype=N.PA_BF16, num_blocks=10, bt=FAKE * 130, bt_stride=8, cl=FAKE * 131,
+             qs=FAKE * 132, R=12, max_q=6, max_ctx=64, S=3, Hq=8, Hkv=2, D=128, B=16,
+             scale=0.1, part=-1, ws=0, ws_bytes=0, stream=0)
+    a.update(kw)
+    return [a[k] for k in ("out", "out_dtype", "q", "k", "v", "kv_dtype", "num_blocks", "bt",
+                           "bt_stride", "cl", "qs", "R", "max_q", "max_ctx", "S", "Hq", "Hkv",
+                           "D", "B", "scale", "part", "ws", "ws_bytes", "stream")]
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(kv_dtype=N.PA_F32), N.PA_ERR_UNSUPPORTED),                # tensor-core path: 16-bit
+    (dict(kv_dtype=9), N.PA_ERR_INVALID),
+    (dict(out_dtype=N.PA_F16), N.PA_ERR_INVALID),                 # neither f32 nor the kv dtype
+    (dict(Hq=6, Hkv=4), N.PA_ERR_INVALID),
+    (dict(Hq=258, Hkv=1), N.PA_ERR_INVALID),                      # group above 128
+    (dict(D=96), N.PA_ERR_UNSUPPORTED),
+    (dict(B=8), N.PA_ERR_UNSUPPORTED),
+    (dict(max_q=65), N.PA_ERR_INVALID),                           # chunk longer than any context
+    (dict(max_ctx=8 * 16 + 1, max_q=6), N.PA_ERR_INVALID),        # beyond the table row
+    (dict(R=-1), N.PA_ERR_INVALID),
+    (dict(part=96), N.PA_ERR_INVALID),                            # not a multiple of 64
+    (dict(qs=0), N.PA_ERR_INVALID),
+    (dict(k=FAKE * 48 + 8), N.PA_ERR_INVALID),                    # misaligned cache
+    (dict(out=FAKE * 16), N.PA_ERR_INVALID),                      # out aliases q
+    (dict(S=70000), N.PA_ERR_INVALID),
+    (dict(scale=float("inf")), N.PA_ERR_INVALID),
+])
+def test_chunk_attention_rejects(lib, kw, status):
+    assert lib.pa_chunk_attention(*chunk_args(**kw)) == status
+
+
+def test_chunk_attention_empty_is_a_no_op(lib):
+    assert lib.pa_chunk_attention(*chunk_args(S=0)) == N.PA_OK
+    assert lib.pa_chunk_attention(*chunk_args(R=0)) == N.PA_OK
+    assert lib.pa_chunk_attention(*chunk_args(max_q=0)) == N.PA_OK
+
+
+def test_chunk_workspace_bytes(lib):
+    # 100 query rows x 64 heads x 64 partitions x (128 + 2) fp32 values
+    assert lib.pa_chunk_workspace_bytes(100, 64, 128, 32768, 512) == \
+        100 * 64 * 64 * 128 * 4 + 100 * 64 * 64 * 2 * 4
+    assert lib.pa_chunk_workspace_bytes(100, 64, 128, 512, 512) == 0
+    assert lib.pa_chunk_workspace_bytes(100, 64, 128, 4096, 0) > 0
+    assert lib.pa_chunk_workspace_bytes(-1, 64, 128, 4096, 0) == 0

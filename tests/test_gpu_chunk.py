@@ -1,0 +1,219 @@
+"""Chunk attention (several new query tokens per sequence, attended causally over the
+paged cache) on the GPU against the CPU oracle.
+
+Each case runs the step as a caller would: pa_reshape_and_cache writes the chunk's
+K/V rows (bit-exact against the oracle's byte copy), then pa_chunk_attention; the
+attention output is compared element by element with the oracle's fp64 result
+(max abs error <= 2e-3 on fp32 output; native output must be the round-to-nearest-
+even of a value within 5e-5 of the oracle).  Head groupings 1, 4, 5 and 8, head_dim
+64 / 128, block_size 16 / 32, fp16 / bf16, ragged chunks (n = L, n = 1, n = 0),
+forced and automatic context splits.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_119_gb300 as P
+from paged_kv_cache_119_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+ATOL = 2e-3
+NATIVE_EPS = 5e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_cache_119_gb300 import build
+    build.build()
+
+
+@pytest.fixture(autouse=True)
+def clear_error_word(built):
+    P.pa_get_device_error()
+    yield
+
+
+def make_case(seed, S, Hq, Hkv, D, B, dtype, lens, chunks, std=1.0):
+    rng = np.random.default_rng(seed)
+    return workloads._assemble("chunk_case", rng, "cuda", lens=lens, Hq=Hq, Hkv=Hkv, D=D, B=B,
+                               dtype=dtype, std=std, chunk=chunks)
+
+
+def run_and_compare(w, out_dtype=torch.float32, partition_size=0, check_caches=True):
+    snap = {n: getattr(w, n).cpu() for n in ("q", "k_cache", "v_cache", "k_new", "v_new",
+                                             "slot_mapping", "block_tables", "context_lens",
+                                             "query_start")}
+    P.pa_reshape_and_cache(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping)
+    out = torch.empty(w.q.shape, dtype=out_dtype, device="cuda")
+    P.pa_chunk_attention(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                         w.query_start, w.scale, w.num_kv_heads, w.block_size,
+                         max_query_len=w.max_query_len, max_context_len=w.max_context_len,
+                         partition_size=partition_size)
+    torch.cuda.synchronize()
+    kc, vc = snap["k_cache"].clone(), snap["v_cache"].clone()
+    oracle.reshape_and_cache(snap["k_new"], snap["v_new"], kc, vc, snap["slot_mapping"],
+                             w.block_size)
+    if check_caches:
+        assert torch.equal(w.k_cache.cpu().view(torch.int16), kc.view(torch.int16))
+        assert torch.equal(w.v_cache.cpu().view(torch.int16), vc.view(torch.int16))
+    ref = oracle.chunk_attention(snap["q"], kc, vc, snap["block_tables"], snap["context_lens"],
+                                 snap["query_start"], w.scale, w.num_kv_heads, w.block_size,
+                                 num_threads=oracle.max_threads())
+    got = out.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    if out_dtype == torch.float32:
+        err = np.abs(got - ref).max() if got.size else 0.0
+        assert err <= ATOL, f"max abs error {err:.3e}"
+    else:
+        lo = torch.from_numpy((ref - NATIVE_EPS).astype(np.float32)).to(out_dtype).double().numpy()
+        hi = torch.from_numpy((ref + NATIVE_EPS).astype(np.float32)).to(out_dtype).double().numpy()
+        bad = (got < lo) | (got > hi)
+        assert not bad.any(), f"{bad.sum()} outputs outside the rounding bracket"
+    assert P.pa_get_device_error() == 0
+    return got, ref
+
+
+def test_verify4_llama13b_shape():
+    """Speculative verification of 4 tokens per sequence on the LLaMA-13B batch shape
+    (MHA: one chunk token row per CTA row group)."""
+    w = workloads.make("llama13b_verify4", device="cuda", num_seqs=12)
+    run_and_compare(w)
+
+
+@pytest.mark.parametrize("part", [0, 512, -1])
+def test_chunk512_long_context_shape(part):
+    """A chunked-prefill step (GQA 8) on a shortened long-context configuration."""
+    w = workloads.make("long16_chunk512", device="cuda", num_seqs=2, context=1500,
+                       query_len=300)
+    run_and_compare(w, partition_size=part)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 4), (40, 8), (64, 8)])
+@pytest.mark.parametrize("D,B", [(128, 16), (64, 32), (128, 32), (64, 16)])
+def test_head_groupings(Hq, Hkv, D, B):
+    rng = np.random.default_rng(Hq * 1000 + D + B)
+    lens = [1, 17, 64, 65, 129, 300]
+    chunks = [1, 17, 1, 30, 129, 77]         # n = L, n = 1, ragged
+    w = make_case(int(rng.integers(1 << 30)), len(lens), Hq, Hkv, D, B, torch.bfloat16, lens,
+                  chunks)
+    run_and_compare(w)
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_native_output(dtype):
+    w = make_case(7, 4, 32, 8, 128, 16, dtype, [40, 200, 513, 90], [40, 16, 100, 3])
+    run_and_compare(w, out_dtype=dtype)
+
+
+@pytest.mark.parametrize("part", [64, 128, 192, 0, -1])
+def test_forced_splits(part):
+    """Partition boundaries inside and at the edges of the causal diagonal."""
+    w = make_case(11, 3, 16, 2, 128, 16, torch.float16, [700, 130, 1025], [200, 130, 64])
+    run_and_compare(w, partition_size=part)
+
+
+def test_empty_chunks_and_short_contexts():
+    """Sequences with no new token own no rows; n = L = 1 is a single-token prefill."""
+    w = make_case(13, 5, 8, 2, 64, 16, torch.bfloat16, [1, 50, 9, 33, 2], [1, 0, 9, 0, 2])
+    got, ref = run_and_compare(w)
+    assert got.shape[0] == 12
+
+
+def test_single_token_chunks_match_decode():
+    """n = 1 for every sequence is decode: the chunk kernel agrees with pa_decode."""
+    w = workloads.make("llama13b_verify4", device="cuda", num_seqs=16, query_len=1)
+    # query_len 1 builds a decode workload; give it a query_start of one row each
+    qs = torch.arange(w.num_seqs + 1, dtype=torch.int32, device="cuda")
+    P.pa_reshape_and_cache(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping)
+    a = torch.empty(w.q.shape, dtype=torch.float32, device="cuda")
+    b = torch.empty_like(a)
+    P.pa_chunk_attention(a, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, qs,
+                         w.scale, w.num_kv_heads, w.block_size, max_query_len=1,
+                         max_context_len=w.max_context_len)
+    P.pa_decode(b, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale,
+                w.num_kv_heads, w.block_size, max_context_len=w.max_context_len)
+    torch.cuda.synchronize()
+    assert (a - b).abs().max().item() <= 2 * ATOL
+    assert P.pa_get_device_error() == 0
+
+
+def test_full_size_sampled_rows():
+    """The full 8 x 32768-token, 512-token chunk step at the launch configuration the
+    benchmark times; sampled rows are checked against the oracle one by one."""
+    w = workloads.make("long16_chunk512", device="cuda")
+    P.pa_reshape_and_cache(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping)
+    out = torch.empty(w.q.shape, dtype=torch.float32, device="cuda")
+    P.pa_chunk_attention(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                         w.query_start, w.scale, w.num_kv_heads, w.block_size,
+                         max_query_len=w.max_query_len, max_context_len=w.max_context_len)
+    torch.cuda.synchronize()
+    assert P.pa_get_device_error() == 0
+    rng = np.random.default_rng(5)
+    qs = w.query_start.cpu().tolist()
+    kc, vc = w.k_cache.cpu(), w.v_cache.cpu()
+    bt, cl = w.block_tables.cpu(), w.context_lens.cpu()
+    for s in rng.choice(w.num_seqs, size=2, replace=False).tolist():
+        for j in sorted(rng.choice(qs[s + 1] - qs[s], size=3, replace=False).tolist()) + [0]:
+            # one row as a one-sequence chunk of length j + 1 ending at its position
+            L = int(cl[s]) - (qs[s + 1] - qs[s]) + j + 1
+            ref = oracle.chunk_attention(w.q[qs[s] + j:qs[s] + j + 1].cpu(), kc, vc, bt[s:s + 1],
+                                         torch.tensor([L], dtype=torch.int32),
+                                         torch.tensor([0, 1], dtype=torch.int32), w.scale,
+                                         w.num_kv_heads, w.block_size,
+                                         num_threads=oracle.max_threads())
+            got = out[qs[s] + j].double().cpu().numpy()
+            err = np.abs(got - ref[0]).max()
+            assert err <= ATOL, (s, j, err)
+
+
+def test_chunk_longer_than_context_is_flagged():
+    """n > L is malformed: the kernel flags it and that sequence's rows are NaN."""
+    w = make_case(17, 3, 8, 8, 128, 16, torch.bfloat16, [30, 40, 50], [5, 6, 7])
+    P.pa_reshape_and_cache(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping)
+    bad_lens = w.context_lens.clone()
+    bad_lens[1] = 3                                   # 6 new tokens, context 3
+    out = torch.zeros(w.q.shape, dtype=torch.float32, device="cuda")
+    P.pa_chunk_attention(out, w.q, w.k_cache, w.v_cache, w.block_tables, bad_lens,
+                         w.query_start, w.scale, w.num_kv_heads, w.block_size,
+                         max_query_len=7, max_context_len=50)
+    torch.cuda.synchronize()
+    assert P.pa_get_device_error() & 0x2
+    assert torch.isnan(out[5:11]).all()
+    assert torch.isfinite(out[:5]).all() and torch.isfinite(out[11:]).all()
+
+
+def test_bad_block_id_is_flagged():
+    w = make_case(19, 2, 8, 2, 64, 16, torch.float16, [100, 80], [10, 20])
+    P.pa_reshape_and_cache(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping)
+    bt = w.block_tables.clone()
+    bt[0, 2] = w.num_blocks + 5
+    out = torch.zeros(w.q.shape, dtype=torch.float32, device="cuda")
+    P.pa_chunk_attention(out, w.q, w.k_cache, w.v_cache, bt, w.context_lens, w.query_start,
+                         w.scale, w.num_kv_heads, w.block_size, max_query_len=20,
+                         max_context_len=100)
+    torch.cuda.synchronize()
+    assert P.pa_get_device_error() & 0x1
+    assert torch.isnan(out[:10]).all()
+    assert torch.isfinite(out[10:]).all()
+
+
+def test_canaries_around_output():
+    w = make_case(23, 3, 16, 4, 128, 32, torch.bfloat16, [77, 150, 33], [20, 45, 33])
+    P.pa_reshape_and_cache(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping)
+    R, Hq, D = w.q.shape
+    buf = torch.full((R * Hq * D + 2 * 4096,), 12345.0, dtype=torch.float32, device="cuda")
+    out = buf[4096:4096 + R * Hq * D].view(R, Hq, D)
+    P.pa_chunk_attention(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                         w.query_start, w.scale, w.num_kv_heads, w.block_size,
+                         max_query_len=45, max_context_len=150, partition_size=64)
+    torch.cuda.synchronize()
+    assert (buf[:4096] == 12345.0).all() and (buf[-4096:] == 12345.0).all()
+    assert torch.isfinite(out).all()
+    assert P.pa_get_device_error() == 0
