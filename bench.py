@@ -48,6 +48,17 @@ WORKLOADS = {
 # model dtype; the step's cache write quantises)
 for _name in ("llama13b", "opt13b", "long16", "long32", "prefix"):
     WORKLOADS[_name + "_fp8"] = WORKLOADS[_name] + "; KV cache in FP8 E4M3 with per-head scales"
+# multi-token queries (pa_chunk_attention): the step writes every new token's K/V and
+# attends each new token causally over its sequence's cache
+WORKLOADS["llama13b_verify4"] = (
+    "speculative verification on the LLaMA-13B batch: 256 seqs, 4 new tokens each (1024 query "
+    "rows) attended causally, 40 q / 40 kv heads, head_dim 128, bf16, block_size 16, context "
+    "lognormal(median 400, sigma 0.8) in [16, 2048], N(0, 0.5)")
+WORKLOADS["long16_chunk512"] = (
+    "chunked prefill: 8 seqs x 32768-token contexts whose last 512 tokens are new (4096 query "
+    "rows), 64 q / 8 kv heads, head_dim 128, bf16, block_size 16, N(0, 1)")
+CHUNK_METRIC = {"llama13b_verify4": "paged verify attention KV GB/s",
+                "long16_chunk512": "paged chunk attention TFLOP/s"}
 DTYPE_NAME = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32",
               torch.float8_e4m3fn: "fp8_e4m3"}
 METRIC = "paged decode attention KV GB/s"
@@ -107,6 +118,18 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
+def load_tensor_peak():
+    """Dense bf16 tensor TFLOP/s: the sustained measurement (the chunk kernel is timed
+    inside a seconds-long loop of steps), else the recipe's fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops_sustained"]), "measured sustained"
+    except (OSError, KeyError, ValueError):
+        return 1700.0, "fallback sustained"
+
+
 def kernel_hash() -> str:
     h = hashlib.sha256()
     for name in ("decode_kernel.cuh", "decode_mma.cuh", "pa_device.cuh", "pa_internal.h"):
@@ -146,8 +169,25 @@ def algorithmic_bytes(w) -> dict:
     copies = 0
     if w.copy_pairs is not None:
         copies = 2 * 2 * len(w.copy_pairs) * w.num_kv_heads * w.block_size * w.head_dim * csz
+    if w.query_start is not None:                  # one q and out row per new token
+        qo = 2 * int(w.q.shape[0]) * w.num_q_heads * w.head_dim * esz + 4 * (w.num_seqs + 1)
     return {"kv": kv, "decode": kv + qo + tables, "reshape": reshape, "copy": copies,
             "step": kv + qo + tables + reshape + copies}
+
+
+def algorithmic_flops(w) -> int:
+    """Multiply-adds x 2 of the attention a step must do: q.k and p.v over every
+    (query row, head, visible token), 4 * head_dim flops each; chunk token j of a
+    sequence with n new tokens and context L sees L - n + j + 1 tokens."""
+    lens = w.context_lens.tolist()
+    if w.query_start is None:
+        return 4 * w.head_dim * w.num_q_heads * int(sum(lens))
+    qs = w.query_start.tolist()
+    total = 0
+    for s, L in enumerate(lens):
+        n = qs[s + 1] - qs[s]
+        total += n * (L - n) + n * (n + 1) // 2
+    return 4 * w.head_dim * w.num_q_heads * total
 
 
 class ClockSampler:
@@ -206,8 +246,31 @@ def make_workload(config: str, device, num_seqs=None):
     return workloads.make(config, device=device, **kw)
 
 
+def launched_split(pa, w) -> bool:
+    """Whether the library's automatic choice splits this workload (one more launch)."""
+    if w.query_start is not None:
+        return pa.pa_chunk_partition_tokens(w.dtype, w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                            w.head_dim, w.block_size, w.max_query_len,
+                                            w.max_context_len, 0) > 0
+    return pa.pa_decode_partition_tokens(w.q.dtype, w.k_cache.dtype, w.num_seqs, w.num_q_heads,
+                                         w.num_kv_heads, w.head_dim, w.block_size,
+                                         w.max_context_len, 0) > 0
+
+
 def step_ops(pa, w):
-    """(cache write, decode) callables of the library for this workload's cache type."""
+    """(cache write, decode) callables of the library for this workload's cache type
+    (for a chunk workload the attention call is pa_chunk_attention)."""
+    if w.query_start is not None:
+        def write(k, v, slots):
+            pa.pa_reshape_and_cache(k, v, w.k_cache, w.v_cache, slots)
+
+        def decode(out, q, bt, cl, part, ws, qs=None):
+            pa.pa_chunk_attention(out, q, w.k_cache, w.v_cache, bt, cl,
+                                  w.query_start if qs is None else qs, w.scale, w.num_kv_heads,
+                                  w.block_size, max_query_len=w.max_query_len,
+                                  max_context_len=w.max_context_len, partition_size=part,
+                                  workspace=ws)
+        return write, decode
     if w.fp8:
         ks, vs = w.meta["k_scale"], w.meta["v_scale"]
 
@@ -243,10 +306,16 @@ def run_ours(args, rank, world, local):
     w = make_workload(args.config, dev, args.num_seqs)
     part = 0 if args.partition_size is None else args.partition_size
     nbytes = algorithmic_bytes(w)
-    out = torch.empty(w.num_seqs, w.num_q_heads, w.head_dim, dtype=w.dtype, device=dev)
-    ws_bytes = pa.pa_decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.head_dim,
-                                            w.max_context_len, w.block_size, max(part, 0)) \
-        if part >= 0 else 0
+    chunk = w.query_start is not None
+    out = torch.empty(w.q.shape, dtype=w.dtype, device=dev)
+    if chunk:
+        ws_bytes = pa.pa_chunk_workspace_bytes(w.q.shape[0], w.num_q_heads, w.head_dim,
+                                               w.max_context_len, max(part, 0)) \
+            if part >= 0 else 0
+    else:
+        ws_bytes = pa.pa_decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.head_dim,
+                                                w.max_context_len, w.block_size, max(part, 0)) \
+            if part >= 0 else 0
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if args.flush_l2 else None
     cow_src = None
@@ -322,9 +391,36 @@ def run_ours(args, rank, world, local):
     peak, peak_kind = load_peaks()
     achieved = nbytes["decode"] / (decode_ms / 1e3) / 1e9
     split = part > 0 and w.max_context_len > part
+    if part == 0:
+        split = launched_split(pa, w)
     launches_per_step = 2 + (1 if split else 0) + (1 if cow_src is not None else 0)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": recorded_traffic(args.config),
+                "kernel": ("chunk_attn_kernel" if chunk else "decode_kernel")
+                + (" + reduce kernel" if split else ""),
+                "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "algorithmic_bytes_per_launch": nbytes["decode"]}
+    metric, unit = METRIC, "GB/s"
+    flops = algorithmic_flops(w)
+    tpeak, tpeak_kind = load_tensor_peak()
+    if chunk and flops / (tpeak * 1e12) > nbytes["decode"] / (peak * 1e9):
+        # bound by the tensor cores: a long chunk makes every K/V byte feed many rows
+        tflops = flops / (decode_ms / 1e3) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(tflops, 1), "peak": tpeak,
+                    "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
+                    "traffic": recorded_traffic(args.config),
+                    "kernel": roofline["kernel"],
+                    "peak_kind": f"{tpeak_kind} dense bf16 (MEASURED_PEAKS.json)",
+                    "algorithmic_flops_per_launch": flops,
+                    "algorithmic_bytes_per_launch": nbytes["decode"]}
+        value = flops * args.steps * world / sec / 1e12
+        metric, unit = CHUNK_METRIC[args.config], "TFLOP/s"
+    elif chunk:
+        metric = CHUNK_METRIC[args.config]
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[w.k_cache.dtype],
@@ -341,17 +437,17 @@ def run_ours(args, rank, world, local):
         "decode_us": round(decode_ms * 1e3, 2), "reshape_us": round(reshape_ms * 1e3, 2),
         "decode_kv_gbs": round(nbytes["kv"] / (decode_ms / 1e3) / 1e9, 1),
         "pct_of_hbm_peak": round(100 * achieved / peak, 1),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(args.config),
-                     "kernel": "decode_kernel" + (" + reduce_kernel" if split else ""),
-                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                     if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "algorithmic_bytes_per_launch": nbytes["decode"]},
+        "roofline": roofline,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
+    if chunk:
+        line["query_rows"] = int(w.q.shape[0])
+        line["attention_tflops"] = round(flops / (decode_ms / 1e3) / 1e12, 2)
     if e2e is not None:
+        if chunk and unit == "TFLOP/s":
+            e2e["value"] = round(flops / (e2e["ms_per_step"] / 1e3) / 1e12, 2)
+            e2e["unit"] = "TFLOP/s"
         line["e2e"] = e2e
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
@@ -363,6 +459,8 @@ def measure_e2e(args, pa, w, out, ws, part, dev):
     H2D of q, new K/V, slots, block tables and context lengths, the kernels, and a
     D2H read of the output, all inside the timed region."""
     names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+    if w.query_start is not None:
+        names = names + ("query_start",)
     host = {n: getattr(w, n).cpu().pin_memory() for n in names}
     devb = {n: torch.empty_like(getattr(w, n)) for n in names}
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -375,7 +473,11 @@ def measure_e2e(args, pa, w, out, ws, part, dev):
         for n in names:
             devb[n].copy_(host[n], non_blocking=True)
         write(devb["k_new"], devb["v_new"], devb["slot_mapping"])
-        decode(out, devb["q"], devb["block_tables"], devb["context_lens"], part, ws)
+        if w.query_start is not None:
+            decode(out, devb["q"], devb["block_tables"], devb["context_lens"], part, ws,
+                   devb["query_start"])
+        else:
+            decode(out, devb["q"], devb["block_tables"], devb["context_lens"], part, ws)
         out_host.copy_(out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 

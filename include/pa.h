@@ -265,6 +265,23 @@ int pa_chunk_attention(void* out, pa_dtype out_dtype, const void* q, const void*
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The partition length (tokens) a pa_decode / pa_decode_fp8 call, or a
+ * pa_chunk_attention call, with these arguments splits contexts into; 0 when it
+ * runs one pass per sequence (no merge launch).  partition_size as in those calls;
+ * the automatic choice (0) depends on the current device's SM count and the
+ * kernels' occupancy.  Returns a negative pa_status for invalid arguments, or
+ * PA_ERR_CUDA when the automatic choice cannot query the device.
+ */
+int32_t pa_decode_partition_tokens(pa_dtype q_dtype, pa_dtype kv_dtype, int32_t num_seqs,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t block_size, int32_t max_context_len,
+                                   int32_t partition_size);
+int32_t pa_chunk_partition_tokens(pa_dtype kv_dtype, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                  int32_t max_query_len, int32_t max_context_len,
+                                  int32_t partition_size);
+
+/*
  * Reads and clears the calling device's error word (PA_DEVERR_* bits).
  * Synchronises with `stream` to do so.  flags: host pointer.
  */

@@ -318,6 +318,34 @@ def pa_chunk_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor
     return out
 
 
+def pa_decode_partition_tokens(q_dtype: torch.dtype, kv_dtype: torch.dtype, num_seqs: int,
+                               num_q_heads: int, num_kv_heads: int, head_dim: int,
+                               block_size: int, max_context_len: int,
+                               partition_size: int = 0) -> int:
+    """The partition length pa_decode / pa_decode_fp8 would split contexts into
+    (0: one pass, no merge launch)."""
+    kv = N.PA_FP8_E4M3 if kv_dtype == torch.float8_e4m3fn else _DT[kv_dtype]
+    r = int(N.load().pa_decode_partition_tokens(_DT[q_dtype], kv, num_seqs, num_q_heads,
+                                                num_kv_heads, head_dim, block_size,
+                                                max_context_len, partition_size))
+    if r < 0:
+        N.check("pa_decode_partition_tokens", r)
+    return r
+
+
+def pa_chunk_partition_tokens(kv_dtype: torch.dtype, num_seqs: int, num_q_heads: int,
+                              num_kv_heads: int, head_dim: int, block_size: int,
+                              max_query_len: int, max_context_len: int,
+                              partition_size: int = 0) -> int:
+    """The partition length pa_chunk_attention would split contexts into (0: one pass)."""
+    r = int(N.load().pa_chunk_partition_tokens(_DT[kv_dtype], num_seqs, num_q_heads,
+                                               num_kv_heads, head_dim, block_size,
+                                               max_query_len, max_context_len, partition_size))
+    if r < 0:
+        N.check("pa_chunk_partition_tokens", r)
+    return r
+
+
 def pa_get_device_error(stream=None) -> int:
     """Read and clear the device error word (PA_DEVERR_* bits).  Synchronises."""
     flags = ctypes.c_uint32(0)

@@ -261,6 +261,38 @@ size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t 
 
 namespace {
 
+// The partition length pa_decode uses for these arguments (0: one pass).
+int decode_partition(pa_dtype q_dtype, pa_dtype kv_dtype, int num_seqs, int num_kv_heads,
+                     int group, int head_dim, int block_size, int max_context_len,
+                     int partition_size)
+{
+    const int gc = heads_per_cta(group);
+    int occ = 0;
+    if (partition_size == 0) {
+        switch (kv_dtype) {
+        case PA_F32: occ = occupancy_decode_f32(head_dim, block_size, gc); break;
+        case PA_F16: occ = occupancy_decode_f16(head_dim, block_size, gc); break;
+        case PA_BF16: occ = occupancy_decode_bf16(head_dim, block_size, gc); break;
+        case PA_FP8_E4M3: occ = occupancy_decode_fp8(q_dtype, head_dim, block_size, gc); break;
+        }
+    }
+    return choose_partition(partition_size, max_context_len,
+                            (int64_t)num_seqs * num_kv_heads * (group / gc),
+                            (int64_t)device_sm_count() * occ, block_size);
+}
+
+// The partition length pa_chunk_attention uses for these arguments (0: one pass).
+int chunk_partition(pa_dtype kv_dtype, int num_seqs, int num_kv_heads, int m_tiles,
+                    int head_dim, int block_size, int max_context_len, int partition_size)
+{
+    int occ = 0;
+    if (partition_size == 0)
+        occ = occupancy_chunk_attention(kv_dtype, head_dim, block_size);
+    return choose_chunk_partition(partition_size, max_context_len,
+                                  (int64_t)num_seqs * num_kv_heads * m_tiles,
+                                  (int64_t)device_sm_count() * occ);
+}
+
 // Shared body of pa_decode and pa_decode_fp8.  q_dtype is the type of q (and of a
 // native out); kv_dtype the cache's, PA_FP8_E4M3 with k_scale / v_scale.
 int decode_impl(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
@@ -308,19 +340,8 @@ int decode_impl(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
         overlaps(out, out_bytes, v_cache, pool_bytes))
         return PA_ERR_INVALID;
 
-    const int sms = device_sm_count();
-    int occ = 0;
-    if (partition_size == 0) {
-        switch (kv_dtype) {
-        case PA_F32: occ = occupancy_decode_f32(head_dim, block_size, gc); break;
-        case PA_F16: occ = occupancy_decode_f16(head_dim, block_size, gc); break;
-        case PA_BF16: occ = occupancy_decode_bf16(head_dim, block_size, gc); break;
-        case PA_FP8_E4M3: occ = occupancy_decode_fp8(q_dtype, head_dim, block_size, gc); break;
-        }
-    }
-    const int P = choose_partition(partition_size, max_context_len,
-                                   (int64_t)num_seqs * num_kv_heads * chunks,
-                                   (int64_t)sms * occ, block_size);
+    const int P = decode_partition(q_dtype, kv_dtype, num_seqs, num_kv_heads, group, head_dim,
+                                   block_size, max_context_len, partition_size);
     DecodeParams p{};
     p.out = out;
     p.q = q;
@@ -405,6 +426,41 @@ int pa_decode_fp8(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype
                        block_size, scale, partition_size, workspace, workspace_bytes, stream);
 }
 
+int32_t pa_decode_partition_tokens(pa_dtype q_dtype, pa_dtype kv_dtype, int32_t num_seqs,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t block_size, int32_t max_context_len,
+                                   int32_t partition_size)
+{
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        num_q_heads % num_kv_heads != 0 || max_context_len < 0 || block_size <= 0)
+        return PA_ERR_INVALID;
+    if (partition_size > 0 && partition_size % block_size != 0)
+        return PA_ERR_INVALID;
+    if (partition_size == 0 && device_sm_count() <= 0)
+        return PA_ERR_CUDA;
+    return decode_partition(q_dtype, kv_dtype, num_seqs, num_kv_heads, num_q_heads / num_kv_heads,
+                            head_dim, block_size, max_context_len, partition_size);
+}
+
+int32_t pa_chunk_partition_tokens(pa_dtype kv_dtype, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                  int32_t max_query_len, int32_t max_context_len,
+                                  int32_t partition_size)
+{
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > 128 ||
+        max_context_len < 0 || max_query_len < 0)
+        return PA_ERR_INVALID;
+    if (partition_size > 0 && partition_size % 64 != 0)
+        return PA_ERR_INVALID;
+    if (partition_size == 0 && device_sm_count() <= 0)
+        return PA_ERR_CUDA;
+    const int rows_tokens = 128 / (num_q_heads / num_kv_heads);
+    const int m_tiles = (max_query_len + rows_tokens - 1) / rows_tokens;
+    return chunk_partition(kv_dtype, num_seqs, num_kv_heads, m_tiles, head_dim, block_size,
+                           max_context_len, partition_size);
+}
+
 size_t pa_chunk_workspace_bytes(int64_t num_query_tokens, int32_t num_q_heads, int32_t head_dim,
                                 int32_t max_context_len, int32_t partition_size)
 {
@@ -465,12 +521,8 @@ int pa_chunk_attention(void* out, pa_dtype out_dtype, const void* q, const void*
         overlaps(out, out_bytes, v_cache, pool_bytes))
         return PA_ERR_INVALID;
 
-    int occ = 0;
-    if (partition_size == 0)
-        occ = occupancy_chunk_attention(kv_dtype, head_dim, block_size);
-    const int P = choose_chunk_partition(partition_size, max_context_len,
-                                         (int64_t)num_seqs * num_kv_heads * m_tiles,
-                                         (int64_t)device_sm_count() * occ);
+    const int P = chunk_partition(kv_dtype, num_seqs, num_kv_heads, m_tiles, head_dim,
+                                  block_size, max_context_len, partition_size);
     ChunkParams p{};
     p.out = out;
     p.q = q;

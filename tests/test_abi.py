@@ -203,3 +203,19 @@ def test_chunk_workspace_bytes(lib):
     assert lib.pa_chunk_workspace_bytes(100, 64, 128, 512, 512) == 0
     assert lib.pa_chunk_workspace_bytes(100, 64, 128, 4096, 0) > 0
     assert lib.pa_chunk_workspace_bytes(-1, 64, 128, 4096, 0) == 0
+
+
+def test_partition_queries_for_explicit_sizes(lib):
+    """An explicit partition size needs no device query: the call splits exactly when
+    the longest context exceeds it."""
+    assert lib.pa_decode_partition_tokens(N.PA_BF16, N.PA_BF16, 8, 64, 8, 128, 16, 4096, 512) \
+        == 512
+    assert lib.pa_decode_partition_tokens(N.PA_BF16, N.PA_BF16, 8, 64, 8, 128, 16, 512, 512) == 0
+    assert lib.pa_decode_partition_tokens(N.PA_BF16, N.PA_BF16, 8, 64, 8, 128, 16, 4096, -1) == 0
+    assert lib.pa_decode_partition_tokens(N.PA_BF16, N.PA_BF16, 8, 64, 8, 128, 16, 4096, 24) \
+        == N.PA_ERR_INVALID
+    assert lib.pa_chunk_partition_tokens(N.PA_BF16, 8, 64, 8, 128, 16, 512, 32768, 1024) == 1024
+    assert lib.pa_chunk_partition_tokens(N.PA_BF16, 8, 64, 8, 128, 16, 512, 32768, 1000) \
+        == N.PA_ERR_INVALID
+    assert lib.pa_chunk_partition_tokens(N.PA_BF16, 8, 6, 4, 128, 16, 512, 32768, 0) \
+        == N.PA_ERR_INVALID
