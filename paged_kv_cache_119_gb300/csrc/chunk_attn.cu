@@ -6,7 +6,7 @@ namespace pa {
 
 template <typename T, int D, int BS>
 struct ChunkVariant {
-    static constexpr int kStages = 3;
+    static constexpr int kStages = ChunkStages<D>::value;
     using Sm = ChunkSmem<D, kStages>;
     static constexpr auto kernel() { return chunk_attn_kernel<T, D, BS, kStages>; }
     static cudaError_t configure()

@@ -9,24 +9,27 @@
 // the softmax attention of section "背景" over that prefix, read through the
 // block table.
 //
-// Organisation.  A CTA owns up to 128 (query token, query head) rows that share a
-// kv head: TT = 128 / G consecutive chunk tokens x the G heads of the group, row
-// r = token * G + head.  K and V are streamed through the block table in tiles of
-// 64 tokens; both products are dense 128-row contractions:
-//   S[128 x 64]  = Q[128 x D] . K_tile^T      (tcgen05.mma kind::f16, fp32 in TMEM)
-//   O[128 x D]  += P[128 x 64] . V_tile        (P = hi + lo halves of the 16-bit type)
+// Organisation.  A CTA owns 256 (query token, query head) rows that share a kv
+// head -- TT = 256 / G consecutive chunk tokens x the G heads of the group, row
+// r = token * G + head -- as two 128-row query tiles.  K and V stream through the
+// block table in tiles of 64 tokens, each tile serving both query tiles:
+//   S_q[128 x 64]  = Q_q[128 x D] . K^T      (tcgen05.mma kind::f16, fp32 in TMEM)
+//   O_q[128 x D]  += P_q[128 x 64] . V        (P = hi + lo halves of the 16-bit type)
 //   * warp 0 (producer): block-table entries and tensor-map TMA of the tile's K
 //     and V boxes (64 dims x B tokens, 128-byte swizzle) into an mbarrier ring;
-//   * warp 1: allocates tensor memory and (one thread) issues the MMAs: S of the
-//     next tile is issued before P.V of the current one, into a second S buffer,
-//     so the tensor core works while the softmax warps read scores;
-//   * warps 2-5 (one thread per row = TMEM lane): read S, mask (causal within the
-//     chunk, end of context), online softmax in base 2, write P to shared memory
-//     in the operand layout, and keep O in tensor memory up to date.
+//   * warp 1: allocates all 512 tensor-memory columns and (one thread) issues the
+//     MMAs: the scores of the next tile for both query tiles go out before P.V of
+//     the current one, into second S buffers, so the tensor core keeps busy while
+//     the softmax warps work;
+//   * warps 2-5 (query tile 0) and 6-9 (query tile 1), one thread per row = TMEM
+//     lane: read S, mask (causal within the chunk, end of context), online softmax
+//     in base 2, write P to shared memory in the operand layout, keep O up to date.
+// Two softmax warps per SM sub-partition hide each other's latency; the MUFU work
+// (one exp2 per score) stays below the tensor-core time of a tile.
 // Rescaling O is lazy: a row's reference maximum moves only when a tile's maximum
-// exceeds it by more than 2^8 in probability, so p = 2^(x - m_ref) <= 256 and
-// most tiles need no tensor-memory round trip.  The result O / l is exact for any
-// reference, as O and l share it.
+// exceeds it by more than 2^8 in probability, so p = 2^(x - m_ref) <= 256 and most
+// tiles need no tensor-memory round trip.  O / l is exact for any reference, as O
+// and l share it.
 // P is split into hi = rn(p) and lo = rn(p - hi) of the 16-bit operand type
 // (p = hi + lo to ~2^-17 relative) and both halves are multiplied with V, so the
 // probabilities keep fp32-level accuracy (one 8-bit-mantissa rounding of p would
@@ -43,34 +46,53 @@
 
 namespace pa {
 
+constexpr int kChunkQTiles = 2;      // 128-row query tiles per CTA
 constexpr int kChunkRows = 128;      // M of the tensor-core tile
 constexpr int kChunkTileTok = 64;    // tokens per K/V tile (N of the score product)
-constexpr int kChunkThreads = 192;   // producer, MMA, four softmax warps
+constexpr int kChunkSoftmaxWarps = 4 * kChunkQTiles;
+constexpr int kChunkThreads = 64 + 32 * kChunkSoftmaxWarps;   // producer, MMA, softmax
 
 template <int D, int NST>
 struct ChunkSmem {
     static constexpr int kHalves = D / 64;                       // 128-byte column groups
     static constexpr int kQHalf = kChunkRows * 128;              // 16 KB
-    static constexpr int kQBytes = kHalves * kQHalf;
+    static constexpr int kQTile = kHalves * kQHalf;              // one 128-row query tile
     static constexpr int kPBytes = kChunkRows * 128;             // 128 rows x 64 tokens x 2 B
     static constexpr int kKVHalf = kChunkTileTok * 128;          // 8 KB
     static constexpr int kKBytes = kHalves * kKVHalf;
     static constexpr int kStageBytes = 2 * kKBytes;              // K then V
     static constexpr int kQOff = 0;
-    static constexpr int kPOff = kQOff + kQBytes;                // [buffer 2][hi, lo][kPBytes]
-    static constexpr int kStageOff = kPOff + 4 * kPBytes;
+    static constexpr int kPOff = kQOff + kChunkQTiles * kQTile;  // [query tile][hi, lo]
+    static constexpr int kStageOff = kPOff + kChunkQTiles * 2 * kPBytes;
     static constexpr int kBarOff = kStageOff + NST * kStageBytes;
-    // full[NST], empty[NST], s_full[2], s_free[2], p_full[2], pv_done[2], q_full, mma_done
-    static constexpr int kNumBars = 2 * NST + 10;
+    // full[NST], empty[NST], s_full[2][2], s_free[2][2], p_full[2], pv_done[2],
+    // q_full, mma_done
+    static constexpr int kNumBars = 2 * NST + 14;
     static constexpr int kOkOff = kBarOff + 8 * kNumBars;        // stage_ok[NST]
     static constexpr int kSlotOff = kOkOff + 4 * NST;            // TMEM address
     static constexpr int kBytes = kSlotOff + 16;
     static constexpr int kAlloc = kBytes + 1024;                 // 1 KB alignment slack
-    static constexpr int kTmemCols = 256;                        // O at 0, S buffers at 128, 192
-    static constexpr int kSCol = 128;
-    static_assert(D <= 128, "O must fit below the S buffers");
+    // tensor memory: O of query tile q at column 128 q, its two S buffers at
+    // 256 + 128 q and 256 + 128 q + 64
+    static constexpr int kTmemCols = 512;
+    static constexpr int kSCol = 256;
+    static_assert(D <= 128, "O must fit in 128 columns");
     static_assert(kAlloc <= 227 * 1024, "shared memory");
 };
+
+// Stages of the K/V ring: as many as fit next to the query tiles and P buffers.
+template <int D>
+struct ChunkStages {
+    static constexpr int value = D == 128 ? 3 : 5;
+};
+
+// 2^x on the MUFU unit (relative error far below the 2^-17 of the P split).
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // Stores 32 consecutive outputs v[i] * mul (NaN when nan_out) at base + idx as
 // fp32 (which = 0), f16 (1) or bf16 (2); idx is a multiple of 32.
@@ -106,28 +128,31 @@ __device__ __forceinline__ void store_row32(void* base, int64_t idx, const float
         dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
 }
 
+// (p0, p1) -> hi = rn(p0, p1) and lo = rn(p - hi) in the 16-bit type T, packed.
 template <typename T>
-__device__ __forceinline__ uint32_t pack2(float a, float b)
+__device__ __forceinline__ void split_pair(float p0, float p1, uint32_t& hi, uint32_t& lo)
 {
+    float2 h;
     if constexpr (DType<T>::id == PA_F16) {
-        __half2 h = __floats2half2_rn(a, b);
-        return *reinterpret_cast<uint32_t*>(&h);
+        __half2 v = __floats2half2_rn(p0, p1);
+        hi = *reinterpret_cast<uint32_t*>(&v);
+        h = __half22float2(v);
     } else {
-        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-        return *reinterpret_cast<uint32_t*>(&h);
+        __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
+        hi = *reinterpret_cast<uint32_t*>(&v);
+        h = make_float2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u));
+    }
+    const float2 r = ffma2(h, make_float2(-1.f, -1.f), make_float2(p0, p1));   // p - hi, exact
+    if constexpr (DType<T>::id == PA_F16) {
+        __half2 v = __floats2half2_rn(r.x, r.y);
+        lo = *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __nv_bfloat162 v = __floats2bfloat162_rn(r.x, r.y);
+        lo = *reinterpret_cast<uint32_t*>(&v);
     }
 }
 
-template <typename T>
-__device__ __forceinline__ float2 unpack2(uint32_t w)
-{
-    if constexpr (DType<T>::id == PA_F16)
-        return __half22float2(*reinterpret_cast<__half2*>(&w));
-    else
-        return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w));
-}
-
-// grid = (partitions, num_kv_heads * m_tiles, num_seqs); 192 threads.
+// grid = (partitions, num_kv_heads * m_tiles, num_seqs); kChunkThreads threads.
 template <typename T, int D, int BS, int NST>
 __global__ void __launch_bounds__(kChunkThreads, 1)
     chunk_attn_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ CUtensorMap tk,
@@ -145,9 +170,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sm::kBarOff);
     uint64_t* empty = full + NST;
-    uint64_t* s_full = empty + NST;
-    uint64_t* s_free = s_full + 2;
-    uint64_t* p_full = s_free + 2;
+    uint64_t* s_full = empty + NST;              // [query tile][S buffer]
+    uint64_t* s_free = s_full + 4;
+    uint64_t* p_full = s_free + 4;               // [query tile]
     uint64_t* pv_done = p_full + 2;
     uint64_t* q_full = pv_done + 2;
     uint64_t* mma_done = q_full + 1;
@@ -187,11 +212,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         }
         return;
     }
-    if (seq == p.num_seqs - 1 && part == 0 && blockIdx.y == 0 && (int64_t)qs1 != p.num_rows) {
-        // rows after the last sequence's chunk are owned by nobody
-        if (threadIdx.x == 0)
-            atomicOr(p.err, PA_DEVERR_CONTEXT_LEN);
-    }
+    if (seq == p.num_seqs - 1 && part == 0 && blockIdx.y == 0 && threadIdx.x == 0 &&
+        (int64_t)qs1 != p.num_rows)
+        atomicOr(p.err, PA_DEVERR_CONTEXT_LEN);   // rows after the last chunk belong to no one
     const int j0 = mt * TT;
     if (j0 >= n)
         return;                                  // no chunk token in this row tile
@@ -214,13 +237,16 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             mbar_init(&empty[s], 1);
         }
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&s_full[b], 1);
-            mbar_init(&s_free[b], 4);
-            mbar_init(&p_full[b], 4);
-            mbar_init(&pv_done[b], 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_free[i], 4);
         }
-        mbar_init(q_full, 4);
+#pragma unroll
+        for (int q = 0; q < kChunkQTiles; ++q) {
+            mbar_init(&p_full[q], 4);
+            mbar_init(&pv_done[q], 1);
+        }
+        mbar_init(q_full, kChunkSoftmaxWarps);
         mbar_init(mma_done, 1);
         fence_mbar_init();
     }
@@ -293,16 +319,22 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             const uint32_t idesc_s = mma_idesc_f16(kBf16, kChunkRows, NT, false);
             const uint32_t idesc_o = mma_idesc_f16(kBf16, kChunkRows, D, true);
             bool ok = mbar_wait(q_full, 0);
+            // S_q of tile it for both query tiles, into S buffer it & 1
             auto issue_scores = [&](int it) {
                 const uint32_t kb = smem_addr(smem + Sm::kStageOff + (it % NST) * Sm::kStageBytes);
-                const uint32_t dcol = tbase + Sm::kSCol + (it & 1) * NT;
 #pragma unroll
-                for (int kk = 0; kk < KS; ++kk) {
-                    const uint64_t a = sw128_desc(sq + (kk / 4) * Sm::kQHalf + (kk % 4) * 32, 16, 1024);
-                    const uint64_t b = sw128_desc(kb + (kk / 4) * Sm::kKVHalf + (kk % 4) * 32, 16, 1024);
-                    tc_mma_f16(dcol, a, b, idesc_s, kk > 0 ? 1u : 0u);
+                for (int q = 0; q < kChunkQTiles; ++q) {
+                    const uint32_t dcol = tbase + Sm::kSCol + q * 128 + (it & 1) * NT;
+#pragma unroll
+                    for (int kk = 0; kk < KS; ++kk) {
+                        const uint64_t a = sw128_desc(
+                            sq + q * Sm::kQTile + (kk / 4) * Sm::kQHalf + (kk % 4) * 32, 16, 1024);
+                        const uint64_t b =
+                            sw128_desc(kb + (kk / 4) * Sm::kKVHalf + (kk % 4) * 32, 16, 1024);
+                        tc_mma_f16(dcol, a, b, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(&s_full[q * 2 + (it & 1)]);
                 }
-                tc_commit(&s_full[it & 1]);
             };
             if (ok)
                 ok = mbar_wait(&full[0], 0);
@@ -313,30 +345,36 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             for (int it = 0; it < ntiles && ok; ++it) {
                 if (it + 1 < ntiles) {
                     ok = mbar_wait(&full[(it + 1) % NST], ((it + 1) / NST) & 1);
-                    if (ok && it >= 1)        // S buffer (it+1)&1 was read by the softmax of tile it-1
-                        ok = mbar_wait(&s_free[(it + 1) & 1], ((it - 1) >> 1) & 1);
+                    // S buffers (it+1)&1 were read by the softmax of tile it-1
+                    for (int q = 0; q < kChunkQTiles && ok && it >= 1; ++q)
+                        ok = mbar_wait(&s_free[q * 2 + ((it + 1) & 1)], ((it - 1) >> 1) & 1);
                     if (!ok)
                         break;
                     tc_fence_after();
                     issue_scores(it + 1);
                 }
-                ok = mbar_wait(&p_full[it & 1], (it >> 1) & 1);
-                if (!ok)
-                    break;
-                tc_fence_after();
                 const uint32_t vb =
                     smem_addr(smem + Sm::kStageOff + (it % NST) * Sm::kStageBytes + Sm::kKBytes);
-                const uint32_t pb = smem_addr(smem + Sm::kPOff + (it & 1) * 2 * Sm::kPBytes);
+#pragma unroll 1
+                for (int q = 0; q < kChunkQTiles && ok; ++q) {
+                    ok = mbar_wait(&p_full[q], it & 1);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    const uint32_t pb = smem_addr(smem + Sm::kPOff + q * 2 * Sm::kPBytes);
 #pragma unroll
-                for (int half = 0; half < 2; ++half)          // hi, then lo
+                    for (int half = 0; half < 2; ++half)          // hi, then lo
 #pragma unroll
-                    for (int kk = 0; kk < NT / 16; ++kk) {
-                        const uint64_t a = sw128_desc(pb + half * Sm::kPBytes + kk * 32, 16, 1024);
-                        const uint64_t b = sw128_desc(vb + kk * 16 * 128, Sm::kKVHalf, 1024);
-                        tc_mma_f16(tbase, a, b, idesc_o, (it > 0 || half > 0 || kk > 0) ? 1u : 0u);
-                    }
-                tc_commit(&empty[it % NST]);
-                tc_commit(&pv_done[it & 1]);
+                        for (int kk = 0; kk < NT / 16; ++kk) {
+                            const uint64_t a = sw128_desc(pb + half * Sm::kPBytes + kk * 32, 16, 1024);
+                            const uint64_t b = sw128_desc(vb + kk * 16 * 128, Sm::kKVHalf, 1024);
+                            tc_mma_f16(tbase + q * 128, a, b, idesc_o,
+                                       (it > 0 || half > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    tc_commit(&pv_done[q]);
+                }
+                if (ok)
+                    tc_commit(&empty[it % NST]);
             }
             if (!ok)
                 atomicOr(p.err, PA_DEVERR_TIMEOUT);
@@ -346,22 +384,37 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax warps
+        const int q = (warp - 2) >> 2;                   // query tile of this warp
         const int wq = warp & 3;                         // TMEM lane quarter of this warp
-        const int r = 32 * wq + lane;                    // tile row = TMEM lane
+        const int rr = 32 * wq + lane;                   // row within the query tile = TMEM lane
+        const int r = q * kChunkRows + rr;               // row within the CTA
         const int tok = r / G;
         const int g = r - tok * G;
         const bool row_valid = tok < ntok;               // (r >= TT * G gives tok >= TT)
         const int pos = pos_first + tok;
         const int64_t qrow = (int64_t)(qs0 + j0 + tok) * p.num_q_heads + (int64_t)kvh * G + g;
+        // scores are used as s * sl2 with sl2 > 0: a negative scale flips the sign of q
+        // (exact), a zero scale makes q zero (every score 0)
+        const float sl2_raw = p.scale_log2;
+        const uint32_t qflip = sl2_raw < 0.f ? 0x80008000u : 0u;
+        const bool qzero = sl2_raw == 0.f;
+        const float sl2 = qzero ? 1.f : fabsf(sl2_raw);
         {
             // Q rows into the 128-byte-swizzled operand layout; rows past the chunk are 0
             const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
                                                               (row_valid ? qrow : 0) * D);
+            unsigned char* qdst = smem + Sm::kQOff + q * Sm::kQTile + rr * 128;
 #pragma unroll
             for (int c = 0; c < D / 8; ++c) {
-                const uint4 v = row_valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(smem + Sm::kQOff + (c / 8) * Sm::kQHalf + r * 128 +
-                                          (((c & 7) ^ (r & 7)) << 4)) = v;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (row_valid && !qzero) {
+                    v = __ldg(src + c);
+                    v.x ^= qflip;
+                    v.y ^= qflip;
+                    v.z ^= qflip;
+                    v.w ^= qflip;
+                }
+                *reinterpret_cast<uint4*>(qdst + (c / 8) * Sm::kQHalf + (((c & 7) ^ (rr & 7)) << 4)) = v;
             }
         }
         fence_proxy_async_smem();
@@ -371,14 +424,15 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
 
         const bool warp_live = __any_sync(kFullMask, row_valid);
         const uint32_t lane_t = tbase + ((uint32_t)(32 * wq) << 16);
-        const float sl2 = p.scale_log2;
+        const uint32_t o_col = lane_t + q * 128;
         float m_ref = -INFINITY, lsum = 0.f;
         bool poisoned = false;
+        unsigned char* prow = smem + Sm::kPOff + q * 2 * Sm::kPBytes + rr * 128;
         for (int it = 0; it < ntiles; ++it) {
             const int b = it & 1;
             const int st = it % NST;
             const int tb = t0 + it * NT;
-            bool ok = mbar_wait(&s_full[b], (it >> 1) & 1);
+            bool ok = mbar_wait(&s_full[q * 2 + b], (it >> 1) & 1);
             ok = ok && mbar_wait(&full[st], (it / NST) & 1);   // stage_ok and the tile's bytes
             if (!ok) {
                 if (lane == 0)
@@ -391,88 +445,106 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             tc_fence_after();
             float s[NT];
             if (warp_live) {
-                tmem_ld32(lane_t + Sm::kSCol + b * NT, *reinterpret_cast<float(*)[32]>(&s[0]));
-                tmem_ld32(lane_t + Sm::kSCol + b * NT + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
+                tmem_ld32(lane_t + Sm::kSCol + q * 128 + b * NT, *reinterpret_cast<float(*)[32]>(&s[0]));
+                tmem_ld32(lane_t + Sm::kSCol + q * 128 + b * NT + 32,
+                          *reinterpret_cast<float(*)[32]>(&s[32]));
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&s_free[b]);
+                mbar_arrive(&s_free[q * 2 + b]);
 
-            uint32_t hi[NT / 2], lo[NT / 2];
+            bool waited = false;
             if (warp_live) {
                 const int lim = row_valid ? pos - tb : -1;   // columns c <= lim are visible
-                float tmax = -INFINITY;
+                if (lim < NT - 1) {
 #pragma unroll
-                for (int c = 0; c < NT; ++c) {
-                    s[c] = c <= lim ? s[c] * sl2 : -INFINITY;
-                    tmax = fmaxf(tmax, s[c]);
+                    for (int c = 0; c < NT; ++c)
+                        s[c] = c <= lim ? s[c] : -INFINITY;
                 }
+                float mx[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    mx[i] = s[i];
+#pragma unroll
+                for (int c = 8; c < NT; ++c)
+                    mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+                const float smax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                const float tmax = smax == -INFINITY ? -INFINITY : smax * sl2;
                 const bool need = tmax > m_ref + 8.f;
-                if (__any_sync(kFullMask, need && it > 0)) {
+                if (it > 0 && __any_sync(kFullMask, need)) {
                     // O holds P.V of tiles 0 .. it-1: wait for the last, then rescale the
                     // rows whose reference maximum moves
-                    if (!mbar_wait(&pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1)) {
+                    if (!mbar_wait(&pv_done[q], (it - 1) & 1)) {
                         if (lane == 0)
                             atomicOr(p.err, PA_DEVERR_TIMEOUT);
                         poisoned = true;
                     }
+                    waited = true;
                     tc_fence_after();
-                    const float alpha = need ? exp2f(m_ref - tmax) : 1.f;
+                    const float alpha = need ? ex2_approx(m_ref - tmax) : 1.f;
 #pragma unroll 1
                     for (int c4 = 0; c4 < D / 32; ++c4) {
                         float o[32];
-                        tmem_ld32(lane_t + 32 * c4, o);
+                        tmem_ld32(o_col + 32 * c4, o);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            o[i] *= alpha;
-                        tmem_st32(lane_t + 32 * c4, o);
+                        for (int i = 0; i < 32; i += 2) {
+                            const float2 v = fmul2(make_float2(o[i], o[i + 1]), make_float2(alpha, alpha));
+                            o[i] = v.x;
+                            o[i + 1] = v.y;
+                        }
+                        tmem_st32(o_col + 32 * c4, o);
                     }
                 }
                 if (need) {
-                    lsum *= exp2f(m_ref - tmax);
+                    lsum *= ex2_approx(m_ref - tmax);
                     m_ref = tmax;
                 }
-                float rs = 0.f;
-                const bool any = m_ref != -INFINITY;
+                // p = 2^(s * sl2 - m_ref), in place; 0 where masked (s = -inf) or no reference
+                const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
+                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
                 for (int c = 0; c < NT; c += 2) {
-                    const float p0 = any ? exp2f(s[c] - m_ref) : 0.f;
-                    const float p1 = any ? exp2f(s[c + 1] - m_ref) : 0.f;
-                    rs += p0 + p1;
-                    const uint32_t h2 = pack2<T>(p0, p1);
-                    const float2 hf = unpack2<T>(h2);
-                    hi[c / 2] = h2;
-                    lo[c / 2] = pack2<T>(p0 - hf.x, p1 - hf.y);
+                    const float2 x = ffma2(make_float2(s[c], s[c + 1]), make_float2(sl2, sl2),
+                                           make_float2(nm, nm));
+                    s[c] = ex2_approx(x.x);
+                    s[c + 1] = ex2_approx(x.y);
+                    acc[(c >> 1) & 3] = ffma2(make_float2(s[c], s[c + 1]), make_float2(1.f, 1.f),
+                                              acc[(c >> 1) & 3]);
                 }
-                lsum += rs;
+                lsum += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
+                        ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
             }
-            // P buffer b was last read by P.V of tile it-2
-            if (it >= 2 && !mbar_wait(&pv_done[b], ((it - 2) >> 1) & 1)) {
+            // the P buffer of this query tile was last read by P.V of tile it-1
+            if (it > 0 && !waited && !mbar_wait(&pv_done[q], (it - 1) & 1)) {
                 if (lane == 0)
                     atomicOr(p.err, PA_DEVERR_TIMEOUT);
                 poisoned = true;
                 break;
             }
             if (warp_live) {
-                unsigned char* ph = smem + Sm::kPOff + b * 2 * Sm::kPBytes + r * 128;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    const int off = (c ^ (r & 7)) << 4;
-                    *reinterpret_cast<uint4*>(ph + off) =
-                        make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
-                    *reinterpret_cast<uint4*>(ph + Sm::kPBytes + off) =
-                        make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        split_pair<T>(s[8 * c + 2 * k], s[8 * c + 2 * k + 1], hi[k], lo[k]);
+                    const int off = (c ^ (rr & 7)) << 4;
+                    *reinterpret_cast<uint4*>(prow + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(prow + Sm::kPBytes + off) =
+                        make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
             }
-            if (tb + NT > t1) {
+            if (q == 0 && tb + NT > t1) {
                 // V rows past the range may hold anything (unused slots, stale tiles):
-                // zero them so that 0 * V stays 0
+                // zero them so that 0 * V stays 0.  Query tile 0's warps do it before
+                // their P is published; P.V of tile 1 is issued after that of tile 0.
                 const int v0 = t1 - tb;
                 const int rows = NT - v0;
                 unsigned char* vbase = smem + Sm::kStageOff + st * Sm::kStageBytes + Sm::kKBytes;
-                const int tid = threadIdx.x - 64;
-                for (int idx = tid; idx < Sm::kHalves * rows * 8; idx += 128) {
+                for (int idx = rr; idx < Sm::kHalves * rows * 8; idx += kChunkRows) {
                     const int h = idx / (rows * 8);
                     const int w = idx - h * rows * 8;
                     *reinterpret_cast<uint4*>(vbase + h * Sm::kKVHalf + (v0 + w / 8) * 128 +
@@ -483,11 +555,11 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&p_full[b]);
+                mbar_arrive(&p_full[q]);
         }
 
         // ---------------------------------------------------------------- epilogue
-        if (!mbar_wait(&pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) {
+        if (!mbar_wait(&pv_done[q], (ntiles - 1) & 1)) {
             if (lane == 0)
                 atomicOr(p.err, PA_DEVERR_TIMEOUT);
             poisoned = true;
@@ -495,19 +567,19 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         tc_fence_after();
         if (warp_live) {
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-            const int which = split || p.out_f32 ? 0 : (DType<T>::id == PA_F16 ? 1 : 2);
+            const int which = (split || p.out_f32) ? 0 : (DType<T>::id == PA_F16 ? 1 : 2);
 #pragma unroll 1
             for (int c4 = 0; c4 < D / 32; ++c4) {
                 float o[32];
-                tmem_ld32(lane_t + 32 * c4, o);
+                tmem_ld32(o_col + 32 * c4, o);
                 if (!row_valid)
                     continue;
                 if (split) {
-                    const int64_t prow = qrow * p.max_parts + part;
-                    store_row32(p.part_o, prow * D + 32 * c4, o, inv, poisoned, 0);
+                    const int64_t prw = qrow * p.max_parts + part;
+                    store_row32(p.part_o, prw * D + 32 * c4, o, inv, poisoned, 0);
                     if (c4 == 0) {
-                        p.part_ml[prow * 2 + 0] = poisoned ? __int_as_float(0x7fc00000) : m_ref;
-                        p.part_ml[prow * 2 + 1] = lsum;
+                        p.part_ml[prw * 2 + 0] = poisoned ? __int_as_float(0x7fc00000) : m_ref;
+                        p.part_ml[prw * 2 + 1] = lsum;
                     }
                 } else {
                     store_row32(p.out, qrow * D + 32 * c4, o, inv, poisoned, which);

@@ -455,7 +455,7 @@ int32_t pa_chunk_partition_tokens(pa_dtype kv_dtype, int32_t num_seqs, int32_t n
         return PA_ERR_INVALID;
     if (partition_size == 0 && device_sm_count() <= 0)
         return PA_ERR_CUDA;
-    const int rows_tokens = 128 / (num_q_heads / num_kv_heads);
+    const int rows_tokens = kChunkCtaRows / (num_q_heads / num_kv_heads);
     const int m_tiles = (max_query_len + rows_tokens - 1) / rows_tokens;
     return chunk_partition(kv_dtype, num_seqs, num_kv_heads, m_tiles, head_dim, block_size,
                            max_context_len, partition_size);
@@ -508,7 +508,7 @@ int pa_chunk_attention(void* out, pa_dtype out_dtype, const void* q, const void*
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
         return PA_ERR_INVALID;
     const int group = num_q_heads / num_kv_heads;
-    const int rows_tokens = 128 / group;
+    const int rows_tokens = kChunkCtaRows / group;
     const int m_tiles = (max_query_len + rows_tokens - 1) / rows_tokens;
     if ((int64_t)num_kv_heads * m_tiles > 65535)
         return PA_ERR_INVALID;

@@ -128,6 +128,9 @@ cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);
 cudaError_t kv_tensor_map(CUtensorMap* map, const void* base, int64_t num_blocks, int num_kv_heads,
                           int block_size, int head_dim, pa_dtype dtype);
 
+// (query token, query head) rows one chunk-attention CTA serves (two 128-row tiles).
+constexpr int kChunkCtaRows = 256;
+
 // Causal attention of chunks of new query tokens over the paged cache (the
 // tensor-core kernel of chunk_attn.cuh).  Rows of q / out are (query token, query
 // head) pairs, [num_rows][num_q_heads][head_dim].
@@ -147,7 +150,7 @@ struct ChunkParams {
     int num_q_heads;
     int num_kv_heads;
     int group;                   // num_q_heads / num_kv_heads (<= 128)
-    int rows_tokens;             // chunk tokens per CTA row tile: 128 / group
+    int rows_tokens;             // chunk tokens per CTA: kChunkCtaRows / group
     int m_tiles;                 // row tiles per (sequence, kv head)
     int max_query_len;
     int max_context_len;
