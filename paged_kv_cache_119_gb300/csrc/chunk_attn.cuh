@@ -14,7 +14,8 @@
 // r = token * G + head -- as two 128-row query tiles.  K and V stream through the
 // block table in tiles of 64 tokens, each tile serving both query tiles:
 //   S_q[128 x 64]  = Q_q[128 x D] . K^T      (tcgen05.mma kind::f16, fp32 in TMEM)
-//   O_q[128 x D]  += P_q[128 x 64] . V        (P = hi + lo halves of the 16-bit type)
+//   O_q[128 x D]  += P_q[128 x 64] . V        (P = hi + lo halves of the 16-bit type,
+//                                              A operand read from tensor memory)
 //   * warp 0 (producer): block-table entries and tensor-map TMA of the tile's K
 //     and V boxes (64 dims x B tokens, 128-byte swizzle) into an mbarrier ring;
 //   * warp 1: allocates all 512 tensor-memory columns and (one thread) issues the
@@ -23,7 +24,11 @@
 //     the softmax warps work;
 //   * warps 2-5 (query tile 0) and 6-9 (query tile 1), one thread per row = TMEM
 //     lane: read S, mask (causal within the chunk, end of context), online softmax
-//     in base 2, write P to shared memory in the operand layout, keep O up to date.
+//     in base 2, write P back over the S buffer it came from (packed 16-bit pairs),
+//     keep O up to date.
+// The S/P buffers alternate between tiles, so the softmax of tile i+1 never waits
+// for P.V of tile i; the scores of tile i+2 reuse a buffer only once P.V of tile i
+// has read it.
 // Two softmax warps per SM sub-partition hide each other's latency; the MUFU work
 // (one exp2 per score) stays below the tensor-core time of a tile.
 // Rescaling O is lazy: a row's reference maximum moves only when a tile's maximum
@@ -57,33 +62,30 @@ struct ChunkSmem {
     static constexpr int kHalves = D / 64;                       // 128-byte column groups
     static constexpr int kQHalf = kChunkRows * 128;              // 16 KB
     static constexpr int kQTile = kHalves * kQHalf;              // one 128-row query tile
-    static constexpr int kPBytes = kChunkRows * 128;             // 128 rows x 64 tokens x 2 B
     static constexpr int kKVHalf = kChunkTileTok * 128;          // 8 KB
     static constexpr int kKBytes = kHalves * kKVHalf;
     static constexpr int kStageBytes = 2 * kKBytes;              // K then V
     static constexpr int kQOff = 0;
-    static constexpr int kPOff = kQOff + kChunkQTiles * kQTile;  // [query tile][hi, lo]
-    static constexpr int kStageOff = kPOff + kChunkQTiles * 2 * kPBytes;
+    static constexpr int kStageOff = kQOff + kChunkQTiles * kQTile;
     static constexpr int kBarOff = kStageOff + NST * kStageBytes;
-    // full[NST], empty[NST], s_full[2][2], s_free[2][2], p_full[2], pv_done[2],
-    // q_full, mma_done
-    static constexpr int kNumBars = 2 * NST + 14;
+    // full[NST], empty[NST], s_full[2][2], p_full[2][2], pv_done[2], q_full, mma_done
+    static constexpr int kNumBars = 2 * NST + 12;
     static constexpr int kOkOff = kBarOff + 8 * kNumBars;        // stage_ok[NST]
     static constexpr int kSlotOff = kOkOff + 4 * NST;            // TMEM address
     static constexpr int kBytes = kSlotOff + 16;
     static constexpr int kAlloc = kBytes + 1024;                 // 1 KB alignment slack
-    // tensor memory: O of query tile q at column 128 q, its two S buffers at
-    // 256 + 128 q and 256 + 128 q + 64
+    // tensor memory: O of query tile q at column 128 q, its two S/P buffers at
+    // 256 + 128 q and 256 + 128 q + 64 (P: hi in the first 32 columns, lo in the next)
     static constexpr int kTmemCols = 512;
     static constexpr int kSCol = 256;
     static_assert(D <= 128, "O must fit in 128 columns");
     static_assert(kAlloc <= 227 * 1024, "shared memory");
 };
 
-// Stages of the K/V ring: as many as fit next to the query tiles and P buffers.
+// Stages of the K/V ring: as many as fit next to the query tiles.
 template <int D>
 struct ChunkStages {
-    static constexpr int value = D == 128 ? 3 : 5;
+    static constexpr int value = D == 128 ? 5 : 8;
 };
 
 // 2^x on the MUFU unit (relative error far below the 2^-17 of the P split).
@@ -170,10 +172,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sm::kBarOff);
     uint64_t* empty = full + NST;
-    uint64_t* s_full = empty + NST;              // [query tile][S buffer]
-    uint64_t* s_free = s_full + 4;
-    uint64_t* p_full = s_free + 4;               // [query tile]
-    uint64_t* pv_done = p_full + 2;
+    uint64_t* s_full = empty + NST;              // [query tile][S/P buffer]
+    uint64_t* p_full = s_full + 4;               // [query tile][S/P buffer]
+    uint64_t* pv_done = p_full + 4;              // [query tile]
     uint64_t* q_full = pv_done + 2;
     uint64_t* mma_done = q_full + 1;
     int* stage_ok = reinterpret_cast<int*>(smem + Sm::kOkOff);
@@ -239,13 +240,11 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 4);
+            mbar_init(&p_full[i], 4);
         }
 #pragma unroll
-        for (int q = 0; q < kChunkQTiles; ++q) {
-            mbar_init(&p_full[q], 4);
+        for (int q = 0; q < kChunkQTiles; ++q)
             mbar_init(&pv_done[q], 1);
-        }
         mbar_init(q_full, kChunkSoftmaxWarps);
         mbar_init(mma_done, 1);
         fence_mbar_init();
@@ -345,9 +344,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             for (int it = 0; it < ntiles && ok; ++it) {
                 if (it + 1 < ntiles) {
                     ok = mbar_wait(&full[(it + 1) % NST], ((it + 1) / NST) & 1);
-                    // S buffers (it+1)&1 were read by the softmax of tile it-1
+                    // S/P buffers (it+1)&1 hold P of tile it-1 until its P.V completes
                     for (int q = 0; q < kChunkQTiles && ok && it >= 1; ++q)
-                        ok = mbar_wait(&s_free[q * 2 + ((it + 1) & 1)], ((it - 1) >> 1) & 1);
+                        ok = mbar_wait(&pv_done[q], (it - 1) & 1);
                     if (!ok)
                         break;
                     tc_fence_after();
@@ -357,19 +356,18 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                     smem_addr(smem + Sm::kStageOff + (it % NST) * Sm::kStageBytes + Sm::kKBytes);
 #pragma unroll 1
                 for (int q = 0; q < kChunkQTiles && ok; ++q) {
-                    ok = mbar_wait(&p_full[q], it & 1);
+                    ok = mbar_wait(&p_full[q * 2 + (it & 1)], (it >> 1) & 1);
                     if (!ok)
                         break;
                     tc_fence_after();
-                    const uint32_t pb = smem_addr(smem + Sm::kPOff + q * 2 * Sm::kPBytes);
+                    const uint32_t pcol = tbase + Sm::kSCol + q * 128 + (it & 1) * NT;
 #pragma unroll
                     for (int half = 0; half < 2; ++half)          // hi, then lo
 #pragma unroll
                         for (int kk = 0; kk < NT / 16; ++kk) {
-                            const uint64_t a = sw128_desc(pb + half * Sm::kPBytes + kk * 32, 16, 1024);
                             const uint64_t b = sw128_desc(vb + kk * 16 * 128, Sm::kKVHalf, 1024);
-                            tc_mma_f16(tbase + q * 128, a, b, idesc_o,
-                                       (it > 0 || half > 0 || kk > 0) ? 1u : 0u);
+                            tc_mma_f16_ts(tbase + q * 128, pcol + half * (NT / 2) + kk * 8, b, idesc_o,
+                                          (it > 0 || half > 0 || kk > 0) ? 1u : 0u);
                         }
                     tc_commit(&pv_done[q]);
                 }
@@ -427,7 +425,6 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         const uint32_t o_col = lane_t + q * 128;
         float m_ref = -INFINITY, lsum = 0.f;
         bool poisoned = false;
-        unsigned char* prow = smem + Sm::kPOff + q * 2 * Sm::kPBytes + rr * 128;
         for (int it = 0; it < ntiles; ++it) {
             const int b = it & 1;
             const int st = it % NST;
@@ -443,18 +440,10 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             if (!stage_ok[st])
                 poisoned = true;
             tc_fence_after();
+            const uint32_t sp_col = lane_t + Sm::kSCol + q * 128 + b * NT;   // this row's S/P buffer
             float s[NT];
-            if (warp_live) {
-                tmem_ld32(lane_t + Sm::kSCol + q * 128 + b * NT, *reinterpret_cast<float(*)[32]>(&s[0]));
-                tmem_ld32(lane_t + Sm::kSCol + q * 128 + b * NT + 32,
-                          *reinterpret_cast<float(*)[32]>(&s[32]));
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&s_free[q * 2 + b]);
-
-            bool waited = false;
+            if (warp_live)
+                tmem_ld64(sp_col, s);
             if (warp_live) {
                 const int lim = row_valid ? pos - tb : -1;   // columns c <= lim are visible
                 if (lim < NT - 1) {
@@ -481,7 +470,6 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                             atomicOr(p.err, PA_DEVERR_TIMEOUT);
                         poisoned = true;
                     }
-                    waited = true;
                     tc_fence_after();
                     const float alpha = need ? ex2_approx(m_ref - tmax) : 1.f;
 #pragma unroll 1
@@ -517,30 +505,20 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 lsum += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
                         ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
             }
-            // the P buffer of this query tile was last read by P.V of tile it-1
-            if (it > 0 && !waited && !mbar_wait(&pv_done[q], (it - 1) & 1)) {
-                if (lane == 0)
-                    atomicOr(p.err, PA_DEVERR_TIMEOUT);
-                poisoned = true;
-                break;
-            }
             if (warp_live) {
+                // P over the S buffer: hi in its first 32 columns, lo in the next 32
+                uint32_t hi[NT / 2], lo[NT / 2];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint32_t hi[4], lo[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        split_pair<T>(s[8 * c + 2 * k], s[8 * c + 2 * k + 1], hi[k], lo[k]);
-                    const int off = (c ^ (rr & 7)) << 4;
-                    *reinterpret_cast<uint4*>(prow + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4*>(prow + Sm::kPBytes + off) =
-                        make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                }
+                for (int k = 0; k < NT / 2; ++k)
+                    split_pair<T>(s[2 * k], s[2 * k + 1], hi[k], lo[k]);
+                tmem_st32_raw(sp_col, hi);
+                tmem_st32_raw(sp_col + NT / 2, lo);
             }
             if (q == 0 && tb + NT > t1) {
                 // V rows past the range may hold anything (unused slots, stale tiles):
                 // zero them so that 0 * V stays 0.  Query tile 0's warps do it before
-                // their P is published; P.V of tile 1 is issued after that of tile 0.
+                // their P is published; P.V of query tile 1 is issued after that of
+                // query tile 0.
                 const int v0 = t1 - tb;
                 const int rows = NT - v0;
                 unsigned char* vbase = smem + Sm::kStageOff + st * Sm::kStageBytes + Sm::kKBytes;
@@ -555,14 +533,18 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&p_full[q]);
+                mbar_arrive(&p_full[q * 2 + b]);
         }
 
         // ---------------------------------------------------------------- epilogue
-        if (!mbar_wait(&pv_done[q], (ntiles - 1) & 1)) {
-            if (lane == 0)
-                atomicOr(p.err, PA_DEVERR_TIMEOUT);
-            poisoned = true;
+        // P.V of the last two tiles may both be pending (the loop waits for P.V only to
+        // rescale): wait for them in order, so no parity wait runs two phases behind
+        for (int it = max(0, ntiles - 2); it < ntiles; ++it) {
+            if (!mbar_wait(&pv_done[q], it & 1)) {
+                if (lane == 0)
+                    atomicOr(p.err, PA_DEVERR_TIMEOUT);
+                poisoned = true;
+            }
         }
         tc_fence_after();
         if (warp_live) {
