@@ -247,7 +247,10 @@ int pa_decode_fp8(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype
  *                    happens (16-byte aligned, caller-owned), else may be NULL
  * Supported: head_dim 64 / 128, block_size 16 / 32, num_q_heads / num_kv_heads <= 128.
  * Accumulation is fp32 on the tensor cores; probabilities enter the P.V product as
- * hi + lo halves of the 16-bit type, so they keep fp32-level accuracy.
+ * hi + lo halves of the 16-bit type, so they keep fp32-level accuracy.  A kv head with
+ * at most 32 (token, head) rows (max_query_len * num_q_heads / num_kv_heads: e.g.
+ * verifying a few speculated tokens) runs on the memory-bound decode kernel in a
+ * multi-row mode; longer chunks run on the tcgen05 kernel (256 rows per CTA).
  * Errors: invalid arguments return a negative pa_status with nothing launched.  On
  * the device, n_s > L_s, L_s > max_context_len, n_s > max_query_len or rows beyond
  * query_start[num_seqs] set PA_DEVERR_CONTEXT_LEN (that sequence's rows become NaN);

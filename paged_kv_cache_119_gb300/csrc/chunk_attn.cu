@@ -1,6 +1,9 @@
-// chunk_attn.cu -- host launchers of the chunk-attention kernel (chunk_attn.cuh)
-// for f16 and bf16 caches: head_dim 64 / 128, block_size 16 / 32.
+// chunk_attn.cu -- host launchers of chunk attention for f16 and bf16 caches
+// (head_dim 64 / 128, block_size 16 / 32): the tcgen05 kernel of chunk_attn.cuh
+// for long chunks, and the mma.sync decode kernel in its chunk-row mode
+// (decode_mma.cuh) when a kv head has only a few (token, head) rows.
 #include "chunk_attn.cuh"
+#include "decode_mma.cuh"
 
 namespace pa {
 
@@ -38,6 +41,73 @@ struct ChunkVariant {
         return n;
     }
 };
+
+// Chunk rows on the mma.sync decode kernel: NH rows per CTA, the split merged by
+// chunk_reduce_kernel (the same partial-row layout).
+template <typename T, int D, int BS, int NH>
+struct ChunkRowsVariant {
+    static constexpr int kStages = MmaStages<T, D, BS>::value;
+    using Sm = MmaSmem<T, D, BS, kStages>;
+    static constexpr auto kernel() { return decode_mma_kernel<T, T, D, BS, NH, kStages, true>; }
+    static cudaError_t configure()
+    {
+        return configure_once(reinterpret_cast<const void*>(kernel()), Sm::kAlloc);
+    }
+    static cudaError_t launch(const DecodeParams& p, const ChunkParams& cp, const CUtensorMap& tk,
+                              const CUtensorMap& tv, cudaStream_t stream)
+    {
+        cudaError_t err = configure();
+        if (err != cudaSuccess)
+            return err;
+        const bool split = p.partition_tokens > 0;
+        const dim3 grid(split ? p.max_parts : 1, p.num_kv_heads * p.chunks, p.num_seqs);
+        kernel()<<<grid, kDecodeThreads, Sm::kAlloc, stream>>>(p, tk, tv);
+        err = cudaGetLastError();
+        if (err != cudaSuccess || !split)
+            return err;
+        chunk_reduce_kernel<T, D><<<dim3((unsigned)cp.num_rows, cp.num_q_heads), D, 0, stream>>>(cp);
+        return cudaGetLastError();
+    }
+    static int occupancy()
+    {
+        return configure() == cudaSuccess
+                   ? kernel_occupancy(reinterpret_cast<const void*>(kernel()), Sm::kAlloc)
+                   : 0;
+    }
+};
+
+#define PA_CHUNK_ROWS_VARIANTS(X) \
+    X(128, 16, 8) X(128, 16, 4) X(128, 32, 8) X(128, 32, 4) X(64, 16, 8) X(64, 16, 4) \
+    X(64, 32, 8) X(64, 32, 4)
+
+cudaError_t launch_chunk_rows(const DecodeParams& p, const ChunkParams& cp, pa_dtype dtype,
+                              int head_dim, int block_size, int nh, const CUtensorMap& tk,
+                              const CUtensorMap& tv, cudaStream_t stream)
+{
+#define PA_CHUNK_ROWS_CASE(D_, BS_, NH_)                                                    \
+    if (head_dim == D_ && block_size == BS_ && nh == NH_)                                   \
+        return dtype == PA_BF16                                                             \
+                   ? ChunkRowsVariant<__nv_bfloat16, D_, BS_, NH_>::launch(p, cp, tk, tv, stream) \
+                   : ChunkRowsVariant<__half, D_, BS_, NH_>::launch(p, cp, tk, tv, stream);
+    if (dtype == PA_BF16 || dtype == PA_F16) {
+        PA_CHUNK_ROWS_VARIANTS(PA_CHUNK_ROWS_CASE)
+    }
+#undef PA_CHUNK_ROWS_CASE
+    return cudaErrorInvalidValue;
+}
+
+int occupancy_chunk_rows(pa_dtype dtype, int head_dim, int block_size, int nh)
+{
+#define PA_CHUNK_ROWS_OCC(D_, BS_, NH_)                                          \
+    if (head_dim == D_ && block_size == BS_ && nh == NH_)                        \
+        return dtype == PA_BF16 ? ChunkRowsVariant<__nv_bfloat16, D_, BS_, NH_>::occupancy() \
+                                : ChunkRowsVariant<__half, D_, BS_, NH_>::occupancy();
+    if (dtype == PA_BF16 || dtype == PA_F16) {
+        PA_CHUNK_ROWS_VARIANTS(PA_CHUNK_ROWS_OCC)
+    }
+#undef PA_CHUNK_ROWS_OCC
+    return 0;
+}
 
 #define PA_CHUNK_VARIANTS(X) X(128, 16) X(128, 32) X(64, 16) X(64, 32)
 

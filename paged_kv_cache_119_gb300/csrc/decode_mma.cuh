@@ -196,7 +196,11 @@ struct MmaSmem {
 // T: query / native output type (the mma operand type).  TK: cache element type,
 // T itself (tiles by tensor-map TMA) or __nv_fp8_e4m3 (raw tiles by 1-D bulk copy,
 // converted exactly to T in shared memory; the value is code * per-kv-head scale).
-template <typename T, typename TK, int D, int BS, int NH, int NSTAGE>
+// CH (chunk rows): the NH B-operand columns are rows R0 .. R0+NH-1 of the
+// (chunk token, query head) rows of one kv head -- several new query tokens of a
+// sequence attended causally, each row masked at its own position (speculative
+// verification, short chunks) -- instead of NH query heads of one token.
+template <typename T, typename TK, int D, int BS, int NH, int NSTAGE, bool CH = false>
 __global__ void __launch_bounds__(kDecodeThreads)
     decode_mma_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv)
@@ -231,22 +235,47 @@ __global__ void __launch_bounds__(kDecodeThreads)
     const bool split = p.partition_tokens > 0;
 
     const int L = p.context_lens[seq];
-    if (L < 0 || L > p.max_context_len) {
+    // chunk rows: the sequence's rows of q / out are query_start[seq] .. + n - 1
+    int qs0 = 0, n = 1, R0 = 0;
+    if constexpr (CH) {
+        qs0 = p.query_start[seq];
+        n = p.query_start[seq + 1] - qs0;
+        R0 = (blockIdx.y % p.chunks) * NH;
+    }
+    const bool rows_sane = !CH || (qs0 >= 0 && n >= 0 && (int64_t)qs0 + n <= p.num_rows);
+    if (L < 0 || L > p.max_context_len || !rows_sane ||
+        (CH && (n > L || n > p.max_query_len))) {
         if (part == 0 && blockIdx.y == 0 && threadIdx.x == 0)
             atomicOr(p.err, PA_DEVERR_CONTEXT_LEN);
-        if (!split) {
-            for (int idx = threadIdx.x; idx < NH * D; idx += blockDim.x)
-                store_out<T>(p, ((int64_t)seq * p.num_q_heads + h0) * D + idx,
-                             __int_as_float(0x7fc00000));
+        if (!split && rows_sane) {
+            for (int idx = threadIdx.x; idx < NH * D; idx += blockDim.x) {
+                if constexpr (CH) {
+                    const int R = R0 + idx / D;
+                    const int j = R / p.group;
+                    if (j < n)
+                        store_out<T>(p, ((int64_t)(qs0 + j) * p.num_q_heads + kvh * p.group +
+                                         (R - j * p.group)) * D + idx % D,
+                                     __int_as_float(0x7fc00000));
+                } else {
+                    store_out<T>(p, ((int64_t)seq * p.num_q_heads + h0) * D + idx,
+                                 __int_as_float(0x7fc00000));
+                }
+            }
         }
         return;
     }
-    int t0 = 0, t1 = L;
+    int t_end = L;
+    if constexpr (CH) {
+        if (R0 / p.group >= n)
+            return;                                // no chunk token in this row chunk
+        t_end = L - n + min(n - 1, (R0 + NH - 1) / p.group) + 1;   // last row's position + 1
+    }
+    int t0 = 0, t1 = t_end;
     if (split) {
         t0 = part * p.partition_tokens;
-        if (t0 >= L)
+        if (t0 >= t_end)
             return;
-        t1 = min(L, t0 + p.partition_tokens);
+        t1 = min(t_end, t0 + p.partition_tokens);
     }
     const int jb = t0 / BS;
     const int ntiles = (t1 > t0) ? (t1 + BS - 1) / BS - jb : 0;
@@ -338,9 +367,15 @@ __global__ void __launch_bounds__(kDecodeThreads)
     uint32_t qb[KS][2];
     float q_unscale = 1.f;            // for E4M3 caches: q was scaled by 2^-e to fit f16
     {
-        const bool live = g < NH;
-        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-            reinterpret_cast<const T*>(p.q) + ((int64_t)seq * p.num_q_heads + h0 + (live ? g : 0)) * D);
+        bool live = g < NH;
+        int64_t qr = (int64_t)seq * p.num_q_heads + h0 + (live ? g : 0);
+        if constexpr (CH) {
+            const int R = R0 + g;
+            const int j = R / p.group;
+            live = live && j < n;
+            qr = live ? (int64_t)(qs0 + j) * p.num_q_heads + kvh * p.group + (R - j * p.group) : 0;
+        }
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(reinterpret_cast<const T*>(p.q) + qr * D);
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             // k-indices 2c, 2c+1 | 2c+8, 2c+9 of step ks are head dims 16ks + 2c.. | +8..,
@@ -392,6 +427,16 @@ __global__ void __launch_bounds__(kDecodeThreads)
     bool poisoned = false;
     // scores carry the softmax scale (base 2) and, for a quantised cache, the K scale
     const float sl2 = kFp8 ? p.scale_log2 * p.k_scale[kvh] * q_unscale : p.scale_log2;
+    // chunk rows: the last visible position of rows 2c and 2c+1 (-1: padding row)
+    int lim[2] = {0, 0};
+    if constexpr (CH) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int R = R0 + 2 * c + j;
+            const int tk = R / p.group;
+            lim[j] = (2 * c + j < NH && tk < n) ? L - n + tk : -1;
+        }
+    }
 
     for (int it = warp; it < ntiles; it += NCW) {
         const int stage = it % NSTAGE;
@@ -468,6 +513,14 @@ __global__ void __launch_bounds__(kDecodeThreads)
             x[1] = tok_a < nvalid ? s[1] * sl2 : -INFINITY;
             x[2] = tok_b < nvalid ? s[2] * sl2 : -INFINITY;
             x[3] = tok_b < nvalid ? s[3] * sl2 : -INFINITY;
+            if constexpr (CH) {
+                // causal within the chunk: token t is visible to a row at position >= t
+                const int abs_a = (jb + it) * BS + tok_a, abs_b = abs_a + 8;
+                x[0] = abs_a <= lim[0] ? x[0] : -INFINITY;
+                x[1] = abs_a <= lim[1] ? x[1] : -INFINITY;
+                x[2] = abs_b <= lim[0] ? x[2] : -INFINITY;
+                x[3] = abs_b <= lim[1] ? x[3] : -INFINITY;
+            }
             float alpha[2];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
@@ -619,7 +672,14 @@ __global__ void __launch_bounds__(kDecodeThreads)
             out *= p.v_scale[kvh];
         if (bad)
             out = __int_as_float(0x7fc00000);
-        const int64_t row = (int64_t)seq * p.num_q_heads + h0 + h;
+        int64_t row = (int64_t)seq * p.num_q_heads + h0 + h;
+        if constexpr (CH) {
+            const int R = R0 + h;
+            const int j = R / p.group;
+            if (j >= n)
+                continue;                          // padding row
+            row = (int64_t)(qs0 + j) * p.num_q_heads + kvh * p.group + (R - j * p.group);
+        }
         if (split) {
             const int64_t prow = row * p.max_parts + part;
             p.part_o[prow * D + d] = out;

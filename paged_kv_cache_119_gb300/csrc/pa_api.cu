@@ -281,16 +281,45 @@ int decode_partition(pa_dtype q_dtype, pa_dtype kv_dtype, int num_seqs, int num_
                             (int64_t)device_sm_count() * occ, block_size);
 }
 
-// The partition length pa_chunk_attention uses for these arguments (0: one pass).
-int chunk_partition(pa_dtype kv_dtype, int num_seqs, int num_kv_heads, int m_tiles,
-                    int head_dim, int block_size, int max_context_len, int partition_size)
+// How pa_chunk_attention runs a call: few (token, head) rows per kv head go to the
+// mma.sync decode kernel in chunk-row mode (nh rows per CTA), longer chunks to the
+// tcgen05 kernel (rows_tokens chunk tokens per CTA); partition = split length.
+struct ChunkPlan {
+    bool rows_path;
+    int nh;          // rows per CTA on the decode kernel
+    int chunks;      // CTAs per (sequence, kv head, partition)
+    int rows_tokens; // tcgen05 kernel: chunk tokens per CTA
+    int partition;
+};
+
+ChunkPlan chunk_plan(pa_dtype kv_dtype, int num_seqs, int num_q_heads, int num_kv_heads,
+                     int head_dim, int block_size, int max_query_len, int max_context_len,
+                     int partition_size)
 {
+    ChunkPlan c{};
+    const int group = num_q_heads / num_kv_heads;
+    const int64_t rows = (int64_t)max_query_len * group;
+    if (rows <= kChunkRowsMax) {
+        c.rows_path = true;
+        c.nh = rows <= 4 ? 4 : 8;
+        c.chunks = (int)((rows + c.nh - 1) / c.nh);
+        int occ = 0;
+        if (partition_size == 0)
+            occ = occupancy_chunk_rows(kv_dtype, head_dim, block_size, c.nh);
+        c.partition = choose_partition(partition_size, max_context_len,
+                                       (int64_t)num_seqs * num_kv_heads * c.chunks,
+                                       (int64_t)device_sm_count() * occ, block_size);
+        return c;
+    }
+    c.rows_tokens = kChunkCtaRows / group;
+    c.chunks = (max_query_len + c.rows_tokens - 1) / c.rows_tokens;
     int occ = 0;
     if (partition_size == 0)
         occ = occupancy_chunk_attention(kv_dtype, head_dim, block_size);
-    return choose_chunk_partition(partition_size, max_context_len,
-                                  (int64_t)num_seqs * num_kv_heads * m_tiles,
-                                  (int64_t)device_sm_count() * occ);
+    c.partition = choose_chunk_partition(partition_size, max_context_len,
+                                         (int64_t)num_seqs * num_kv_heads * c.chunks,
+                                         (int64_t)device_sm_count() * occ);
+    return c;
 }
 
 // Shared body of pa_decode and pa_decode_fp8.  q_dtype is the type of q (and of a
@@ -455,10 +484,9 @@ int32_t pa_chunk_partition_tokens(pa_dtype kv_dtype, int32_t num_seqs, int32_t n
         return PA_ERR_INVALID;
     if (partition_size == 0 && device_sm_count() <= 0)
         return PA_ERR_CUDA;
-    const int rows_tokens = kChunkCtaRows / (num_q_heads / num_kv_heads);
-    const int m_tiles = (max_query_len + rows_tokens - 1) / rows_tokens;
-    return chunk_partition(kv_dtype, num_seqs, num_kv_heads, m_tiles, head_dim, block_size,
-                           max_context_len, partition_size);
+    return chunk_plan(kv_dtype, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                      max_query_len, max_context_len, partition_size)
+        .partition;
 }
 
 size_t pa_chunk_workspace_bytes(int64_t num_query_tokens, int32_t num_q_heads, int32_t head_dim,
@@ -508,9 +536,9 @@ int pa_chunk_attention(void* out, pa_dtype out_dtype, const void* q, const void*
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
         return PA_ERR_INVALID;
     const int group = num_q_heads / num_kv_heads;
-    const int rows_tokens = kChunkCtaRows / group;
-    const int m_tiles = (max_query_len + rows_tokens - 1) / rows_tokens;
-    if ((int64_t)num_kv_heads * m_tiles > 65535)
+    const ChunkPlan plan = chunk_plan(kv_dtype, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                      block_size, max_query_len, max_context_len, partition_size);
+    if ((int64_t)num_kv_heads * plan.chunks > 65535)
         return PA_ERR_INVALID;
     const size_t row_elems = (size_t)num_query_tokens * num_q_heads * head_dim;
     const size_t q_bytes = row_elems * elem_size(kv_dtype);
@@ -521,8 +549,7 @@ int pa_chunk_attention(void* out, pa_dtype out_dtype, const void* q, const void*
         overlaps(out, out_bytes, v_cache, pool_bytes))
         return PA_ERR_INVALID;
 
-    const int P = chunk_partition(kv_dtype, num_seqs, num_kv_heads, m_tiles, head_dim,
-                                  block_size, max_context_len, partition_size);
+    const int P = plan.partition;
     ChunkParams p{};
     p.out = out;
     p.q = q;
@@ -536,8 +563,8 @@ int pa_chunk_attention(void* out, pa_dtype out_dtype, const void* q, const void*
     p.num_q_heads = num_q_heads;
     p.num_kv_heads = num_kv_heads;
     p.group = group;
-    p.rows_tokens = rows_tokens;
-    p.m_tiles = m_tiles;
+    p.rows_tokens = plan.rows_tokens;
+    p.m_tiles = plan.chunks;
     p.max_query_len = max_query_len;
     p.max_context_len = max_context_len;
     p.partition_tokens = P;
@@ -568,8 +595,38 @@ int pa_chunk_attention(void* out, pa_dtype out_dtype, const void* q, const void*
         return PA_ERR_INVALID;
     if (e != cudaSuccess)
         return PA_ERR_CUDA;
-    e = launch_chunk_attention(p, kv_dtype, head_dim, block_size, tk, tv,
-                               static_cast<cudaStream_t>(stream));
+    if (plan.rows_path) {
+        DecodeParams d{};
+        d.out = out;
+        d.q = q;
+        d.k_cache = k_cache;
+        d.v_cache = v_cache;
+        d.block_tables = block_tables;
+        d.context_lens = context_lens;
+        d.part_o = p.part_o;
+        d.part_ml = p.part_ml;
+        d.err = p.err;
+        d.num_blocks = num_blocks;
+        d.bt_stride = block_table_stride;
+        d.num_seqs = num_seqs;
+        d.num_q_heads = num_q_heads;
+        d.num_kv_heads = num_kv_heads;
+        d.group = group;
+        d.chunks = plan.chunks;
+        d.max_context_len = max_context_len;
+        d.partition_tokens = P;
+        d.max_parts = p.max_parts;
+        d.out_f32 = p.out_f32;
+        d.scale_log2 = p.scale_log2;
+        d.query_start = query_start;
+        d.num_rows = num_query_tokens;
+        d.max_query_len = max_query_len;
+        e = launch_chunk_rows(d, p, kv_dtype, head_dim, block_size, plan.nh, tk, tv,
+                              static_cast<cudaStream_t>(stream));
+    } else {
+        e = launch_chunk_attention(p, kv_dtype, head_dim, block_size, tk, tv,
+                                   static_cast<cudaStream_t>(stream));
+    }
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

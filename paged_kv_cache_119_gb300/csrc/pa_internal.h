@@ -50,6 +50,10 @@ struct DecodeParams {
     int max_parts;
     int out_f32;
     float scale_log2;    // scale * log2(e): scores are kept in base-2 units
+    // chunk rows (decode_mma_kernel's CH mode only; null / 0 for decode)
+    const int32_t* query_start;
+    int64_t num_rows;
+    int max_query_len;
 };
 
 // Per-dtype decode launchers (one translation unit each).  `gc` is the number of
@@ -164,6 +168,15 @@ cudaError_t launch_chunk_attention(const ChunkParams& p, pa_dtype dtype, int hea
                                    cudaStream_t stream);
 // Resident chunk-attention CTAs per SM (0 if unknown).
 int occupancy_chunk_attention(pa_dtype dtype, int head_dim, int block_size);
+// Few rows per kv head: the mma.sync decode kernel in chunk-row mode, `nh` (4 or 8)
+// rows per CTA; p carries the chunk fields (query_start, num_rows, max_query_len)
+// and p.chunks = row chunks per kv head; cp describes the same call for the merge.
+// Rows per kv head at or below this use it.
+constexpr int kChunkRowsMax = 32;
+cudaError_t launch_chunk_rows(const DecodeParams& p, const ChunkParams& cp, pa_dtype dtype,
+                              int head_dim, int block_size, int nh, const CUtensorMap& tk,
+                              const CUtensorMap& tv, cudaStream_t stream);
+int occupancy_chunk_rows(pa_dtype dtype, int head_dim, int block_size, int nh);
 
 // Sets the dynamic shared-memory limit of a kernel once per device and process.
 inline cudaError_t configure_once(const void* kernel, int smem_bytes)

@@ -217,3 +217,50 @@ def test_canaries_around_output():
     assert (buf[:4096] == 12345.0).all() and (buf[-4096:] == 12345.0).all()
     assert torch.isfinite(out).all()
     assert P.pa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("Hq,Hkv,nmax", [(8, 8, 3), (8, 8, 4), (40, 40, 4), (16, 4, 2),
+                                         (16, 4, 8), (40, 8, 6), (64, 8, 4), (64, 8, 1)])
+@pytest.mark.parametrize("D,B", [(128, 16), (64, 32), (128, 32)])
+def test_short_chunks_few_rows(Hq, Hkv, nmax, D, B):
+    """At most 32 (token, head) rows per kv head -- speculative verification, short
+    chunks -- run on the mma.sync decode kernel in its chunk-row mode."""
+    rng = np.random.default_rng(Hq * 7919 + nmax * 31 + D + B)
+    lens = [int(x) for x in rng.integers(1, 600, size=7)] + [nmax, 1]
+    chunks = [min(L, int(rng.integers(0, nmax + 1))) for L in lens]
+    chunks[0] = min(lens[0], nmax)
+    w = make_case(int(rng.integers(1 << 30)), len(lens), Hq, Hkv, D, B, torch.bfloat16, lens,
+                  chunks)
+    run_and_compare(w)
+
+
+@pytest.mark.parametrize("part", [0, 64, 256, -1])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.float16])
+def test_short_chunks_splits_and_native_output(part, out_dtype):
+    w = make_case(29, 4, 32, 8, 128, 16, torch.float16, [3000, 700, 64, 1], [4, 4, 2, 1])
+    run_and_compare(w, out_dtype=out_dtype, partition_size=part)
+
+
+def test_verify4_full_batch_sampled_rows():
+    """The full 256-sequence verification step at the benchmark's launch configuration;
+    sampled rows against the oracle."""
+    w = workloads.make("llama13b_verify4", device="cuda")
+    P.pa_reshape_and_cache(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping)
+    out = torch.empty(w.q.shape, dtype=torch.float32, device="cuda")
+    P.pa_chunk_attention(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                         w.query_start, w.scale, w.num_kv_heads, w.block_size,
+                         max_query_len=w.max_query_len, max_context_len=w.max_context_len)
+    torch.cuda.synchronize()
+    assert P.pa_get_device_error() == 0
+    rng = np.random.default_rng(6)
+    seqs = sorted(rng.choice(w.num_seqs, size=12, replace=False).tolist())
+    qs = w.query_start.cpu()
+    rows = torch.cat([torch.arange(int(qs[s]), int(qs[s + 1])) for s in seqs])
+    sub_qs = torch.tensor(np.concatenate([[0], np.cumsum([int(qs[s + 1] - qs[s]) for s in seqs])]),
+                          dtype=torch.int32)
+    ref = oracle.chunk_attention(w.q[rows.cuda()].cpu(), w.k_cache.cpu(), w.v_cache.cpu(),
+                                 w.block_tables.cpu()[seqs], w.context_lens.cpu()[seqs], sub_qs,
+                                 w.scale, w.num_kv_heads, w.block_size,
+                                 num_threads=oracle.max_threads())
+    err = np.abs(out[rows.cuda()].double().cpu().numpy() - ref).max()
+    assert err <= ATOL, err
