@@ -69,6 +69,8 @@ def _declare(lib):
     lib.orc_reshape_and_cache.restype = ctypes.c_int
     lib.orc_reshape_and_cache.argtypes = [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i32, c_i32,
                                           c_i32, c_i64, c_i32]
+    lib.orc_swap_blocks.restype = ctypes.c_int
+    lib.orc_swap_blocks.argtypes = [c_vp, c_vp, c_i32, c_vp, c_i64, c_i64, c_i64, c_i64]
     lib.orc_copy_blocks.restype = ctypes.c_int
     lib.orc_copy_blocks.argtypes = [c_vp, c_i32, c_vp, c_i64, c_i64, c_i64]
     lib.orc_f16_to_f64.restype = c_dbl
@@ -270,6 +272,28 @@ def copy_blocks(caches, pairs, lib=None) -> None:
     rc = lib.orc_copy_blocks(ptrs, len(arrs), _ptr(pr), pr.shape[0], block_bytes, n_blocks)
     if rc != 0:
         raise ValueError(f"oracle copy_blocks rejected its inputs (status {rc})")
+
+
+def swap_blocks(src_caches, dst_caches, pairs, lib=None) -> None:
+    """Move whole blocks src -> dst between two pools per cache (in place on dst):
+    dst_caches[c][d] = src_caches[c][s] for every (s, d) pair.  CPU tensors/arrays whose
+    first dim is the block id; the src and dst pools of a cache may differ in size."""
+    lib = lib or load_library()
+    srcs = [_raw(c) for c in src_caches]
+    dsts = [_raw(c, inplace=True) for c in dst_caches]
+    assert len(srcs) == len(dsts)
+    ns, nd = srcs[0].shape[0], dsts[0].shape[0]
+    bb = srcs[0].nbytes // ns
+    for a in srcs:
+        assert a.shape[0] == ns and a.nbytes // ns == bb
+    for a in dsts:
+        assert a.shape[0] == nd and a.nbytes // nd == bb
+    pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
+    sp = (ctypes.c_void_p * len(srcs))(*[_ptr(a) for a in srcs])
+    dp = (ctypes.c_void_p * len(dsts))(*[_ptr(a) for a in dsts])
+    rc = lib.orc_swap_blocks(dp, sp, len(srcs), _ptr(pr), pr.shape[0], bb, ns, nd)
+    if rc != 0:
+        raise ValueError(f"oracle swap_blocks rejected its inputs (status {rc})")
 
 
 def f16_bits_to_f64(bits: int) -> float:

@@ -433,6 +433,29 @@ int orc_copy_blocks(void* const* caches, int num_caches, const int64_t* pairs,
     return 0;
 }
 
+/*
+ * swap_blocks: moves whole blocks between two pools of one cache that live in
+ * different memories -- the swapping of a preempted sequence group's KV blocks to
+ * CPU memory and back ("PagedAttention 完全拆解", section "调度与抢占：内存不够时
+ * 怎么办", 换出 (Swapping)).  For every cache c and pair (s, d):
+ * dst[c][d] = src[c][s], block_bytes bytes; nothing else changes.  Returns 0, or -1
+ * for a block id outside its pool.
+ */
+int orc_swap_blocks(void* const* dst, void* const* src, int num_caches, const int64_t* pairs,
+                    int64_t num_pairs, int64_t block_bytes, int64_t src_blocks,
+                    int64_t dst_blocks)
+{
+    for (int64_t p = 0; p < num_pairs; ++p)
+        if (pairs[2 * p] < 0 || pairs[2 * p] >= src_blocks || pairs[2 * p + 1] < 0 ||
+            pairs[2 * p + 1] >= dst_blocks)
+            return -1;
+    for (int c = 0; c < num_caches; ++c)
+        for (int64_t p = 0; p < num_pairs; ++p)
+            memcpy((char*)dst[c] + pairs[2 * p + 1] * block_bytes,
+                   (const char*)src[c] + pairs[2 * p] * block_bytes, (size_t)block_bytes);
+    return 0;
+}
+
 int orc_max_threads(void)
 {
 #ifdef _OPENMP

@@ -624,4 +624,48 @@ def pin_chunk_longer_than_context_is_nan(lib):
     np.testing.assert_allclose(out[n0], ref, rtol=1e-12, atol=1e-13)
 
 
+# ----------------------------------------------------------------------------- swapping
+
+def pin_swap_moves_blocks_by_index(lib):
+    """swap_blocks writes dst[d] = src[s] for each pair (numpy fancy indexing as the
+    reference), leaves every other destination block and the source untouched."""
+    g = torch.Generator().manual_seed(31)
+    src = [torch.randn(9, 2, 4, 8, generator=g).to(torch.bfloat16) for _ in range(3)]
+    dst = [torch.randn(6, 2, 4, 8, generator=g).to(torch.bfloat16) for _ in range(3)]
+    before_src = [t.clone() for t in src]
+    want = [t.clone() for t in dst]
+    pairs = [(7, 0), (2, 5), (4, 3)]
+    for w, sr in zip(want, src):
+        w[[d for _, d in pairs]] = sr[[s for s, _ in pairs]]
+    oracle.swap_blocks(src, dst, pairs, lib=lib)
+    for a, b in zip(dst, want):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    for a, b in zip(src, before_src):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def pin_swap_out_and_in_restores_attention(lib):
+    """A preempted sequence swapped out to a CPU pool and back into other GPU blocks
+    ("调度与抢占", 换出: copied out, returned when memory frees) attends exactly as
+    before once its block table names the new blocks."""
+    rng = np.random.default_rng(32)
+    c = random_case(rng, 3, 4, 2, 32, 8, torch.float32, 60, extra_blocks=12)
+    lens, tables = c["lens"], c["tables"]
+    before = run_oracle(lib, c["q"], c["kc"], c["vc"], tables, lens, 0.2, 2, 8)
+    victim = 1
+    used = {b for t in tables for b in t}
+    free = [b for b in range(c["N"]) if b not in used]
+    cpu_k = torch.zeros((len(tables[victim]),) + tuple(c["kc"].shape[1:]))
+    cpu_v = torch.zeros_like(cpu_k)
+    out_pairs = [(b, i) for i, b in enumerate(tables[victim])]
+    oracle.swap_blocks([c["kc"], c["vc"]], [cpu_k, cpu_v], out_pairs, lib=lib)
+    c["kc"][tables[victim]] = float("nan")               # the GPU blocks are reused
+    c["vc"][tables[victim]] = float("nan")
+    new = free[:len(tables[victim])]
+    oracle.swap_blocks([cpu_k, cpu_v], [c["kc"], c["vc"]], list(enumerate(new)), lib=lib)
+    tables = [t if s != victim else new for s, t in enumerate(tables)]
+    after = run_oracle(lib, c["q"], c["kc"], c["vc"], tables, lens, 0.2, 2, 8)
+    assert np.array_equal(before, after)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -61,6 +61,12 @@ MUTANTS = {
                                     "block_tables + (int64_t)s * bt_stride, s, h,"),
     "chunk_row_owner_off_by_one": ("while (query_start[s + 1] <= row)",
                                    "while (query_start[s + 1] < row)"),
+    "swap_first_cache_only": ("(const char*)src[c] + pairs[2 * p] * block_bytes, (size_t)block_bytes);",
+                              "(const char*)src[0] + pairs[2 * p] * block_bytes, (size_t)block_bytes);"),
+    "swap_dst_is_pair_index": ("memcpy((char*)dst[c] + pairs[2 * p + 1] * block_bytes,",
+                               "memcpy((char*)dst[c] + p * block_bytes,"),
+    "swap_short_copy": ("(const char*)src[c] + pairs[2 * p] * block_bytes, (size_t)block_bytes);",
+                        "(const char*)src[c] + pairs[2 * p] * block_bytes, (size_t)block_bytes / 2);"),
 }
 
 
