@@ -59,6 +59,12 @@ WORKLOADS["long16_chunk512"] = (
     "rows), 64 q / 8 kv heads, head_dim 128, bf16, block_size 16, N(0, 1)")
 CHUNK_METRIC = {"llama13b_verify4": "paged verify attention KV GB/s",
                 "long16_chunk512": "paged chunk attention TFLOP/s"}
+# swapping (pa_swap_blocks): a preempted group's blocks out to pinned CPU memory and back
+WORKLOADS["llama13b_swap"] = (
+    "KV swapping on the LLaMA-13B batch: every block of the last 64 of 256 sequences "
+    "(all-or-nothing per sequence), one layer's K and V pools (160 KB blocks), out to a "
+    "pinned CPU pool and back into the GPU pool, one pa_swap_blocks launch each way")
+SWAP_METRIC = "paged KV swap GB/s (out + in)"
 DTYPE_NAME = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32",
               torch.float8_e4m3fn: "fp8_e4m3"}
 METRIC = "paged decode attention KV GB/s"
@@ -294,9 +300,188 @@ def step_ops(pa, w):
 
 # ------------------------------------------------------------------------------ our arm
 
+def swap_plan(w, victims=64):
+    """(GPU block ids of the last `victims` sequences, bytes of one block)."""
+    bt = w.block_tables.cpu()
+    lens = w.context_lens.tolist()
+    blocks = []
+    for s in range(w.num_seqs - victims, w.num_seqs):
+        n = (lens[s] + w.block_size - 1) // w.block_size
+        blocks += [int(b) for b in bt[s, :n]]
+    bb = w.k_cache[0].numel() * w.k_cache.element_size()
+    return blocks, bb
+
+
+def link_peak_gbs(dev, nbytes=1 << 30, reps=5):
+    """Best 1 GiB pinned-host <-> device DMA copy rate, each way, in GB/s."""
+    host = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    devb = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    best = {}
+    for name, (dst, src) in (("d2h", (host, devb)), ("h2d", (devb, host))):
+        b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t = []
+        for _ in range(reps):
+            b.record()
+            dst.copy_(src, non_blocking=True)
+            e.record()
+            torch.cuda.synchronize()
+            t.append(b.elapsed_time(e))
+        best[name] = nbytes / (min(t) / 1e3) / 1e9
+    return best
+
+
+def run_swap(args, rank, world, local):
+    """The swap step: every block of the victim sequences, K and V, out to a pinned CPU
+    pool (one launch) and back into its GPU blocks (one launch)."""
+    import paged_kv_cache_119_gb300 as pa
+    from paged_kv_cache_119_gb300 import build as pa_build
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pa_build.build()
+    w = make_workload("llama13b", dev, args.num_seqs)
+    blocks, bb = swap_plan(w, min(64, w.num_seqs))
+    n = len(blocks)
+    cpu_k = torch.empty((n,) + tuple(w.k_cache.shape[1:]), dtype=w.dtype).pin_memory()
+    cpu_v = torch.empty_like(cpu_k).pin_memory()
+    out_pairs = [(b, i) for i, b in enumerate(blocks)]
+    in_pairs = [(i, b) for i, b in enumerate(blocks)]
+    moved = 2 * 2 * n * bb                       # K and V, out and in
+
+    def step(e=None):
+        if e is not None:
+            e[0].record()
+        pa.pa_swap_blocks([w.k_cache, w.v_cache], [cpu_k, cpu_v], out_pairs)
+        if e is not None:
+            e[1].record()
+        pa.pa_swap_blocks([cpu_k, cpu_v], [w.k_cache, w.v_cache], in_pairs)
+        if e is not None:
+            e[2].record()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    begin, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0_wall = time.time()
+    begin.record()
+    for i in range(args.steps):
+        step(ev[i])
+    end.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t1_wall = time.time()
+    clocks = sampler.stop(t0_wall, t1_wall) if rank == 0 else None
+    total_ms = begin.elapsed_time(end)
+    out_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    in_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    sec = max_over_ranks(total_ms / 1e3, dev) if world > 1 else total_ms / 1e3
+    value = moved * args.steps * world / sec / 1e9
+
+    # the same moves as one cudaMemcpyAsync per block and pool (the per-block transfers
+    # whose small size the pages' Figure 19a blames), for comparison
+    def per_block():
+        for (g, c) in out_pairs:
+            cpu_k[c].copy_(w.k_cache[g], non_blocking=True)
+            cpu_v[c].copy_(w.v_cache[g], non_blocking=True)
+        for (c, g) in in_pairs:
+            w.k_cache[g].copy_(cpu_k[c], non_blocking=True)
+            w.v_cache[g].copy_(cpu_v[c], non_blocking=True)
+    per_block()
+    torch.cuda.synchronize()
+    b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b.record()
+    for _ in range(3):
+        per_block()
+    e.record()
+    torch.cuda.synchronize()
+    per_block_gbs = 3 * moved / (b.elapsed_time(e) / 1e3) / 1e9
+
+    # end to end through the public API: each step waits for its moves on the host
+    def e2e_step():
+        pa.pa_swap_blocks([w.k_cache, w.v_cache], [cpu_k, cpu_v], out_pairs)
+        pa.pa_swap_blocks([cpu_k, cpu_v], [w.k_cache, w.v_cache], in_pairs)
+        torch.cuda.current_stream().synchronize()
+    for _ in range(args.warmup):
+        e2e_step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    e2e_ms = (time.perf_counter() - t) / args.steps * 1e3
+    peaks = link_peak_gbs(dev)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return None
+    peak = (peaks["d2h"] + peaks["h2d"]) / 2
+    achieved = moved / ((out_ms + in_ms) / 1e3) / 1e9
+    line = {
+        "metric": SWAP_METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[w.k_cache.dtype],
+        "data": "synthetic",
+        "config": {"workload": WORKLOADS[args.config], "name": args.config,
+                   "swapped_blocks": n, "block_bytes": bb, "bytes_per_step": moved,
+                   "l2": "no flush: each direction moves "
+                         f"{2 * n * bb / 1e9:.2f} GB, larger than the 129 MB L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "swap_out_us": round(out_ms * 1e3, 2), "swap_in_us": round(in_ms * 1e3, 2),
+        "swap_out_gbs": round(2 * n * bb / (out_ms / 1e3) / 1e9, 1),
+        "swap_in_gbs": round(2 * n * bb / (in_ms / 1e3) / 1e9, 1),
+        "per_block_memcpy_gbs": round(per_block_gbs, 1),
+        "roofline": {"bound": "link", "achieved": round(achieved, 1), "peak": round(peak, 1),
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "swap_blocks_kernel",
+                     "peak_kind": "measured in this run: mean of the best 1 GiB pinned "
+                                  f"DMA copy each way (d2h {peaks['d2h']:.0f}, "
+                                  f"h2d {peaks['h2d']:.0f} GB/s)",
+                     "algorithmic_bytes_per_launch": 2 * n * bb},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "e2e": {"value": round(moved / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": moved // 2,
+                "d2h_bytes_per_step": moved // 2},
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = swap_cpu_baseline(w, blocks, bb, args.cpu_budget)
+    return line
+
+
+def swap_cpu_baseline(w, blocks, bb, budget_s):
+    """The oracle's byte moves on host copies of the same pools and pairs."""
+    import oracle
+    k, v = w.k_cache.cpu(), w.v_cache.cpu()
+    ck = torch.empty((len(blocks),) + tuple(k.shape[1:]), dtype=k.dtype)
+    cv = torch.empty_like(ck)
+    out_pairs = [(b, i) for i, b in enumerate(blocks)]
+    in_pairs = [(i, b) for i, b in enumerate(blocks)]
+    reps, t = 0, time.perf_counter()
+    while time.perf_counter() - t < budget_s / 2 or reps == 0:
+        oracle.swap_blocks([k, v], [ck, cv], out_pairs)
+        oracle.swap_blocks([ck, cv], [k, v], in_pairs)
+        reps += 1
+    el = time.perf_counter() - t
+    return {"value": round(reps * 4 * len(blocks) * bb / el / 1e9, 2), "unit": "GB/s",
+            "cores": 1, "kind": "oracle",
+            "sample": f"C oracle memcpy, 1 thread: {reps} swap out + in rounds of "
+                      f"{len(blocks)} blocks x K, V, {el:.1f} s"}
+
+
 def run_ours(args, rank, world, local):
     import paged_kv_cache_119_gb300 as pa
     from paged_kv_cache_119_gb300 import build as pa_build
+
+    if args.config == "llama13b_swap":
+        return run_swap(args, rank, world, local)
 
     if world > 1:
         torch.distributed.init_process_group("nccl")
@@ -499,6 +684,8 @@ def measure_e2e(args, pa, w, out, ws, part, dev):
 def _host_inputs(w):
     h = {n: getattr(w, n).cpu() for n in ("q", "k_cache", "v_cache", "k_new", "v_new",
                                           "slot_mapping", "block_tables", "context_lens")}
+    if w.query_start is not None:
+        h["query_start"] = w.query_start.cpu()
     if w.fp8:
         h["k_scale"], h["v_scale"] = w.meta["k_scale"].cpu(), w.meta["v_scale"].cpu()
     return h
@@ -523,12 +710,57 @@ def _sample_bytes(w, seqs):
     return int(sum(w.context_lens.tolist()[:seqs])) * w.num_kv_heads * 2 * w.head_dim * esz
 
 
+def _chunk_rows(h, w, s, j0, j1, threads) -> int:
+    """The oracle on rows j0 .. j1-1 of sequence s's chunk (all heads), as a
+    one-sequence chunk ending at row j1-1's position.  Returns its attention flops."""
+    import oracle
+    qs = h["query_start"].tolist()
+    n, L = qs[s + 1] - qs[s], int(h["context_lens"][s])
+    oracle.chunk_attention(h["q"][qs[s] + j0:qs[s] + j1], h["k_cache"], h["v_cache"],
+                           h["block_tables"][s:s + 1],
+                           torch.tensor([L - n + j1], dtype=torch.int32),
+                           torch.tensor([0, j1 - j0], dtype=torch.int32), w.scale,
+                           w.num_kv_heads, w.block_size, num_threads=threads)
+    return 4 * w.head_dim * w.num_q_heads * sum(L - n + j + 1 for j in range(j0, j1))
+
+
+def _chunk_sample(w, h, budget_s, threads):
+    """(value, unit, description) of the oracle on a bounded leading sample of a
+    chunk workload, in the bench line's unit (KV GB/s or attention TFLOP/s)."""
+    qs = h["query_start"].tolist()
+    if CHUNK_METRIC.get(w.name, "").endswith("TFLOP/s"):
+        t = time.perf_counter()
+        flops = _chunk_rows(h, w, 0, 0, 1, threads)
+        per_row = max(time.perf_counter() - t, 1e-6)
+        rows = max(1, min(qs[1], int(budget_s / per_row)))
+        t = time.perf_counter()
+        flops = _chunk_rows(h, w, 0, 0, rows, threads)
+        el = time.perf_counter() - t
+        return (flops / el / 1e12, "TFLOP/s",
+                f"fp64 C oracle (OpenMP, {threads} threads): the first {rows} query rows of "
+                f"sequence 0's {qs[1]}-token chunk, all heads, {el:.1f} s")
+    seqs, el = 0, 0.0
+    t = time.perf_counter()
+    while seqs < w.num_seqs and el < budget_s:
+        _chunk_rows(h, w, seqs, 0, qs[seqs + 1] - qs[seqs], threads)
+        seqs += 1
+        el = time.perf_counter() - t
+    return (_sample_bytes(w, seqs) / el / 1e9, "GB/s",
+            f"fp64 C oracle (OpenMP, {threads} threads): the chunks of the first {seqs} of "
+            f"{w.num_seqs} sequences, all heads, {el:.1f} s")
+
+
 def cpu_baseline(w, budget_s: float) -> dict:
     """The oracle, as it stands, on the same workload: whole passes over the batch
     (decode of every sequence, all heads) repeated until about budget_s seconds of
     CPU work, or a leading slice of the batch when one pass would take longer."""
     import oracle
     h = _host_inputs(w)
+    if w.query_start is not None:
+        threads = oracle.max_threads()
+        value, unit, sample = _chunk_sample(w, h, budget_s, threads)
+        return {"value": round(value, 4), "unit": unit, "cores": threads, "kind": "oracle",
+                "sample": sample}
     threads = oracle.max_threads()
     # calibrate on the first 8 sequences, then size the sample to the budget
     t = time.perf_counter()
@@ -563,9 +795,50 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     import oracle
+    if args.config == "llama13b_swap":
+        w = make_workload("llama13b", "cpu", args.num_seqs)
+        blocks, bb = swap_plan(w, min(64, w.num_seqs))
+        for _ in range(args.warmup):
+            swap_cpu_baseline(w, blocks, bb, 0.0)
+        t = time.perf_counter()
+        vals = [swap_cpu_baseline(w, blocks, bb, 0.0) for _ in range(args.steps)]
+        sec = (time.perf_counter() - t) / args.steps
+        value = sum(v["value"] for v in vals) / len(vals)
+        return {"impl": "reference", "metric": SWAP_METRIC, "value": round(value, 2),
+                "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bytes", "data": "synthetic",
+                "config": {"workload": WORKLOADS[args.config], "name": args.config},
+                "cpu_baseline": dict(vals[-1], value=round(value, 2)),
+                "e2e": {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0},
+                "gpu_launches": 0}
     w = make_workload(args.config, "cpu", args.num_seqs)
     h = _host_inputs(w)
     threads = oracle.max_threads()
+    if w.query_start is not None:
+        # each step: the oracle on a bounded leading sample (about 0.5 s of work)
+        for _ in range(args.warmup):
+            _chunk_sample(w, h, 0.5, threads)
+        vals = []
+        t = time.perf_counter()
+        for _ in range(args.steps):
+            value, unit, sample = _chunk_sample(w, h, 0.5, threads)
+            vals.append(value)
+        sec = (time.perf_counter() - t) / args.steps
+        value = sum(vals) / len(vals)
+        return {"impl": "reference", "metric": CHUNK_METRIC[args.config],
+                "value": round(value, 4), "unit": unit, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic",
+                "config": {"workload": WORKLOADS[args.config], "name": args.config,
+                           "num_seqs": w.num_seqs},
+                "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": threads,
+                                 "kind": "oracle", "sample": sample},
+                "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0},
+                "gpu_launches": 0}
     # a bounded sample: enough sequences for ~0.5 s of oracle work per step
     seqs = max(1, min(w.num_seqs, 16))
     for _ in range(args.warmup):

@@ -183,6 +183,31 @@ int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_lay
                    int64_t num_blocks, void* stream);
 
 /*
+ * pa_swap_blocks: batched block moves between two pools that live in different
+ * memories -- swapping the KV blocks of a preempted sequence group out to a CPU
+ * pool and back in ("PagedAttention 完全拆解", section 调度与抢占：内存不够时怎么办,
+ * 换出 (Swapping); its Figure 19a shows per-block transfers leaving the link idle
+ * when blocks are small, so every pair and cache moves in one launch here).
+ *   src_caches, dst_caches  HOST arrays of num_caches pool base addresses (one per
+ *                       layer and per K / V); each pool is device memory or pinned
+ *                       host memory the device can address (cudaHostAlloc /
+ *                       cudaHostRegister); a cache's src and dst pools must not overlap
+ *   src_dst_pairs_host  HOST int64 [num_pairs][2]: (block id in src pool, block id in
+ *                       dst pool)
+ *   block_bytes         bytes of one block (a multiple of 16)
+ *   src_num_blocks, dst_num_blocks   pool sizes in blocks
+ * For every cache c and pair (s, d): dst_caches[c][d] = src_caches[c][s], byte for
+ * byte.  Validation (host): ids in range, destination ids pairwise distinct, pools
+ * 16-byte aligned, non-overlapping and device-addressable; otherwise a negative
+ * pa_status with nothing launched.  Launches one kernel per 64 caches x 1024 pairs;
+ * allocates nothing.  Whether a group is swapped out or in is the caller's choice of
+ * src and dst (the pages swap whole sequence groups, all-or-nothing).
+ */
+int pa_swap_blocks(void* const* src_caches, void* const* dst_caches, int32_t num_caches,
+                   const int64_t* src_dst_pairs_host, int64_t num_pairs, int64_t block_bytes,
+                   int64_t src_num_blocks, int64_t dst_num_blocks, void* stream);
+
+/*
  * FP8 KV cache (OCP E4M3: 4 exponent bits, bias 7, 3 fraction bits, largest finite
  * magnitude 448, no infinities).  A cache element is a one-byte code c; its value is
  * e4m3(c) * scale[h], with one fp32 scale per kv head for K (k_scale[Hkv]) and one

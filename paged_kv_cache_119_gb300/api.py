@@ -179,6 +179,47 @@ def pa_copy_blocks(k_caches, v_caches, src_dst_pairs, stream=None) -> None:
     N.check("pa_copy_blocks", status)
 
 
+def pa_swap_blocks(src_caches, dst_caches, src_dst_pairs, stream=None) -> None:
+    """Move whole blocks between two pools per cache: dst_caches[c][d] = src_caches[c][s]
+    for every (s, d) pair -- swapping a preempted sequence group out to a pinned host
+    pool (src on the GPU, dst pinned CPU tensors) or back in (the reverse).
+
+    src_caches, dst_caches: equal-length lists of contiguous tensors whose first dim is
+    the block id, each a CUDA tensor or a pinned CPU tensor (``pin_memory()``); every
+    block has the same byte size.  src_dst_pairs: host (s, d) int pairs.
+    """
+    if isinstance(src_caches, torch.Tensor):
+        src_caches, dst_caches = [src_caches], [dst_caches]
+    if len(src_caches) != len(dst_caches) or not src_caches:
+        raise ValueError("src_caches and dst_caches must be non-empty lists of equal length")
+
+    def block_bytes(t):
+        if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+            raise ValueError("caches must be contiguous tensors")
+        if t.device.type == "cpu" and not t.is_pinned():
+            raise ValueError("a host pool must be pinned (tensor.pin_memory())")
+        if t.device.type not in ("cpu", "cuda"):
+            raise ValueError("caches must be CUDA or pinned CPU tensors")
+        return t.numel() * t.element_size() // t.shape[0]
+
+    bb = block_bytes(src_caches[0])
+    for t in list(src_caches) + list(dst_caches):
+        if block_bytes(t) != bb:
+            raise ValueError("every pool must have the same block size in bytes")
+    ns, nd = src_caches[0].shape[0], dst_caches[0].shape[0]
+    if any(t.shape[0] != ns for t in src_caches) or any(t.shape[0] != nd for t in dst_caches):
+        raise ValueError("the source pools (and the destination pools) must have one size")
+    pairs = torch.as_tensor(src_dst_pairs, dtype=torch.int64).reshape(-1, 2).contiguous()
+    if pairs.device.type != "cpu":
+        raise ValueError("src_dst_pairs must live in host memory")
+    C = len(src_caches)
+    sp = (ctypes.c_void_p * C)(*[t.data_ptr() for t in src_caches])
+    dp = (ctypes.c_void_p * C)(*[t.data_ptr() for t in dst_caches])
+    pp = ctypes.cast(pairs.data_ptr(), ctypes.POINTER(ctypes.c_int64))
+    status = N.load().pa_swap_blocks(sp, dp, C, pp, pairs.shape[0], bb, ns, nd, _stream(stream))
+    N.check("pa_swap_blocks", status)
+
+
 def _fp8_cache(name: str, t: torch.Tensor) -> None:
     _cuda(name, t)
     if t.dtype not in (torch.float8_e4m3fn, torch.uint8):

@@ -10,6 +10,12 @@
 // many non-contiguous whole-block copies in one launch instead of one
 // cudaMemcpyAsync per block.  The (src, dst) pairs and per-layer pool pointers
 // travel in the kernel parameter block, so nothing is allocated or uploaded.
+//
+// swap_blocks (same page, section 调度与抢占, 换出 (Swapping); Figure 19a: many small
+// per-block transfers leave the link idle): the same gather between two pools in
+// different memories -- device and pinned host memory, which the GPU reads and
+// writes directly over NVLink-C2C -- so swapping a sequence group out or in is one
+// launch whatever its block count.
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -156,6 +162,43 @@ cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream)
         splits = 64;
     dim3 grid(p.num_pairs, 2 * p.num_layers, (unsigned)splits);
     copy_blocks_kernel<<<grid, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// grid = (pairs, caches, slices): CTA (p, c, s) moves the s-th slice of block
+// pairs[p].x of src[c] to block pairs[p].y of dst[c].  Four independent 16-byte
+// loads per thread are in flight before the stores, to cover the latency of the
+// host link.
+__global__ void __launch_bounds__(256) swap_blocks_kernel(const SwapParams p)
+{
+    const int pair = blockIdx.x;
+    const uint4* src = p.src[blockIdx.y] + (int64_t)p.pairs[pair].x * p.block_vecs;
+    uint4* dst = p.dst[blockIdx.y] + (int64_t)p.pairs[pair].y * p.block_vecs;
+    const int64_t slice = (p.block_vecs + gridDim.z - 1) / gridDim.z;
+    const int64_t lo = blockIdx.z * slice;
+    const int64_t hi = min(p.block_vecs, lo + slice);
+    int64_t i = lo + threadIdx.x;
+    for (; i + 3 * 256 < hi; i += 4 * 256) {
+        const uint4 a = src[i], b = src[i + 256], c = src[i + 512], d = src[i + 768];
+        dst[i] = a;
+        dst[i + 256] = b;
+        dst[i + 512] = c;
+        dst[i + 768] = d;
+    }
+    for (; i < hi; i += 256)
+        dst[i] = src[i];
+}
+
+cudaError_t launch_swap_blocks(const SwapParams& p, cudaStream_t stream)
+{
+    if (p.num_pairs == 0 || p.num_caches == 0)
+        return cudaSuccess;
+    // about 16 vectors per thread per CTA; large blocks are split across CTAs
+    int64_t splits = (p.block_vecs + 4095) / 4096;
+    if (splits > 64)
+        splits = 64;
+    dim3 grid(p.num_pairs, p.num_caches, (unsigned)splits);
+    swap_blocks_kernel<<<grid, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

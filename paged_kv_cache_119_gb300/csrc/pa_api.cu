@@ -760,6 +760,75 @@ int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_lay
     return PA_OK;
 }
 
+int pa_swap_blocks(void* const* src_caches, void* const* dst_caches, int32_t num_caches,
+                   const int64_t* src_dst_pairs_host, int64_t num_pairs, int64_t block_bytes,
+                   int64_t src_num_blocks, int64_t dst_num_blocks, void* stream)
+{
+    if (num_caches < 0 || num_pairs < 0 || block_bytes <= 0 || block_bytes % 16 != 0 ||
+        src_num_blocks <= 0 || src_num_blocks > INT32_MAX || dst_num_blocks <= 0 ||
+        dst_num_blocks > INT32_MAX)
+        return PA_ERR_INVALID;
+    if (num_caches == 0 || num_pairs == 0)
+        return PA_OK;
+    if (!src_caches || !dst_caches || !src_dst_pairs_host)
+        return PA_ERR_INVALID;
+    std::vector<int64_t> dst(num_pairs);
+    for (int64_t i = 0; i < num_pairs; ++i) {
+        const int64_t s = src_dst_pairs_host[2 * i], d = src_dst_pairs_host[2 * i + 1];
+        if (s < 0 || s >= src_num_blocks || d < 0 || d >= dst_num_blocks)
+            return PA_ERR_INVALID;
+        dst[i] = d;
+    }
+    std::sort(dst.begin(), dst.end());
+    if (std::adjacent_find(dst.begin(), dst.end()) != dst.end())
+        return PA_ERR_INVALID;                       // two pairs write one block
+    const size_t src_bytes = (size_t)src_num_blocks * block_bytes;
+    const size_t dst_bytes = (size_t)dst_num_blocks * block_bytes;
+    std::vector<const uint4*> srcp(num_caches);
+    std::vector<uint4*> dstp(num_caches);
+    for (int c = 0; c < num_caches; ++c) {
+        void* pools[2] = {src_caches[c], dst_caches[c]};
+        if (!pools[0] || !pools[1] || !aligned16(pools[0]) || !aligned16(pools[1]) ||
+            overlaps(pools[0], src_bytes, pools[1], dst_bytes))
+            return PA_ERR_INVALID;
+        void* dev[2] = {nullptr, nullptr};
+        for (int k = 0; k < 2; ++k) {
+            // device memory, or pinned host memory the device can address
+            cudaPointerAttributes a{};
+            if (cudaPointerGetAttributes(&a, pools[k]) != cudaSuccess) {
+                cudaGetLastError();
+                return PA_ERR_INVALID;
+            }
+            if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeHost &&
+                a.type != cudaMemoryTypeManaged)
+                return PA_ERR_INVALID;
+            dev[k] = a.devicePointer ? a.devicePointer : pools[k];
+        }
+        srcp[c] = static_cast<const uint4*>(dev[0]);
+        dstp[c] = static_cast<uint4*>(dev[1]);
+    }
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    SwapParams p{};
+    for (int c0 = 0; c0 < num_caches; c0 += kSwapMaxCaches) {
+        for (int64_t p0 = 0; p0 < num_pairs; p0 += kSwapMaxPairs) {
+            p.num_caches = std::min<int>(kSwapMaxCaches, num_caches - c0);
+            p.num_pairs = (int)std::min<int64_t>(kSwapMaxPairs, num_pairs - p0);
+            p.block_vecs = block_bytes / 16;
+            for (int c = 0; c < p.num_caches; ++c) {
+                p.src[c] = srcp[c0 + c];
+                p.dst[c] = dstp[c0 + c];
+            }
+            for (int i = 0; i < p.num_pairs; ++i)
+                p.pairs[i] = make_int2((int)src_dst_pairs_host[2 * (p0 + i)],
+                                       (int)src_dst_pairs_host[2 * (p0 + i) + 1]);
+            if (launch_swap_blocks(p, st) != cudaSuccess)
+                return PA_ERR_CUDA;
+        }
+    }
+    return PA_OK;
+}
+
 int pa_get_device_error(uint32_t* flags, void* stream)
 {
     if (!flags)

@@ -124,6 +124,21 @@ struct CopyParams {
 };
 cudaError_t launch_copy_blocks(const CopyParams& p, cudaStream_t stream);
 
+// Block moves between two pools of each cache (swapping to and from a pinned host
+// pool).  Up to kSwapMaxCaches caches and kSwapMaxPairs pairs per launch: about
+// 9 KB of kernel parameters (sm_70 and later take up to 32 KB).
+constexpr int kSwapMaxCaches = 64;
+constexpr int kSwapMaxPairs = 1024;
+struct SwapParams {
+    const uint4* src[kSwapMaxCaches];
+    uint4* dst[kSwapMaxCaches];
+    int2 pairs[kSwapMaxPairs];   // (source block, destination block)
+    int64_t block_vecs;          // 16-byte vectors per block
+    int num_caches;
+    int num_pairs;
+};
+cudaError_t launch_swap_blocks(const SwapParams& p, cudaStream_t stream);
+
 // Tensor map over a [num_blocks][num_kv_heads][block_size][head_dim] cache, as
 // 3-D (head_dim, block_size, num_blocks * num_kv_heads) with 128-byte swizzle and
 // a box of 128-byte rows x block_size tokens (64 dims of a 16-bit dtype, or 128

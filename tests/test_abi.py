@@ -219,3 +219,33 @@ def test_partition_queries_for_explicit_sizes(lib):
         == N.PA_ERR_INVALID
     assert lib.pa_chunk_partition_tokens(N.PA_BF16, 8, 6, 4, 128, 16, 512, 32768, 0) \
         == N.PA_ERR_INVALID
+
+
+def _swap(lib, pairs, block_bytes=64, ns=4, nd=6, caches=2):
+    arr = (ctypes.c_int64 * (2 * len(pairs)))(*[x for pr in pairs for x in pr])
+    src = (ctypes.c_void_p * caches)(*[FAKE * (i + 1) for i in range(caches)])
+    dst = (ctypes.c_void_p * caches)(*[FAKE * (i + 8) for i in range(caches)])
+    return lib.pa_swap_blocks(src, dst, caches, arr, len(pairs), block_bytes, ns, nd, None)
+
+
+@pytest.mark.parametrize("pairs", [[(4, 0)], [(0, 6)], [(-1, 0)], [(0, 1), (2, 1)]])
+def test_swap_blocks_rejects_bad_pairs(lib, pairs):
+    assert _swap(lib, pairs) == N.PA_ERR_INVALID
+
+
+def test_swap_blocks_rejects_bad_sizes_and_empty_is_a_no_op(lib):
+    assert _swap(lib, [(0, 1)], block_bytes=24) == N.PA_ERR_INVALID
+    assert _swap(lib, [(0, 1)], ns=0) == N.PA_ERR_INVALID
+    assert _swap(lib, []) == N.PA_OK
+    assert _swap(lib, [(0, 1)], caches=0) == N.PA_OK
+
+
+def test_swap_blocks_rejects_host_memory_that_is_not_pinned(lib):
+    """A pageable host buffer is not device-addressable: refused before any launch."""
+    import numpy as np
+    a = np.zeros(4 * 64, dtype=np.uint8)
+    b = np.zeros(6 * 64, dtype=np.uint8)
+    src = (ctypes.c_void_p * 1)(a.ctypes.data)
+    dst = (ctypes.c_void_p * 1)(b.ctypes.data)
+    arr = (ctypes.c_int64 * 2)(0, 1)
+    assert lib.pa_swap_blocks(src, dst, 1, arr, 1, 64, 4, 6, None) == N.PA_ERR_INVALID
