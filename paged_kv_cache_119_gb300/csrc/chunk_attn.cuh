@@ -18,10 +18,11 @@
 //                                              A operand read from tensor memory)
 //   * warp 0 (producer): block-table entries and tensor-map TMA of the tile's K
 //     and V boxes (64 dims x B tokens, 128-byte swizzle) into an mbarrier ring;
-//   * warp 1: allocates all 512 tensor-memory columns and (one thread) issues the
-//     MMAs: the scores of the next tile for both query tiles go out before P.V of
-//     the current one, into second S buffers, so the tensor core keeps busy while
-//     the softmax warps work;
+//   * warps 1 and 10: one thread each issues the MMAs of one query tile (warp 1 also
+//     allocates all 512 tensor-memory columns): the scores of the next tile go out
+//     before P.V of the current one, into a second S buffer.  Each issuer waits only
+//     on its own query tile's completions, so the tensor core takes work from the
+//     other while one waits;
 //   * warps 2-5 (query tile 0) and 6-9 (query tile 1), one thread per row = TMEM
 //     lane: read S, mask (causal within the chunk, end of context), online softmax
 //     in base 2, write P back over the S buffer it came from (packed 16-bit pairs),
@@ -55,7 +56,9 @@ constexpr int kChunkQTiles = 2;      // 128-row query tiles per CTA
 constexpr int kChunkRows = 128;      // M of the tensor-core tile
 constexpr int kChunkTileTok = 64;    // tokens per K/V tile (N of the score product)
 constexpr int kChunkSoftmaxWarps = 4 * kChunkQTiles;
-constexpr int kChunkThreads = 64 + 32 * kChunkSoftmaxWarps;   // producer, MMA, softmax
+// warps: 0 producer, 1 tensor-memory allocator + MMA issuer of query tile 0, 2-9
+// softmax, 10 MMA issuer of query tile 1
+constexpr int kChunkThreads = 64 + 32 * kChunkSoftmaxWarps + 32;
 
 template <int D, int NST>
 struct ChunkSmem {
@@ -68,8 +71,9 @@ struct ChunkSmem {
     static constexpr int kQOff = 0;
     static constexpr int kStageOff = kQOff + kChunkQTiles * kQTile;
     static constexpr int kBarOff = kStageOff + NST * kStageBytes;
-    // full[NST], empty[NST], s_full[2][2], p_full[2][2], pv_done[2], q_full, mma_done
-    static constexpr int kNumBars = 2 * NST + 12;
+    // full[NST], empty[NST], s_full[2][2], p_full[2][2], pv_done[2], q_full, mma_done[2],
+    // v_zero
+    static constexpr int kNumBars = 2 * NST + 14;
     static constexpr int kOkOff = kBarOff + 8 * kNumBars;        // stage_ok[NST]
     static constexpr int kSlotOff = kOkOff + 4 * NST;            // TMEM address
     static constexpr int kBytes = kSlotOff + 16;
@@ -176,7 +180,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     uint64_t* p_full = s_full + 4;               // [query tile][S/P buffer]
     uint64_t* pv_done = p_full + 4;              // [query tile]
     uint64_t* q_full = pv_done + 2;
-    uint64_t* mma_done = q_full + 1;
+    uint64_t* mma_done = q_full + 1;             // [query tile]
+    uint64_t* v_zero = mma_done + 2;             // the last tile's V rows past the range are 0
     int* stage_ok = reinterpret_cast<int*>(smem + Sm::kOkOff);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Sm::kSlotOff);
 
@@ -235,7 +240,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
 #pragma unroll
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], kChunkQTiles);          // one commit per issuer
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -243,10 +248,12 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             mbar_init(&p_full[i], 4);
         }
 #pragma unroll
-        for (int q = 0; q < kChunkQTiles; ++q)
+        for (int q = 0; q < kChunkQTiles; ++q) {
             mbar_init(&pv_done[q], 1);
+            mbar_init(&mma_done[q], 1);
+        }
         mbar_init(q_full, kChunkSoftmaxWarps);
-        mbar_init(mma_done, 1);
+        mbar_init(v_zero, kChunkSoftmaxWarps);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -311,29 +318,26 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             for (int it = max(0, issued - NST); it < issued; ++it)
                 mbar_wait(&full[it % NST], (it / NST) & 1);
         __syncwarp();
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issue
+    } else if (warp == 1 || warp == 2 + kChunkSoftmaxWarps) {
+        // ------------------------------------------- MMA issue, one query tile per warp
+        const int q = warp == 1 ? 0 : 1;
         if (lane == 0) {
-            const uint32_t sq = smem_addr(smem + Sm::kQOff);
+            const uint32_t sq = smem_addr(smem + Sm::kQOff + q * Sm::kQTile);
             const uint32_t idesc_s = mma_idesc_f16(kBf16, kChunkRows, NT, false);
             const uint32_t idesc_o = mma_idesc_f16(kBf16, kChunkRows, D, true);
             bool ok = mbar_wait(q_full, 0);
-            // S_q of tile it for both query tiles, into S buffer it & 1
+            // S of tile it into this query tile's S buffer it & 1
             auto issue_scores = [&](int it) {
                 const uint32_t kb = smem_addr(smem + Sm::kStageOff + (it % NST) * Sm::kStageBytes);
+                const uint32_t dcol = tbase + Sm::kSCol + q * 128 + (it & 1) * NT;
 #pragma unroll
-                for (int q = 0; q < kChunkQTiles; ++q) {
-                    const uint32_t dcol = tbase + Sm::kSCol + q * 128 + (it & 1) * NT;
-#pragma unroll
-                    for (int kk = 0; kk < KS; ++kk) {
-                        const uint64_t a = sw128_desc(
-                            sq + q * Sm::kQTile + (kk / 4) * Sm::kQHalf + (kk % 4) * 32, 16, 1024);
-                        const uint64_t b =
-                            sw128_desc(kb + (kk / 4) * Sm::kKVHalf + (kk % 4) * 32, 16, 1024);
-                        tc_mma_f16(dcol, a, b, idesc_s, kk > 0 ? 1u : 0u);
-                    }
-                    tc_commit(&s_full[q * 2 + (it & 1)]);
+                for (int kk = 0; kk < KS; ++kk) {
+                    const uint64_t a = sw128_desc(sq + (kk / 4) * Sm::kQHalf + (kk % 4) * 32, 16, 1024);
+                    const uint64_t b =
+                        sw128_desc(kb + (kk / 4) * Sm::kKVHalf + (kk % 4) * 32, 16, 1024);
+                    tc_mma_f16(dcol, a, b, idesc_s, kk > 0 ? 1u : 0u);
                 }
+                tc_commit(&s_full[q * 2 + (it & 1)]);
             };
             if (ok)
                 ok = mbar_wait(&full[0], 0);
@@ -344,40 +348,38 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             for (int it = 0; it < ntiles && ok; ++it) {
                 if (it + 1 < ntiles) {
                     ok = mbar_wait(&full[(it + 1) % NST], ((it + 1) / NST) & 1);
-                    // S/P buffers (it+1)&1 hold P of tile it-1 until its P.V completes
-                    for (int q = 0; q < kChunkQTiles && ok && it >= 1; ++q)
+                    // S/P buffer (it+1)&1 holds P of tile it-1 until its P.V completes
+                    if (ok && it >= 1)
                         ok = mbar_wait(&pv_done[q], (it - 1) & 1);
                     if (!ok)
                         break;
                     tc_fence_after();
                     issue_scores(it + 1);
                 }
+                ok = mbar_wait(&p_full[q * 2 + (it & 1)], (it >> 1) & 1);
+                if (ok && t0 + (it + 1) * NT > t1)
+                    ok = mbar_wait(v_zero, 0);       // last tile: V rows past the range zeroed
+                if (!ok)
+                    break;
+                tc_fence_after();
                 const uint32_t vb =
                     smem_addr(smem + Sm::kStageOff + (it % NST) * Sm::kStageBytes + Sm::kKBytes);
-#pragma unroll 1
-                for (int q = 0; q < kChunkQTiles && ok; ++q) {
-                    ok = mbar_wait(&p_full[q * 2 + (it & 1)], (it >> 1) & 1);
-                    if (!ok)
-                        break;
-                    tc_fence_after();
-                    const uint32_t pcol = tbase + Sm::kSCol + q * 128 + (it & 1) * NT;
+                const uint32_t pcol = tbase + Sm::kSCol + q * 128 + (it & 1) * NT;
 #pragma unroll
-                    for (int half = 0; half < 2; ++half)          // hi, then lo
+                for (int half = 0; half < 2; ++half)          // hi, then lo
 #pragma unroll
-                        for (int kk = 0; kk < NT / 16; ++kk) {
-                            const uint64_t b = sw128_desc(vb + kk * 16 * 128, Sm::kKVHalf, 1024);
-                            tc_mma_f16_ts(tbase + q * 128, pcol + half * (NT / 2) + kk * 8, b, idesc_o,
-                                          (it > 0 || half > 0 || kk > 0) ? 1u : 0u);
-                        }
-                    tc_commit(&pv_done[q]);
-                }
-                if (ok)
-                    tc_commit(&empty[it % NST]);
+                    for (int kk = 0; kk < NT / 16; ++kk) {
+                        const uint64_t b = sw128_desc(vb + kk * 16 * 128, Sm::kKVHalf, 1024);
+                        tc_mma_f16_ts(tbase + q * 128, pcol + half * (NT / 2) + kk * 8, b, idesc_o,
+                                      (it > 0 || half > 0 || kk > 0) ? 1u : 0u);
+                    }
+                tc_commit(&pv_done[q]);
+                tc_commit(&empty[it % NST]);
             }
             if (!ok)
                 atomicOr(p.err, PA_DEVERR_TIMEOUT);
-            tc_commit(mma_done);              // every MMA above completes before TMEM is freed
-            mbar_wait(mma_done, 0);
+            tc_commit(&mma_done[q]);          // every MMA above completes before TMEM is freed
+            mbar_wait(&mma_done[q], 0);
         }
         __syncwarp();
     } else {
@@ -514,20 +516,24 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 tmem_st32_raw(sp_col, hi);
                 tmem_st32_raw(sp_col + NT / 2, lo);
             }
-            if (q == 0 && tb + NT > t1) {
+            if (tb + NT > t1) {
                 // V rows past the range may hold anything (unused slots, stale tiles):
-                // zero them so that 0 * V stays 0.  Query tile 0's warps do it before
-                // their P is published; P.V of query tile 1 is issued after that of
-                // query tile 0.
+                // zero them so that 0 * V stays 0; both issuers wait for v_zero before
+                // their last P.V
                 const int v0 = t1 - tb;
                 const int rows = NT - v0;
                 unsigned char* vbase = smem + Sm::kStageOff + st * Sm::kStageBytes + Sm::kKBytes;
-                for (int idx = rr; idx < Sm::kHalves * rows * 8; idx += kChunkRows) {
+                for (int idx = threadIdx.x - 64; idx < Sm::kHalves * rows * 8;
+                     idx += 32 * kChunkSoftmaxWarps) {
                     const int h = idx / (rows * 8);
                     const int w = idx - h * rows * 8;
                     *reinterpret_cast<uint4*>(vbase + h * Sm::kKVHalf + (v0 + w / 8) * 128 +
                                               (w % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(v_zero);
             }
             fence_proxy_async_smem();
             tc_fence_before();
