@@ -82,6 +82,39 @@ int32_t pa_bm_ref_count(const pa_block_manager* bm, int32_t block);
 /* Token count of a sequence, or -1 if unknown. */
 int32_t pa_bm_num_tokens(const pa_block_manager* bm, int64_t seq_id);
 
+/*
+ * Swapping ("PagedAttention 完全拆解", section 调度与抢占：内存不够时怎么办, 换出
+ * (Swapping)): a preempted sequence group moves to CPU memory as a whole and comes
+ * back as a whole; the pages' workers keep a CPU block allocator beside the GPU one.
+ *
+ * pa_bm_set_cpu_pool: gives the manager a CPU pool of num_cpu_blocks block ids
+ * (0 .. num_cpu_blocks-1, handed out first-in first-out).  Once, before swapping.
+ *
+ * pa_bm_swap_out: every distinct GPU block of the listed sequences (in order of first
+ * appearance) gets one CPU block; pairs_out (HOST, room for max_pairs pairs) receives
+ * (gpu block, cpu block) pairs -- the pairs pa_swap_blocks takes to copy the GPU pools
+ * into the CPU pools -- and *num_pairs their count.  Blocks the group shares stay
+ * shared on the CPU (one copy, the group's references counted on it); the group's
+ * references leave the GPU blocks, which return to the free list when no other
+ * sequence names them.  The sequences are then swapped out: pa_bm_append, pa_bm_fork
+ * and pa_bm_block_tables refuse them; pa_bm_free releases their CPU blocks.
+ * pa_bm_swap_in: the reverse, with (cpu block, gpu block) pairs for pa_swap_blocks
+ * from the CPU pools into the GPU pools; sharing is preserved again.
+ * Both are all-or-nothing: PA_ERR_INVALID with nothing changed if no CPU pool was set,
+ * a sequence is unknown, listed twice or already on the target side, the target pool
+ * has too few free blocks, or the pairs do not fit in max_pairs.
+ */
+int pa_bm_set_cpu_pool(pa_block_manager* bm, int32_t num_cpu_blocks);
+int pa_bm_swap_out(pa_block_manager* bm, const int64_t* seq_ids, int32_t n, int64_t* pairs_out,
+                   int32_t max_pairs, int32_t* num_pairs);
+int pa_bm_swap_in(pa_block_manager* bm, const int64_t* seq_ids, int32_t n, int64_t* pairs_out,
+                  int32_t max_pairs, int32_t* num_pairs);
+int32_t pa_bm_num_free_cpu_blocks(const pa_block_manager* bm);
+/* Reference count of a CPU block (0 = free), or -1 for an invalid id. */
+int32_t pa_bm_cpu_ref_count(const pa_block_manager* bm, int32_t block);
+/* 1 if the sequence is swapped out, 0 if on the GPU, -1 if unknown. */
+int32_t pa_bm_is_swapped(const pa_block_manager* bm, int64_t seq_id);
+
 #ifdef __cplusplus
 }
 #endif

@@ -13,7 +13,10 @@ sections 原理详解（一） (Figure 6), 内存共享 / 引用计数 (Figure 8
     records a (old, new) copy, and moves the writer onto the new block;
   * free uncounts each block; a block whose count reaches zero is free again.
 
-The free list hands blocks out first-in first-out.  Pinned by
+  * swapping (section 调度与抢占：内存不够时怎么办, 换出): a sequence group moves to a
+    CPU pool as a whole -- each distinct block once, sharing kept -- and back.
+
+The free lists hand blocks out first-in first-out.  Pinned by
 tests/test_block_manager.py against Figures 6, 8 and 9.
 """
 from __future__ import annotations
@@ -34,6 +37,9 @@ class BlockManagerModel:
         self.refs = [0] * num_blocks
         self.tables: dict[int, list[int]] = {}
         self.tokens: dict[int, int] = {}
+        self.cpu_free: deque = deque()
+        self.cpu_refs: list[int] = []
+        self.on_cpu: set = set()
 
     def _take(self) -> int:
         if not self.free:
@@ -55,7 +61,7 @@ class BlockManagerModel:
         return [self._slot(seq, t) for t in range(num_tokens)]
 
     def fork(self, parent: int, child: int) -> None:
-        assert child not in self.tables and parent in self.tables
+        assert child not in self.tables and parent in self.tables and parent not in self.on_cpu
         self.tables[child] = list(self.tables[parent])
         self.tokens[child] = self.tokens[parent]
         for b in self.tables[child]:
@@ -63,7 +69,7 @@ class BlockManagerModel:
 
     def append(self, seqs) -> tuple[list[int], list[tuple[int, int]]]:
         """One new token for each listed sequence, in order.  All or nothing."""
-        assert len(set(seqs)) == len(seqs)
+        assert len(set(seqs)) == len(seqs) and not set(seqs) & self.on_cpu
         snapshot = (deque(self.free), list(self.refs),
                     {s: list(t) for s, t in self.tables.items()}, dict(self.tokens))
         try:
@@ -87,8 +93,51 @@ class BlockManagerModel:
             raise
 
     def free_sequence(self, seq: int) -> None:
+        cpu = seq in self.on_cpu
+        refs, free = (self.cpu_refs, self.cpu_free) if cpu else (self.refs, self.free)
         for b in self.tables.pop(seq):
-            self.refs[b] -= 1
-            if self.refs[b] == 0:
-                self.free.append(b)
+            refs[b] -= 1
+            if refs[b] == 0:
+                free.append(b)
         del self.tokens[seq]
+        self.on_cpu.discard(seq)
+
+    def set_cpu_pool(self, num_cpu_blocks: int) -> None:
+        assert not self.cpu_refs and num_cpu_blocks > 0
+        self.cpu_refs = [0] * num_cpu_blocks
+        self.cpu_free = deque(range(num_cpu_blocks))
+
+    def _swap(self, seqs, to_cpu: bool) -> list[tuple[int, int]]:
+        assert self.cpu_refs and len(set(seqs)) == len(seqs)
+        assert all((s in self.on_cpu) != to_cpu for s in seqs)
+        order, uses = [], {}
+        for s in seqs:
+            for b in self.tables[s]:
+                if b not in uses:
+                    order.append(b)
+                uses[b] = uses.get(b, 0) + 1
+        src_refs, src_free = (self.refs, self.free) if to_cpu else (self.cpu_refs, self.cpu_free)
+        dst_refs, dst_free = (self.cpu_refs, self.cpu_free) if to_cpu else (self.refs, self.free)
+        if len(order) > len(dst_free):
+            raise PoolExhausted()
+        moved = {}
+        for b in order:
+            d = dst_free.popleft()
+            dst_refs[d] = uses[b]
+            src_refs[b] -= uses[b]
+            if src_refs[b] == 0:
+                src_free.append(b)
+            moved[b] = d
+        for s in seqs:
+            self.tables[s] = [moved[b] for b in self.tables[s]]
+            if to_cpu:
+                self.on_cpu.add(s)
+            else:
+                self.on_cpu.discard(s)
+        return [(b, moved[b]) for b in order]
+
+    def swap_out(self, seqs) -> list[tuple[int, int]]:
+        return self._swap(seqs, True)
+
+    def swap_in(self, seqs) -> list[tuple[int, int]]:
+        return self._swap(seqs, False)

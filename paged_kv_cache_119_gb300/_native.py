@@ -59,6 +59,14 @@ SIGNATURES = {
     "pa_bm_num_free_blocks": (_i32, [_vp]),
     "pa_bm_ref_count": (_i32, [_vp, _i32]),
     "pa_bm_num_tokens": (_i32, [_vp, _i64]),
+    "pa_bm_set_cpu_pool": (ctypes.c_int, [_vp, _i32]),
+    "pa_bm_swap_out": (ctypes.c_int, [_vp, ctypes.POINTER(_i64), _i32, ctypes.POINTER(_i64), _i32,
+                                      ctypes.POINTER(_i32)]),
+    "pa_bm_swap_in": (ctypes.c_int, [_vp, ctypes.POINTER(_i64), _i32, ctypes.POINTER(_i64), _i32,
+                                     ctypes.POINTER(_i32)]),
+    "pa_bm_num_free_cpu_blocks": (_i32, [_vp]),
+    "pa_bm_cpu_ref_count": (_i32, [_vp, _i32]),
+    "pa_bm_is_swapped": (_i32, [_vp, _i64]),
     "pa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pa_version": (ctypes.c_char_p, []),
 }

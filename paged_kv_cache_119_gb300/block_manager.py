@@ -77,3 +77,42 @@ class BlockManager:
 
     def num_tokens(self, seq_id: int) -> int:
         return int(self._lib.pa_bm_num_tokens(self._h, seq_id))
+
+    # -------------------------------------------------------------------- swapping
+    def set_cpu_pool(self, num_cpu_blocks: int) -> None:
+        """A CPU pool of ``num_cpu_blocks`` blocks for swapped-out sequence groups."""
+        N.check("pa_bm_set_cpu_pool", self._lib.pa_bm_set_cpu_pool(self._h, num_cpu_blocks))
+        self.num_cpu_blocks = num_cpu_blocks
+
+    def _swap(self, fn, seq_ids) -> np.ndarray:
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = ids.shape[0]
+        cap = max(1, max(self.num_blocks, getattr(self, "num_cpu_blocks", 0)))
+        pairs = np.zeros(2 * cap, dtype=np.int64)
+        npairs = ctypes.c_int32(0)
+        i64 = ctypes.POINTER(ctypes.c_int64)
+        N.check(fn, getattr(self._lib, fn)(self._h, ids.ctypes.data_as(i64), n,
+                                            pairs.ctypes.data_as(i64), cap, ctypes.byref(npairs)))
+        return pairs[:2 * npairs.value].reshape(-1, 2)
+
+    def swap_out(self, seq_ids) -> np.ndarray:
+        """Moves a sequence group to the CPU pool; returns (gpu block, cpu block) pairs
+        for pa_swap_blocks (GPU pools -> CPU pools)."""
+        return self._swap("pa_bm_swap_out", seq_ids)
+
+    def swap_in(self, seq_ids) -> np.ndarray:
+        """Brings a swapped-out group back; returns (cpu block, gpu block) pairs for
+        pa_swap_blocks (CPU pools -> GPU pools)."""
+        return self._swap("pa_bm_swap_in", seq_ids)
+
+    def num_free_cpu_blocks(self) -> int:
+        return int(self._lib.pa_bm_num_free_cpu_blocks(self._h))
+
+    def cpu_ref_count(self, block: int) -> int:
+        return int(self._lib.pa_bm_cpu_ref_count(self._h, block))
+
+    def is_swapped(self, seq_id: int) -> bool:
+        r = int(self._lib.pa_bm_is_swapped(self._h, seq_id))
+        if r < 0:
+            raise KeyError(seq_id)
+        return bool(r)

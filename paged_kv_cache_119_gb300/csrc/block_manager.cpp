@@ -2,7 +2,9 @@
 //
 // Reference counts, a first-in first-out free list, and the three primitives of
 // "PagedAttention 完全拆解" section 三种原语：fork、append、free, with copy-on-write
-// on append to a shared partially filled block (section 内存共享, Figure 8).
+// on append to a shared partially filled block (section 内存共享, Figure 8); and a
+// CPU block pool for swapping whole sequence groups out and back in (section 调度与
+// 抢占：内存不够时怎么办, 换出 (Swapping): all-or-nothing per group).
 #include <cstdint>
 #include <deque>
 #include <new>
@@ -14,14 +16,18 @@
 
 struct pa_block_manager {
     struct Seq {
-        std::vector<int32_t> blocks;
+        std::vector<int32_t> blocks;   // GPU block ids, or CPU block ids while swapped out
         int32_t tokens = 0;
+        bool on_cpu = false;
     };
     int32_t num_blocks = 0;
     int32_t block_size = 0;
     std::deque<int32_t> free_list;
     std::vector<int32_t> refs;
     std::unordered_map<int64_t, Seq> seqs;
+    // CPU pool for swapped-out groups (empty until pa_bm_set_cpu_pool)
+    std::deque<int32_t> cpu_free;
+    std::vector<int32_t> cpu_refs;
 
     int64_t slot(const Seq& s, int32_t t) const
     {
@@ -96,7 +102,7 @@ int pa_bm_fork(pa_block_manager* bm, int64_t parent_id, int64_t child_id)
     if (!bm || parent_id == child_id || bm->seqs.count(child_id))
         return PA_ERR_INVALID;
     auto it = bm->seqs.find(parent_id);
-    if (it == bm->seqs.end())
+    if (it == bm->seqs.end() || it->second.on_cpu)
         return PA_ERR_INVALID;
     pa_block_manager::Seq child = it->second;
     for (int32_t b : child.blocks)
@@ -117,7 +123,7 @@ int pa_bm_append(pa_block_manager* bm, const int64_t* seq_ids, int32_t n, int64_
     int32_t need = 0;
     for (int32_t i = 0; i < n; ++i) {
         auto it = bm->seqs.find(seq_ids[i]);
-        if (it == bm->seqs.end() || !listed.insert(seq_ids[i]).second)
+        if (it == bm->seqs.end() || it->second.on_cpu || !listed.insert(seq_ids[i]).second)
             return PA_ERR_INVALID;
         const auto& s = it->second;
         if (s.tokens % bm->block_size == 0) {
@@ -162,8 +168,12 @@ int pa_bm_free(pa_block_manager* bm, int64_t seq_id)
     auto it = bm->seqs.find(seq_id);
     if (it == bm->seqs.end())
         return PA_ERR_INVALID;
-    for (int32_t b : it->second.blocks)
-        bm->drop(b);
+    for (int32_t b : it->second.blocks) {
+        if (!it->second.on_cpu)
+            bm->drop(b);
+        else if (--bm->cpu_refs[b] == 0)
+            bm->cpu_free.push_back(b);
+    }
     bm->seqs.erase(it);
     return PA_OK;
 }
@@ -175,7 +185,7 @@ int pa_bm_block_tables(const pa_block_manager* bm, const int64_t* seq_ids, int32
         return PA_ERR_INVALID;
     for (int32_t i = 0; i < n; ++i) {
         auto it = bm->seqs.find(seq_ids[i]);
-        if (it == bm->seqs.end() || it->second.blocks.size() > (size_t)stride)
+        if (it == bm->seqs.end() || it->second.on_cpu || it->second.blocks.size() > (size_t)stride)
             return PA_ERR_INVALID;
     }
     for (int32_t i = 0; i < n; ++i) {
@@ -186,6 +196,101 @@ int pa_bm_block_tables(const pa_block_manager* bm, const int64_t* seq_ids, int32
         context_lens_out[i] = s.tokens;
     }
     return PA_OK;
+}
+
+int pa_bm_set_cpu_pool(pa_block_manager* bm, int32_t num_cpu_blocks)
+{
+    if (!bm || num_cpu_blocks <= 0 || !bm->cpu_refs.empty())
+        return PA_ERR_INVALID;
+    bm->cpu_refs.assign(num_cpu_blocks, 0);
+    for (int32_t i = 0; i < num_cpu_blocks; ++i)
+        bm->cpu_free.push_back(i);
+    return PA_OK;
+}
+
+namespace {
+
+// Moves a group's blocks between the pools: every distinct block of the listed
+// sequences (first appearance order) gets one block of the other pool, a (from, to)
+// pair is recorded, and the group's references move across.  to_cpu: GPU -> CPU.
+int swap_group(pa_block_manager* bm, const int64_t* seq_ids, int32_t n, int64_t* pairs_out,
+               int32_t max_pairs, int32_t* num_pairs, bool to_cpu)
+{
+    if (!bm || n < 0 || (n > 0 && (!seq_ids || !pairs_out)) || !num_pairs || bm->cpu_refs.empty())
+        return PA_ERR_INVALID;
+    std::unordered_set<int64_t> listed;
+    std::vector<int32_t> order;                          // distinct source blocks
+    std::unordered_map<int32_t, int32_t> uses;           // source block -> group references
+    for (int32_t i = 0; i < n; ++i) {
+        auto it = bm->seqs.find(seq_ids[i]);
+        if (it == bm->seqs.end() || it->second.on_cpu != !to_cpu || !listed.insert(seq_ids[i]).second)
+            return PA_ERR_INVALID;
+        for (int32_t b : it->second.blocks)
+            if (uses[b]++ == 0)
+                order.push_back(b);
+    }
+    std::deque<int32_t>& dst_free = to_cpu ? bm->cpu_free : bm->free_list;
+    if (order.size() > dst_free.size() || (int64_t)order.size() > max_pairs)
+        return PA_ERR_INVALID;                           // all or nothing
+    std::vector<int32_t>& src_refs = to_cpu ? bm->refs : bm->cpu_refs;
+    std::vector<int32_t>& dst_refs = to_cpu ? bm->cpu_refs : bm->refs;
+    std::deque<int32_t>& src_free = to_cpu ? bm->free_list : bm->cpu_free;
+    std::unordered_map<int32_t, int32_t> moved;          // source block -> destination block
+    int32_t k = 0;
+    for (int32_t b : order) {
+        const int32_t d = dst_free.front();
+        dst_free.pop_front();
+        dst_refs[d] = uses[b];
+        src_refs[b] -= uses[b];
+        if (src_refs[b] == 0)
+            src_free.push_back(b);
+        moved[b] = d;
+        pairs_out[2 * k] = b;
+        pairs_out[2 * k + 1] = d;
+        ++k;
+    }
+    for (int32_t i = 0; i < n; ++i) {
+        auto& s = bm->seqs[seq_ids[i]];
+        for (int32_t& b : s.blocks)
+            b = moved[b];
+        s.on_cpu = to_cpu;
+    }
+    *num_pairs = k;
+    return PA_OK;
+}
+
+}  // namespace
+
+int pa_bm_swap_out(pa_block_manager* bm, const int64_t* seq_ids, int32_t n, int64_t* pairs_out,
+                   int32_t max_pairs, int32_t* num_pairs)
+{
+    return swap_group(bm, seq_ids, n, pairs_out, max_pairs, num_pairs, true);
+}
+
+int pa_bm_swap_in(pa_block_manager* bm, const int64_t* seq_ids, int32_t n, int64_t* pairs_out,
+                  int32_t max_pairs, int32_t* num_pairs)
+{
+    return swap_group(bm, seq_ids, n, pairs_out, max_pairs, num_pairs, false);
+}
+
+int32_t pa_bm_num_free_cpu_blocks(const pa_block_manager* bm)
+{
+    return bm ? (int32_t)bm->cpu_free.size() : -1;
+}
+
+int32_t pa_bm_cpu_ref_count(const pa_block_manager* bm, int32_t block)
+{
+    if (!bm || block < 0 || block >= (int32_t)bm->cpu_refs.size())
+        return -1;
+    return bm->cpu_refs[block];
+}
+
+int32_t pa_bm_is_swapped(const pa_block_manager* bm, int64_t seq_id)
+{
+    if (!bm)
+        return -1;
+    auto it = bm->seqs.find(seq_id);
+    return it == bm->seqs.end() ? -1 : (it->second.on_cpu ? 1 : 0);
 }
 
 int32_t pa_bm_num_free_blocks(const pa_block_manager* bm)

@@ -233,3 +233,152 @@ def test_exhausted_pool_changes_nothing():
         m.append([0, 0])                   # a sequence listed twice
     with pytest.raises(ValueError):
         BlockManager(4, 4, [0, 1, 1, 2])   # not a permutation
+
+
+# --------------------------------------------------------------------------- swapping
+
+def sharing_pattern(tables):
+    """Which (sequence, logical block) positions name the same physical block --
+    the structure swapping must preserve, whatever the ids."""
+    first = {}
+    out = {}
+    for s in sorted(tables):
+        for j, b in enumerate(tables[s]):
+            out[(s, j)] = first.setdefault(b, (s, j))
+    return out
+
+
+def test_beam_group_swaps_out_and_back_keeping_its_sharing():
+    """A beam group (Figure 9's sharing: a prefix shared by all, blocks shared by pairs)
+    is preempted all-or-nothing ("调度与抢占", 换出): each distinct block goes to the CPU
+    once, the references follow, the GPU blocks are free again; swapped back in, the
+    group has the same sharing over new GPU blocks and decodes on."""
+    m = BlockManager(24, 4)
+    m.set_cpu_pool(24)
+    m.add_sequence(0, 10)                      # blocks 0, 1, 2 (2 tokens in the last)
+    for c in (1, 2, 3):
+        m.fork(0, c)
+    m.append([0, 1, 2, 3])                     # CoW of the shared partial last block
+    for _ in range(4):
+        m.append([0, 1, 2, 3])
+    group = [0, 1, 2, 3]
+    before = {s: [int(x) for x in m.block_tables([s], 16)[0][0] if x >= 0] for s in group}
+    distinct = {b for t in before.values() for b in t}
+    refs_before = {b: m.ref_count(b) for b in distinct}
+    free_before = m.num_free_blocks()
+    pairs = m.swap_out(group)
+    assert sorted(int(g) for g, _ in pairs) == sorted(distinct)           # each block once
+    assert len({int(c) for _, c in pairs}) == len(pairs)
+    assert m.num_free_blocks() == free_before + len(distinct)
+    for g, c in pairs:
+        assert m.cpu_ref_count(int(c)) == refs_before[int(g)] and m.ref_count(int(g)) == 0
+    assert all(m.is_swapped(s) for s in group)
+    with pytest.raises(N.PAError):
+        m.append([0])                          # a swapped-out sequence cannot grow
+    with pytest.raises(N.PAError):
+        m.block_tables([1], 16)
+    with pytest.raises(N.PAError):
+        m.fork(2, 9)
+    # the freed GPU blocks serve someone else meanwhile
+    m.add_sequence(100, 4 * m.num_free_blocks())
+    with pytest.raises(N.PAError):
+        m.swap_in(group)                       # no room: nothing changes
+    assert all(m.is_swapped(s) for s in group)
+    m.free(100)
+    back = m.swap_in(group)
+    assert sorted(int(c) for c, _ in back) == sorted(int(c) for _, c in pairs)
+    after = {s: [int(x) for x in m.block_tables([s], 16)[0][0] if x >= 0] for s in group}
+    assert sharing_pattern(after) == sharing_pattern(before)
+    assert m.num_free_cpu_blocks() == 24
+    slots, cow = m.append(group)               # decoding resumes
+    assert len(slots) == 4
+
+
+def test_swap_all_or_nothing_on_a_small_cpu_pool():
+    m = BlockManager(16, 4)
+    m.set_cpu_pool(3)
+    m.add_sequence(0, 13)                      # 4 blocks, more than the CPU pool holds
+    with pytest.raises(N.PAError):
+        m.swap_out([0])
+    assert not m.is_swapped(0) and m.num_free_blocks() == 12 and m.num_free_cpu_blocks() == 3
+    m.add_sequence(1, 12)                      # 3 blocks fit
+    pairs = m.swap_out([1])
+    assert len(pairs) == 3 and m.num_free_cpu_blocks() == 0
+    m.free(1)                                  # freeing a swapped-out sequence returns its CPU blocks
+    assert m.num_free_cpu_blocks() == 3
+    with pytest.raises(N.PAError):
+        m.swap_in([0])                         # not swapped out
+    with pytest.raises(N.PAError):
+        BlockManager(4, 4).swap_out([0])       # no CPU pool
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_native_matches_model_with_swapping(seed):
+    """Random add / fork / append / free / swap-out / swap-in, native against the model."""
+    rng = random.Random(100 + seed)
+    n_blocks, bs, n_cpu = rng.choice([(24, 4, 16), (48, 2, 48), (32, 8, 10)])
+    a, b = BlockManagerModel(n_blocks, bs), BlockManager(n_blocks, bs)
+    a.set_cpu_pool(n_cpu)
+    b.set_cpu_pool(n_cpu)
+    live, next_id = [], 0
+    for _ in range(400):
+        op = rng.random()
+        gpu = [s for s in live if s not in a.on_cpu]
+        cpu = [s for s in live if s in a.on_cpu]
+        if op < 0.12 or not live:
+            n = rng.randrange(0, 3 * bs)
+            try:
+                ra = a.add_sequence(next_id, n)
+            except PoolExhausted:
+                with pytest.raises(N.PAError):
+                    b.add_sequence(next_id, n)
+                continue
+            assert ra == list(b.add_sequence(next_id, n))
+            live.append(next_id)
+            next_id += 1
+        elif op < 0.25 and gpu:
+            p = rng.choice(gpu)
+            a.fork(p, next_id)
+            b.fork(p, next_id)
+            live.append(next_id)
+            next_id += 1
+        elif op < 0.65 and gpu:
+            batch = rng.sample(gpu, rng.randint(1, len(gpu)))
+            try:
+                ra = a.append(batch)
+            except PoolExhausted:
+                with pytest.raises(N.PAError):
+                    b.append(batch)
+                continue
+            rb = b.append(batch)
+            assert ra == (list(rb[0]), [tuple(x) for x in rb[1].tolist()])
+        elif op < 0.78 and gpu:
+            group = rng.sample(gpu, rng.randint(1, min(3, len(gpu))))
+            try:
+                ra = a.swap_out(group)
+            except PoolExhausted:
+                with pytest.raises(N.PAError):
+                    b.swap_out(group)
+                continue
+            assert ra == [tuple(x) for x in b.swap_out(group).tolist()]
+        elif op < 0.9 and cpu:
+            group = rng.sample(cpu, rng.randint(1, min(3, len(cpu))))
+            try:
+                ra = a.swap_in(group)
+            except PoolExhausted:
+                with pytest.raises(N.PAError):
+                    b.swap_in(group)
+                continue
+            assert ra == [tuple(x) for x in b.swap_in(group).tolist()]
+        elif live:
+            s = live.pop(rng.randrange(len(live)))
+            a.free_sequence(s)
+            b.free(s)
+        for s in live:
+            assert b.is_swapped(s) == (s in a.on_cpu)
+            if s not in a.on_cpu:
+                t, _ = b.block_tables([s], 64)
+                assert [int(x) for x in t[0] if x >= 0] == a.tables[s]
+        assert [b.ref_count(x) for x in range(n_blocks)] == a.refs
+        assert [b.cpu_ref_count(x) for x in range(n_cpu)] == a.cpu_refs
+        assert b.num_free_blocks() == len(a.free) and b.num_free_cpu_blocks() == len(a.cpu_free)

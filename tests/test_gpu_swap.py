@@ -120,3 +120,58 @@ def test_swap_refuses_pageable_host_memory():
     host = torch.zeros((4, 64), dtype=torch.float16)          # not pinned
     with pytest.raises(ValueError):
         P.pa_swap_blocks(gpu, host, [(0, 1)])
+
+
+def test_block_manager_drives_swap_out_and_in():
+    """The host manager preempts a forked group (its pairs drive pa_swap_blocks into
+    pinned CPU pools), another sequence reuses the freed GPU blocks, the group returns
+    into new GPU blocks and decodes bit-identically."""
+    from paged_kv_cache_119_gb300.block_manager import BlockManager
+    Hq, Hkv, D, B, N = 16, 4, 128, 16, 64
+    g = torch.Generator(device="cuda").manual_seed(11)
+    m = BlockManager(N, B)
+    m.set_cpu_pool(N)
+    kc = torch.full((N, Hkv, B, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+
+    def write(slots):
+        k = torch.randn(len(slots), Hkv, D, generator=g, device="cuda").to(torch.bfloat16)
+        v = torch.randn(len(slots), Hkv, D, generator=g, device="cuda").to(torch.bfloat16)
+        P.pa_reshape_and_cache(k, v, kc, vc, torch.as_tensor(slots, device="cuda"))
+
+    write(m.add_sequence(0, 70))
+    for c in (1, 2):
+        m.fork(0, c)
+    for _ in range(20):
+        slots, pairs = m.append([0, 1, 2])
+        if len(pairs):
+            P.pa_copy_blocks([kc], [vc], pairs)
+        write(slots)
+    group = [0, 1, 2]
+    q = torch.randn(3, Hq, D, generator=g, device="cuda").to(torch.bfloat16)
+
+    def decode(tables, lens):
+        out = torch.empty(3, Hq, D, dtype=torch.float32, device="cuda")
+        P.pa_decode(out, q, kc, vc, torch.as_tensor(tables, device="cuda"),
+                    torch.as_tensor(lens, device="cuda"), 0.1, Hkv, B)
+        return out
+
+    t0, l0 = m.block_tables(group, 16)
+    out0 = decode(t0, l0)
+    cpu_k = torch.zeros((N,) + tuple(kc.shape[1:]), dtype=kc.dtype).pin_memory()
+    cpu_v = torch.zeros_like(cpu_k).pin_memory()
+    P.pa_swap_blocks([kc, vc], [cpu_k, cpu_v], m.swap_out(group))
+    # another sequence takes every free GPU block and overwrites it
+    other = m.num_free_blocks() * B
+    write(m.add_sequence(50, other))
+    m.free(50)
+    P.pa_swap_blocks([cpu_k, cpu_v], [kc, vc], m.swap_in(group))
+    t1, l1 = m.block_tables(group, 16)
+    assert (l1 == l0).all() and not (t1 == t0).all()
+    out1 = decode(t1, l1)
+    torch.cuda.synchronize()
+    assert torch.equal(out0, out1)
+    ref = oracle.paged_attention(q.cpu(), kc.cpu(), vc.cpu(), torch.as_tensor(t1),
+                                 torch.as_tensor(l1), 0.1, Hkv, B)
+    assert np.abs(out1.double().cpu().numpy() - ref).max() <= 2e-3
+    assert P.pa_get_device_error() == 0
