@@ -57,7 +57,10 @@ WORKLOADS["llama13b_verify4"] = (
 WORKLOADS["long16_chunk512"] = (
     "chunked prefill: 8 seqs x 32768-token contexts whose last 512 tokens are new (4096 query "
     "rows), 64 q / 8 kv heads, head_dim 128, bf16, block_size 16, N(0, 1)")
+WORKLOADS["llama13b_verify4_fp8"] = WORKLOADS["llama13b_verify4"] + \
+    "; KV cache in FP8 E4M3 with per-head scales"
 CHUNK_METRIC = {"llama13b_verify4": "paged verify attention KV GB/s",
+                "llama13b_verify4_fp8": "paged verify attention KV GB/s",
                 "long16_chunk512": "paged chunk attention TFLOP/s"}
 # swapping (pa_swap_blocks): a preempted group's blocks out to pinned CPU memory and back
 WORKLOADS["llama13b_swap"] = (
@@ -259,7 +262,8 @@ def make_workload(config: str, device, num_seqs=None):
 def launched_split(pa, w) -> bool:
     """Whether the library's automatic choice splits this workload (one more launch)."""
     if w.query_start is not None:
-        return pa.pa_chunk_partition_tokens(w.dtype, w.num_seqs, w.num_q_heads, w.num_kv_heads,
+        return pa.pa_chunk_partition_tokens(w.k_cache.dtype if w.fp8 else w.dtype, w.num_seqs,
+                                            w.num_q_heads, w.num_kv_heads,
                                             w.head_dim, w.block_size, w.max_query_len,
                                             w.max_context_len, 0) > 0
     return pa.pa_decode_partition_tokens(w.q.dtype, w.k_cache.dtype, w.num_seqs, w.num_q_heads,
@@ -270,6 +274,19 @@ def launched_split(pa, w) -> bool:
 def step_ops(pa, w):
     """(cache write, decode) callables of the library for this workload's cache type
     (for a chunk workload the attention call is pa_chunk_attention)."""
+    if w.query_start is not None and w.fp8:
+        ks, vs = w.meta["k_scale"], w.meta["v_scale"]
+
+        def write(k, v, slots):
+            pa.pa_reshape_and_cache_fp8(k, v, w.k_cache, w.v_cache, slots, ks, vs)
+
+        def decode(out, q, bt, cl, part, ws, qs=None):
+            pa.pa_chunk_attention_fp8(out, q, w.k_cache, w.v_cache, ks, vs, bt, cl,
+                                      w.query_start if qs is None else qs, w.scale,
+                                      w.num_kv_heads, w.block_size, max_query_len=w.max_query_len,
+                                      max_context_len=w.max_context_len, partition_size=part,
+                                      workspace=ws)
+        return write, decode
     if w.query_start is not None:
         def write(k, v, slots):
             pa.pa_reshape_and_cache(k, v, w.k_cache, w.v_cache, slots)

@@ -293,6 +293,24 @@ int pa_chunk_attention(void* out, pa_dtype out_dtype, const void* q, const void*
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * pa_chunk_attention_fp8: pa_chunk_attention over E4M3 caches (the FP8 cache of
+ * pa_decode_fp8: value = code * per-kv-head scale, k_scale / v_scale DEVICE [Hkv]).
+ * q (and a native-dtype out) have q_dtype, PA_F16 or PA_BF16; out_dtype is PA_F32 or
+ * q_dtype.  Every chunk length runs on the decode kernel's multi-row mode, which reads
+ * the one-byte tiles directly; all other arguments, rules and errors are those of
+ * pa_chunk_attention (returns PA_ERR_UNSUPPORTED when called with an E4M3 kv_dtype).
+ */
+int pa_chunk_attention_fp8(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
+                           const void* k_cache, const void* v_cache, const float* k_scale,
+                           const float* v_scale, int64_t num_blocks, const int32_t* block_tables,
+                           int64_t block_table_stride, const int32_t* context_lens,
+                           const int32_t* query_start, int64_t num_query_tokens,
+                           int32_t max_query_len, int32_t max_context_len, int32_t num_seqs,
+                           int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t block_size, float scale, int32_t partition_size,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * The partition length (tokens) a pa_decode / pa_decode_fp8 call, or a
  * pa_chunk_attention call, with these arguments splits contexts into; 0 when it
  * runs one pass per sequence (no merge launch).  partition_size as in those calls;

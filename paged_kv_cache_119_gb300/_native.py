@@ -31,6 +31,10 @@ SIGNATURES = {
                                      _vp, _i64, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _i32,
                                      _vp, _sz, _vp]),
     "pa_chunk_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32, _i32]),
+    "pa_chunk_attention_fp8": (ctypes.c_int, [_vp, ctypes.c_int, _vp, ctypes.c_int, _vp, _vp, _vp,
+                                              _vp, _i64, _vp, _i64, _vp, _vp, _i64, _i32, _i32,
+                                              _i32, _i32, _i32, _i32, _i32, _f32, _i32, _vp, _sz,
+                                              _vp]),
     "pa_decode_partition_tokens": (_i32, [ctypes.c_int, ctypes.c_int, _i32, _i32, _i32, _i32, _i32,
                                           _i32, _i32]),
     "pa_chunk_partition_tokens": (_i32, [ctypes.c_int, _i32, _i32, _i32, _i32, _i32, _i32, _i32,

@@ -359,6 +359,55 @@ def pa_chunk_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor
     return out
 
 
+def pa_chunk_attention_fp8(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                           v_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor,
+                           query_start: torch.Tensor, scale: float, num_kv_heads: int,
+                           block_size: int, max_query_len: int,
+                           max_context_len: int | None = None, partition_size: int = 0,
+                           workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """pa_chunk_attention over E4M3 caches (torch.float8_e4m3fn or uint8 codes) with
+    per-kv-head scales k_scale, v_scale (float32 CUDA [Hkv]); q float16 or bfloat16."""
+    for name, t in (("out", out), ("q", q), ("block_tables", block_tables),
+                    ("context_lens", context_lens), ("query_start", query_start)):
+        _cuda(name, t)
+    _fp8_cache("k_cache", k_cache)
+    _fp8_cache("v_cache", v_cache)
+    if q.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("q must be float16 or bfloat16 for an E4M3 cache")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 or \
+            query_start.dtype != torch.int32:
+        raise TypeError("block_tables, context_lens and query_start must be int32")
+    if q.dim() != 3 or out.shape != q.shape:
+        raise ValueError("q and out must be [R, Hq, D] of one shape")
+    R, Hq, D = q.shape
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape or \
+            tuple(k_cache.shape[1:]) != (num_kv_heads, block_size, D):
+        raise ValueError(f"k_cache/v_cache must be [N, {num_kv_heads}, {block_size}, {D}]")
+    _scales(k_scale, v_scale, num_kv_heads)
+    S = context_lens.shape[0]
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or query_start.shape != (S + 1,):
+        raise ValueError("block_tables must be [S, W], context_lens [S], query_start [S + 1]")
+    if max_context_len is None:
+        max_context_len = block_tables.shape[1] * block_size
+    ws_need = pa_chunk_workspace_bytes(R, Hq, D, max_context_len, max(partition_size, 0)) \
+        if partition_size >= 0 else 0
+    if ws_need and workspace is None:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
+    ws_ptr, ws_bytes = (0, 0) if workspace is None else (workspace.data_ptr(),
+                                                         workspace.numel() *
+                                                         workspace.element_size())
+    status = N.load().pa_chunk_attention_fp8(
+        out.data_ptr(), _dtype(out), q.data_ptr(), _dtype(q), k_cache.data_ptr(),
+        v_cache.data_ptr(), k_scale.data_ptr(), v_scale.data_ptr(), k_cache.shape[0],
+        block_tables.data_ptr(), block_tables.stride(0), context_lens.data_ptr(),
+        query_start.data_ptr(), R, int(max_query_len), int(max_context_len), S, Hq,
+        num_kv_heads, D, block_size, float(scale), int(partition_size), ws_ptr, ws_bytes,
+        _stream(stream))
+    N.check("pa_chunk_attention_fp8", status)
+    return out
+
+
 def pa_decode_partition_tokens(q_dtype: torch.dtype, kv_dtype: torch.dtype, num_seqs: int,
                                num_q_heads: int, num_kv_heads: int, head_dim: int,
                                block_size: int, max_context_len: int,
@@ -378,8 +427,10 @@ def pa_chunk_partition_tokens(kv_dtype: torch.dtype, num_seqs: int, num_q_heads:
                               num_kv_heads: int, head_dim: int, block_size: int,
                               max_query_len: int, max_context_len: int,
                               partition_size: int = 0) -> int:
-    """The partition length pa_chunk_attention would split contexts into (0: one pass)."""
-    r = int(N.load().pa_chunk_partition_tokens(_DT[kv_dtype], num_seqs, num_q_heads,
+    """The partition length pa_chunk_attention (or, for an E4M3 kv_dtype,
+    pa_chunk_attention_fp8) would split contexts into (0: one pass)."""
+    kv = N.PA_FP8_E4M3 if kv_dtype in (torch.float8_e4m3fn, torch.uint8) else _DT[kv_dtype]
+    r = int(N.load().pa_chunk_partition_tokens(kv, num_seqs, num_q_heads,
                                                num_kv_heads, head_dim, block_size,
                                                max_query_len, max_context_len, partition_size))
     if r < 0:

@@ -43,12 +43,13 @@ struct ChunkVariant {
 };
 
 // Chunk rows on the mma.sync decode kernel: NH rows per CTA, the split merged by
-// chunk_reduce_kernel (the same partial-row layout).
-template <typename T, int D, int BS, int NH>
+// chunk_reduce_kernel (the same partial-row layout).  T: query / native output type;
+// TK: cache element type (T, or __nv_fp8_e4m3 for a quantised cache).
+template <typename T, int D, int BS, int NH, typename TK = T>
 struct ChunkRowsVariant {
-    static constexpr int kStages = MmaStages<T, D, BS>::value;
-    using Sm = MmaSmem<T, D, BS, kStages>;
-    static constexpr auto kernel() { return decode_mma_kernel<T, T, D, BS, NH, kStages, true>; }
+    static constexpr int kStages = MmaStages<TK, D, BS>::value;
+    using Sm = MmaSmem<TK, D, BS, kStages>;
+    static constexpr auto kernel() { return decode_mma_kernel<T, TK, D, BS, NH, kStages, true>; }
     static cudaError_t configure()
     {
         return configure_once(reinterpret_cast<const void*>(kernel()), Sm::kAlloc);
@@ -94,6 +95,39 @@ cudaError_t launch_chunk_rows(const DecodeParams& p, const ChunkParams& cp, pa_d
     }
 #undef PA_CHUNK_ROWS_CASE
     return cudaErrorInvalidValue;
+}
+
+// E4M3 caches: always the chunk-row path (q_dtype F16 or BF16; p.k_scale, p.v_scale set).
+cudaError_t launch_chunk_rows_fp8(const DecodeParams& p, const ChunkParams& cp, pa_dtype q_dtype,
+                                  int head_dim, int block_size, int nh, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, cudaStream_t stream)
+{
+#define PA_CHUNK_ROWS_CASE(D_, BS_, NH_)                                                     \
+    if (head_dim == D_ && block_size == BS_ && nh == NH_)                                    \
+        return q_dtype == PA_BF16                                                            \
+                   ? ChunkRowsVariant<__nv_bfloat16, D_, BS_, NH_, __nv_fp8_e4m3>::launch(    \
+                         p, cp, tk, tv, stream)                                              \
+                   : ChunkRowsVariant<__half, D_, BS_, NH_, __nv_fp8_e4m3>::launch(p, cp, tk, tv, \
+                                                                                  stream);
+    if (q_dtype == PA_BF16 || q_dtype == PA_F16) {
+        PA_CHUNK_ROWS_VARIANTS(PA_CHUNK_ROWS_CASE)
+    }
+#undef PA_CHUNK_ROWS_CASE
+    return cudaErrorInvalidValue;
+}
+
+int occupancy_chunk_rows_fp8(pa_dtype q_dtype, int head_dim, int block_size, int nh)
+{
+#define PA_CHUNK_ROWS_OCC(D_, BS_, NH_)                                                       \
+    if (head_dim == D_ && block_size == BS_ && nh == NH_)                                     \
+        return q_dtype == PA_BF16                                                             \
+                   ? ChunkRowsVariant<__nv_bfloat16, D_, BS_, NH_, __nv_fp8_e4m3>::occupancy() \
+                   : ChunkRowsVariant<__half, D_, BS_, NH_, __nv_fp8_e4m3>::occupancy();
+    if (q_dtype == PA_BF16 || q_dtype == PA_F16) {
+        PA_CHUNK_ROWS_VARIANTS(PA_CHUNK_ROWS_OCC)
+    }
+#undef PA_CHUNK_ROWS_OCC
+    return 0;
 }
 
 int occupancy_chunk_rows(pa_dtype dtype, int head_dim, int block_size, int nh)

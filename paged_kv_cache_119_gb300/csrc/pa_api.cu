@@ -283,7 +283,8 @@ int decode_partition(pa_dtype q_dtype, pa_dtype kv_dtype, int num_seqs, int num_
 
 // How pa_chunk_attention runs a call: few (token, head) rows per kv head go to the
 // mma.sync decode kernel in chunk-row mode (nh rows per CTA), longer chunks to the
-// tcgen05 kernel (rows_tokens chunk tokens per CTA); partition = split length.
+// tcgen05 kernel (rows_tokens chunk tokens per CTA); partition = split length.  E4M3
+// caches always take the chunk-row path (its kernel reads E4M3 tiles directly).
 struct ChunkPlan {
     bool rows_path;
     int nh;          // rows per CTA on the decode kernel
@@ -292,20 +293,22 @@ struct ChunkPlan {
     int partition;
 };
 
-ChunkPlan chunk_plan(pa_dtype kv_dtype, int num_seqs, int num_q_heads, int num_kv_heads,
-                     int head_dim, int block_size, int max_query_len, int max_context_len,
-                     int partition_size)
+ChunkPlan chunk_plan(pa_dtype q_dtype, pa_dtype kv_dtype, int num_seqs, int num_q_heads,
+                     int num_kv_heads, int head_dim, int block_size, int max_query_len,
+                     int max_context_len, int partition_size)
 {
     ChunkPlan c{};
     const int group = num_q_heads / num_kv_heads;
     const int64_t rows = (int64_t)max_query_len * group;
-    if (rows <= kChunkRowsMax) {
+    const bool fp8 = kv_dtype == PA_FP8_E4M3;
+    if (rows <= kChunkRowsMax || fp8) {
         c.rows_path = true;
         c.nh = rows <= 4 ? 4 : 8;
-        c.chunks = (int)((rows + c.nh - 1) / c.nh);
+        c.chunks = (int)std::min<int64_t>((rows + c.nh - 1) / c.nh, INT32_MAX);
         int occ = 0;
         if (partition_size == 0)
-            occ = occupancy_chunk_rows(kv_dtype, head_dim, block_size, c.nh);
+            occ = fp8 ? occupancy_chunk_rows_fp8(q_dtype, head_dim, block_size, c.nh)
+                      : occupancy_chunk_rows(kv_dtype, head_dim, block_size, c.nh);
         c.partition = choose_partition(partition_size, max_context_len,
                                        (int64_t)num_seqs * num_kv_heads * c.chunks,
                                        (int64_t)device_sm_count() * occ, block_size);
@@ -484,8 +487,9 @@ int32_t pa_chunk_partition_tokens(pa_dtype kv_dtype, int32_t num_seqs, int32_t n
         return PA_ERR_INVALID;
     if (partition_size == 0 && device_sm_count() <= 0)
         return PA_ERR_CUDA;
-    return chunk_plan(kv_dtype, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                      max_query_len, max_context_len, partition_size)
+    return chunk_plan(kv_dtype == PA_FP8_E4M3 ? PA_BF16 : kv_dtype, kv_dtype, num_seqs,
+                      num_q_heads, num_kv_heads, head_dim, block_size, max_query_len,
+                      max_context_len, partition_size)
         .partition;
 }
 
@@ -502,20 +506,26 @@ size_t pa_chunk_workspace_bytes(int64_t num_query_tokens, int32_t num_q_heads, i
     return workspace_layout(num_query_tokens * num_q_heads, max_parts, head_dim, nullptr);
 }
 
-int pa_chunk_attention(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
-                       const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
-                       const int32_t* block_tables, int64_t block_table_stride,
-                       const int32_t* context_lens, const int32_t* query_start,
-                       int64_t num_query_tokens, int32_t max_query_len, int32_t max_context_len,
-                       int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                       int32_t head_dim, int32_t block_size, float scale, int32_t partition_size,
-                       void* workspace, size_t workspace_bytes, void* stream)
+// Shared body of pa_chunk_attention and pa_chunk_attention_fp8: q_dtype is the type of
+// q (and of a native out), kv_dtype the cache's (PA_FP8_E4M3 with k_scale / v_scale).
+static int chunk_impl(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
+                      const void* k_cache, const void* v_cache, pa_dtype kv_dtype,
+                      const float* k_scale, const float* v_scale, int64_t num_blocks,
+                      const int32_t* block_tables, int64_t block_table_stride,
+                      const int32_t* context_lens, const int32_t* query_start,
+                      int64_t num_query_tokens, int32_t max_query_len, int32_t max_context_len,
+                      int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t block_size, float scale, int32_t partition_size,
+                      void* workspace, size_t workspace_bytes, void* stream)
 {
-    if (!(kv_dtype == PA_F16 || kv_dtype == PA_BF16)) {
-        return (kv_dtype == PA_F32 || kv_dtype == PA_FP8_E4M3) ? PA_ERR_UNSUPPORTED
-                                                               : PA_ERR_INVALID;
+    const bool fp8 = kv_dtype == PA_FP8_E4M3;
+    if (!(q_dtype == PA_F16 || q_dtype == PA_BF16)) {
+        return (q_dtype == PA_F32 || q_dtype == PA_FP8_E4M3) ? PA_ERR_UNSUPPORTED
+                                                             : PA_ERR_INVALID;
     }
-    if (!(out_dtype == PA_F32 || out_dtype == kv_dtype))
+    if (!(out_dtype == PA_F32 || out_dtype == q_dtype))
+        return PA_ERR_INVALID;
+    if (fp8 && (!k_scale || !v_scale))
         return PA_ERR_INVALID;
     if (num_seqs < 0 || num_seqs > 65535 || num_q_heads <= 0 || num_kv_heads <= 0 ||
         num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > 128)
@@ -536,12 +546,13 @@ int pa_chunk_attention(void* out, pa_dtype out_dtype, const void* q, const void*
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
         return PA_ERR_INVALID;
     const int group = num_q_heads / num_kv_heads;
-    const ChunkPlan plan = chunk_plan(kv_dtype, num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                      block_size, max_query_len, max_context_len, partition_size);
+    const ChunkPlan plan = chunk_plan(q_dtype, kv_dtype, num_seqs, num_q_heads, num_kv_heads,
+                                      head_dim, block_size, max_query_len, max_context_len,
+                                      partition_size);
     if ((int64_t)num_kv_heads * plan.chunks > 65535)
         return PA_ERR_INVALID;
     const size_t row_elems = (size_t)num_query_tokens * num_q_heads * head_dim;
-    const size_t q_bytes = row_elems * elem_size(kv_dtype);
+    const size_t q_bytes = row_elems * elem_size(q_dtype);
     const size_t out_bytes = row_elems * elem_size(out_dtype);
     const size_t pool_bytes =
         (size_t)num_blocks * num_kv_heads * block_size * head_dim * elem_size(kv_dtype);
@@ -587,10 +598,13 @@ int pa_chunk_attention(void* out, pa_dtype out_dtype, const void* q, const void*
     if (!p.err)
         return PA_ERR_CUDA;
     CUtensorMap tk{}, tv{};
-    cudaError_t e = kv_tensor_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim,
-                                  kv_dtype);
-    if (e == cudaSuccess)
-        e = kv_tensor_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim, kv_dtype);
+    cudaError_t e = cudaSuccess;
+    if (!fp8 || head_dim == 128) {               // E4M3 at head_dim 64 moves by 1-D bulk copies
+        e = kv_tensor_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim, kv_dtype);
+        if (e == cudaSuccess)
+            e = kv_tensor_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim,
+                              kv_dtype);
+    }
     if (e == cudaErrorInvalidValue)
         return PA_ERR_INVALID;
     if (e != cudaSuccess)
@@ -621,13 +635,52 @@ int pa_chunk_attention(void* out, pa_dtype out_dtype, const void* q, const void*
         d.query_start = query_start;
         d.num_rows = num_query_tokens;
         d.max_query_len = max_query_len;
-        e = launch_chunk_rows(d, p, kv_dtype, head_dim, block_size, plan.nh, tk, tv,
-                              static_cast<cudaStream_t>(stream));
+        d.k_scale = fp8 ? k_scale : nullptr;
+        d.v_scale = fp8 ? v_scale : nullptr;
+        e = fp8 ? launch_chunk_rows_fp8(d, p, q_dtype, head_dim, block_size, plan.nh, tk, tv,
+                                        static_cast<cudaStream_t>(stream))
+                : launch_chunk_rows(d, p, kv_dtype, head_dim, block_size, plan.nh, tk, tv,
+                                    static_cast<cudaStream_t>(stream));
     } else {
         e = launch_chunk_attention(p, kv_dtype, head_dim, block_size, tk, tv,
                                    static_cast<cudaStream_t>(stream));
     }
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_chunk_attention(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
+                       const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
+                       const int32_t* block_tables, int64_t block_table_stride,
+                       const int32_t* context_lens, const int32_t* query_start,
+                       int64_t num_query_tokens, int32_t max_query_len, int32_t max_context_len,
+                       int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, float scale, int32_t partition_size,
+                       void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (kv_dtype == PA_FP8_E4M3)
+        return PA_ERR_UNSUPPORTED;               // E4M3 caches: pa_chunk_attention_fp8
+    return chunk_impl(out, out_dtype, q, kv_dtype, k_cache, v_cache, kv_dtype, nullptr, nullptr,
+                      num_blocks, block_tables, block_table_stride, context_lens, query_start,
+                      num_query_tokens, max_query_len, max_context_len, num_seqs, num_q_heads,
+                      num_kv_heads, head_dim, block_size, scale, partition_size, workspace,
+                      workspace_bytes, stream);
+}
+
+int pa_chunk_attention_fp8(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
+                           const void* k_cache, const void* v_cache, const float* k_scale,
+                           const float* v_scale, int64_t num_blocks, const int32_t* block_tables,
+                           int64_t block_table_stride, const int32_t* context_lens,
+                           const int32_t* query_start, int64_t num_query_tokens,
+                           int32_t max_query_len, int32_t max_context_len, int32_t num_seqs,
+                           int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t block_size, float scale, int32_t partition_size,
+                           void* workspace, size_t workspace_bytes, void* stream)
+{
+    return chunk_impl(out, out_dtype, q, q_dtype, k_cache, v_cache, PA_FP8_E4M3, k_scale, v_scale,
+                      num_blocks, block_tables, block_table_stride, context_lens, query_start,
+                      num_query_tokens, max_query_len, max_context_len, num_seqs, num_q_heads,
+                      num_kv_heads, head_dim, block_size, scale, partition_size, workspace,
+                      workspace_bytes, stream);
 }
 
 int pa_reshape_and_cache_fp8(const void* k, const void* v, pa_dtype src_dtype, void* k_cache,

@@ -192,6 +192,11 @@ cudaError_t launch_chunk_rows(const DecodeParams& p, const ChunkParams& cp, pa_d
                               int head_dim, int block_size, int nh, const CUtensorMap& tk,
                               const CUtensorMap& tv, cudaStream_t stream);
 int occupancy_chunk_rows(pa_dtype dtype, int head_dim, int block_size, int nh);
+// E4M3 caches: every chunk length runs on the chunk-row path.
+cudaError_t launch_chunk_rows_fp8(const DecodeParams& p, const ChunkParams& cp, pa_dtype q_dtype,
+                                  int head_dim, int block_size, int nh, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, cudaStream_t stream);
+int occupancy_chunk_rows_fp8(pa_dtype q_dtype, int head_dim, int block_size, int nh);
 
 // Sets the dynamic shared-memory limit of a kernel once per device and process.
 inline cudaError_t configure_once(const void* kernel, int smem_bytes)

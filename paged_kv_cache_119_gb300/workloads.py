@@ -194,7 +194,8 @@ def to_fp8(w: Workload, headroom: float = 8.0) -> Workload:
         block_tables=w.block_tables, q=w.q, k_cache=quant(w.k_cache, k_scale),
         v_cache=quant(w.v_cache, v_scale), k_new=w.k_new, v_new=w.v_new,
         slot_mapping=w.slot_mapping, copy_pairs=w.copy_pairs,
-        partition_size=w.partition_size, meta=dict(meta, k_scale=k_scale, v_scale=v_scale))
+        partition_size=w.partition_size, meta=dict(meta, k_scale=k_scale, v_scale=v_scale),
+        query_start=w.query_start)
 
 
 def tiny(device="cpu", seed=None, **kw) -> Workload:

@@ -264,3 +264,63 @@ def test_verify4_full_batch_sampled_rows():
                                  num_threads=oracle.max_threads())
     err = np.abs(out[rows.cuda()].double().cpu().numpy() - ref).max()
     assert err <= ATOL, err
+
+
+# ------------------------------------------------------------------- E4M3 caches
+
+def run_and_compare_fp8(w, out_dtype=torch.float32, partition_size=0):
+    ks, vs = w.meta["k_scale"], w.meta["v_scale"]
+    snap = {n: getattr(w, n).cpu() for n in ("q", "k_cache", "v_cache", "k_new", "v_new",
+                                             "slot_mapping", "block_tables", "context_lens",
+                                             "query_start")}
+    P.pa_reshape_and_cache_fp8(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping, ks, vs)
+    out = torch.empty(w.q.shape, dtype=out_dtype, device="cuda")
+    P.pa_chunk_attention_fp8(out, w.q, w.k_cache, w.v_cache, ks, vs, w.block_tables,
+                             w.context_lens, w.query_start, w.scale, w.num_kv_heads, w.block_size,
+                             max_query_len=w.max_query_len, max_context_len=w.max_context_len,
+                             partition_size=partition_size)
+    torch.cuda.synchronize()
+    kc, vc = snap["k_cache"].view(torch.uint8).clone(), snap["v_cache"].view(torch.uint8).clone()
+    oracle.reshape_and_cache_e4m3(snap["k_new"], snap["v_new"], kc, vc, snap["slot_mapping"],
+                                  w.block_size, ks.cpu(), vs.cpu())
+    assert torch.equal(w.k_cache.cpu().view(torch.uint8), kc)
+    assert torch.equal(w.v_cache.cpu().view(torch.uint8), vc)
+    ref = oracle.chunk_attention(snap["q"], kc, vc, snap["block_tables"], snap["context_lens"],
+                                 snap["query_start"], w.scale, w.num_kv_heads, w.block_size,
+                                 num_threads=oracle.max_threads(), k_scale=ks.cpu(),
+                                 v_scale=vs.cpu())
+    got = out.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    if out_dtype == torch.float32:
+        err = np.abs(got - ref).max()
+        assert err <= ATOL, f"max abs error {err:.3e}"
+    else:
+        lo = torch.from_numpy((ref - NATIVE_EPS).astype(np.float32)).to(out_dtype).double().numpy()
+        hi = torch.from_numpy((ref + NATIVE_EPS).astype(np.float32)).to(out_dtype).double().numpy()
+        assert not ((got < lo) | (got > hi)).any()
+    assert P.pa_get_device_error() == 0
+
+
+def test_fp8_verify4_llama13b_shape():
+    w = workloads.to_fp8(workloads.make("llama13b_verify4", device="cuda", num_seqs=12))
+    run_and_compare_fp8(w)
+
+
+@pytest.mark.parametrize("Hq,Hkv,nmax", [(8, 8, 4), (16, 4, 8), (40, 8, 3), (64, 8, 40)])
+@pytest.mark.parametrize("D,B", [(128, 16), (64, 32)])
+@pytest.mark.parametrize("qdtype", [torch.bfloat16, torch.float16])
+def test_fp8_chunks(Hq, Hkv, nmax, D, B, qdtype):
+    """Short and long chunks over E4M3 caches (every length runs on the multi-row
+    decode kernel), every grouping, both head dims, bf16 and f16 queries."""
+    rng = np.random.default_rng(Hq + 13 * nmax + D + B)
+    lens = [int(x) for x in rng.integers(1, 500, size=6)] + [nmax]
+    chunks = [min(L, int(rng.integers(0, nmax + 1))) for L in lens]
+    chunks[-1] = nmax
+    w = make_case(int(rng.integers(1 << 30)), len(lens), Hq, Hkv, D, B, qdtype, lens, chunks)
+    run_and_compare_fp8(workloads.to_fp8(w))
+
+
+@pytest.mark.parametrize("part", [0, 64, -1])
+def test_fp8_chunk_splits_and_native_output(part):
+    w = make_case(41, 3, 32, 8, 128, 16, torch.bfloat16, [2500, 300, 40], [4, 2, 4])
+    run_and_compare_fp8(workloads.to_fp8(w), out_dtype=torch.bfloat16, partition_size=part)
