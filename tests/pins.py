@@ -609,6 +609,31 @@ def pin_chunk_of_one_is_decode_sdpa(lib):
                                    rtol=1e-12, atol=1e-13)
 
 
+def pin_chunk_e4m3_equals_dequantized_causal_sdpa(lib):
+    """Whole-context chunks over E4M3 pools equal PyTorch's float64 causal SDPA on the
+    dequantised (code x per-kv-head scale) keys and values."""
+    rng = np.random.default_rng(26)
+    c = chunk_case(rng, 2, 8, 2, 32, 8, torch.float32, 30, full_prefill=True)
+    ks = torch.tensor([0.05, 0.11])
+    vs = torch.tensor([0.07, 0.03])
+    kq = (c["kc"] / ks[None, :, None, None]).to(torch.float8_e4m3fn)
+    vq = (c["vc"] / vs[None, :, None, None]).to(torch.float8_e4m3fn)
+    out = oracle.chunk_attention(c["qc"], kq, vq, table_tensor(c["tables"]),
+                                 torch.tensor(c["lens"], dtype=torch.int32), c["query_start"],
+                                 0.25, 2, 8, lib=lib, k_scale=ks, v_scale=vs)
+    kd = kq.double() * ks.double()[None, :, None, None]
+    vd = vq.double() * vs.double()[None, :, None, None]
+    qs = c["query_start"].tolist()
+    for s, (L, tab) in enumerate(zip(c["lens"], c["tables"])):
+        K = torch.stack([kd[tab[t // 8], :, t % 8] for t in range(L)])      # [L, Hkv, D]
+        V = torch.stack([vd[tab[t // 8], :, t % 8] for t in range(L)])
+        q64 = c["qc"][qs[s]:qs[s + 1]].double().permute(1, 0, 2)[None]
+        ref = F.scaled_dot_product_attention(q64, K.permute(1, 0, 2)[None], V.permute(1, 0, 2)[None],
+                                             scale=0.25, is_causal=True, enable_gqa=True)
+        np.testing.assert_allclose(out[qs[s]:qs[s + 1]], ref[0].permute(1, 0, 2).numpy(),
+                                   rtol=1e-12, atol=1e-13)
+
+
 def pin_chunk_longer_than_context_is_nan(lib):
     """A chunk longer than its context is malformed: its rows come back NaN and the
     other sequences are unaffected."""
