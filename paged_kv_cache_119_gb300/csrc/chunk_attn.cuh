@@ -508,13 +508,13 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                         ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
             }
             if (warp_live) {
-                // P over the S buffer: hi in its first 32 columns, lo in the next 32
-                uint32_t hi[NT / 2], lo[NT / 2];
+                // P over the S buffer: hi in its first 32 columns, lo in the next 32,
+                // written by one 64-column store (one wait)
+                uint32_t hl[NT];
 #pragma unroll
                 for (int k = 0; k < NT / 2; ++k)
-                    split_pair<T>(s[2 * k], s[2 * k + 1], hi[k], lo[k]);
-                tmem_st32_raw(sp_col, hi);
-                tmem_st32_raw(sp_col + NT / 2, lo);
+                    split_pair<T>(s[2 * k], s[2 * k + 1], hl[k], hl[NT / 2 + k]);
+                tmem_st64_raw(sp_col, hl);
             }
             if (tb + NT > t1) {
                 // V rows past the range may hold anything (unused slots, stale tiles):
