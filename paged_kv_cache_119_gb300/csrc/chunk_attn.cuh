@@ -535,8 +535,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 if (lane == 0)
                     mbar_arrive(v_zero);
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
+            tc_fence_before();                           // the P store precedes P.V
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&p_full[q * 2 + b]);
