@@ -97,11 +97,14 @@ cudaError_t launch_chunk_rows(const DecodeParams& p, const ChunkParams& cp, pa_d
     return cudaErrorInvalidValue;
 }
 
-// E4M3 caches: always the chunk-row path (q_dtype F16 or BF16; p.k_scale, p.v_scale set).
+// E4M3 caches: always the chunk-row path (q_dtype F16 or BF16; p.k_scale, p.v_scale set);
+// the E4M3 tcgen05 kernel where use_tc8 says so, else the mma.sync kernel.
 cudaError_t launch_chunk_rows_fp8(const DecodeParams& p, const ChunkParams& cp, pa_dtype q_dtype,
                                   int head_dim, int block_size, int nh, const CUtensorMap& tk,
                                   const CUtensorMap& tv, cudaStream_t stream)
 {
+    if (use_tc8(head_dim, nh))
+        return launch_chunk_rows_tc8(p, cp, q_dtype, block_size, nh, tk, tv, stream);
 #define PA_CHUNK_ROWS_CASE(D_, BS_, NH_)                                                     \
     if (head_dim == D_ && block_size == BS_ && nh == NH_)                                    \
         return q_dtype == PA_BF16                                                            \
@@ -118,6 +121,8 @@ cudaError_t launch_chunk_rows_fp8(const DecodeParams& p, const ChunkParams& cp, 
 
 int occupancy_chunk_rows_fp8(pa_dtype q_dtype, int head_dim, int block_size, int nh)
 {
+    if (use_tc8(head_dim, nh))
+        return occupancy_chunk_rows_tc8(q_dtype, block_size, nh);
 #define PA_CHUNK_ROWS_OCC(D_, BS_, NH_)                                                       \
     if (head_dim == D_ && block_size == BS_ && nh == NH_)                                     \
         return q_dtype == PA_BF16                                                             \

@@ -92,14 +92,6 @@ struct ChunkStages {
     static constexpr int value = D == 128 ? 5 : 8;
 };
 
-// 2^x on the MUFU unit (relative error far below the 2^-17 of the P split).
-__device__ __forceinline__ float ex2_approx(float x)
-{
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 // Stores 32 consecutive outputs v[i] * mul (NaN when nan_out) at base + idx as
 // fp32 (which = 0), f16 (1) or bf16 (2); idx is a multiple of 32.
 __device__ __forceinline__ void store_row32(void* base, int64_t idx, const float (&v)[32], float mul,

@@ -1,7 +1,8 @@
 // decode_fp8.cu -- paged decode attention over E4M3 (FP8) caches with per-kv-head
-// scales; queries and native outputs are fp16 or bf16.  The tensor-core kernel
-// (decode_mma.cuh) serves at least kMmaMinHeadsFp8 query heads per CTA, the CUDA-core
-// kernel (decode_kernel.cuh) the rest; both read one byte per cached element.
+// scales; queries and native outputs are fp16 or bf16.  head_dim 128 with up to 4 query
+// heads per CTA runs on the E4M3 tcgen05 kernel (decode_tc8.cuh).  Otherwise the
+// mma.sync kernel (decode_mma.cuh) serves at least kMmaMinHeadsFp8 query heads per CTA,
+// the CUDA-core kernel (decode_kernel.cuh) the rest; all read one byte per cached element.
 #include "decode_mma.cuh"
 
 namespace pa {
@@ -30,6 +31,8 @@ int occupancy_fp8(int head_dim, int block_size, int gc)
 cudaError_t launch_decode_fp8(const DecodeParams& p, pa_dtype q_dtype, int head_dim,
                               int block_size, int gc, cudaStream_t stream)
 {
+    if (use_tc8(head_dim, gc))
+        return launch_decode_tc8(p, q_dtype, block_size, gc, stream);
     if (q_dtype == PA_F16)
         return launch_fp8<__half>(p, head_dim, block_size, gc, stream);
     if (q_dtype == PA_BF16)
@@ -39,6 +42,8 @@ cudaError_t launch_decode_fp8(const DecodeParams& p, pa_dtype q_dtype, int head_
 
 int occupancy_decode_fp8(pa_dtype q_dtype, int head_dim, int block_size, int gc)
 {
+    if (use_tc8(head_dim, gc))
+        return occupancy_decode_tc8(q_dtype, block_size, gc);
     if (q_dtype == PA_F16)
         return occupancy_fp8<__half>(head_dim, block_size, gc);
     if (q_dtype == PA_BF16)

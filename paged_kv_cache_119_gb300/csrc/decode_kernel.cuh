@@ -486,7 +486,8 @@ __global__ void __launch_bounds__(D) reduce_kernel(const DecodeParams p)
         num = fmaf(w, po[(int64_t)i * D], num);
         den += w;
     }
-    store_out<T>(p, row * D + d, den > 0.f ? num / den : 0.f);
+    // no visible token gives 0; a NaN partition (poisoned, or NaN scores) makes the row NaN
+    store_out<T>(p, row * D + d, den > 0.f ? num / den : (den == 0.f ? 0.f : __int_as_float(0x7fc00000)));
 }
 
 // Ring depth: a multiple of the consumer-warp count (about 64 KB of K/V per CTA,

@@ -104,6 +104,32 @@ int choose_chunk_partition(int partition_size, int max_context_len, int64_t unit
     return P >= max_context_len ? 0 : P;
 }
 
+// Partition length of the E4M3 tensor-core decode (decode_tc8.cuh), or 0 for one pass.
+// A CTA of that kernel keeps about one 32 KB tile load in flight, so the grid needs many
+// CTAs to cover the memory latency: with units = CTAs per partition and slots = SMs x
+// resident CTAs per SM, contexts are cut until the grid holds about four CTAs per slot,
+// into whole 128-token tiles of at least 512 tokens.  An explicit partition_size is
+// used as in choose_partition.
+int choose_partition_tc8(int partition_size, int max_context_len, int64_t units, int64_t slots)
+{
+    if (partition_size < 0)
+        return 0;
+    if (partition_size > 0)
+        return max_context_len > partition_size ? partition_size : 0;
+    if (slots <= 0)
+        slots = 3 * 148;
+    const int64_t want = 4 * slots;
+    if (units >= want || max_context_len <= 512)
+        return 0;
+    const int64_t max_parts = (max_context_len + 511) / 512;
+    const int64_t parts = std::min<int64_t>((want + units - 1) / units, max_parts);
+    if (parts <= 1)
+        return 0;
+    const int per = (int)((max_context_len + parts - 1) / parts);
+    const int P = (per + 127) / 128 * 128;
+    return P >= max_context_len ? 0 : P;
+}
+
 size_t workspace_layout(int64_t rows, int max_parts, int head_dim, size_t* ml_offset)
 {
     const size_t o_bytes = align_up((size_t)rows * max_parts * head_dim * sizeof(float), 256);
@@ -276,8 +302,11 @@ int decode_partition(pa_dtype q_dtype, pa_dtype kv_dtype, int num_seqs, int num_
         case PA_FP8_E4M3: occ = occupancy_decode_fp8(q_dtype, head_dim, block_size, gc); break;
         }
     }
-    return choose_partition(partition_size, max_context_len,
-                            (int64_t)num_seqs * num_kv_heads * (group / gc),
+    const int64_t units = (int64_t)num_seqs * num_kv_heads * (group / gc);
+    if (kv_dtype == PA_FP8_E4M3 && use_tc8(head_dim, gc))
+        return choose_partition_tc8(partition_size, max_context_len, units,
+                                    (int64_t)device_sm_count() * occ);
+    return choose_partition(partition_size, max_context_len, units,
                             (int64_t)device_sm_count() * occ, block_size);
 }
 
@@ -309,9 +338,12 @@ ChunkPlan chunk_plan(pa_dtype q_dtype, pa_dtype kv_dtype, int num_seqs, int num_
         if (partition_size == 0)
             occ = fp8 ? occupancy_chunk_rows_fp8(q_dtype, head_dim, block_size, c.nh)
                       : occupancy_chunk_rows(kv_dtype, head_dim, block_size, c.nh);
-        c.partition = choose_partition(partition_size, max_context_len,
-                                       (int64_t)num_seqs * num_kv_heads * c.chunks,
-                                       (int64_t)device_sm_count() * occ, block_size);
+        const int64_t units = (int64_t)num_seqs * num_kv_heads * c.chunks;
+        const int64_t slots = (int64_t)device_sm_count() * occ;
+        c.partition = (fp8 && use_tc8(head_dim, c.nh))
+                          ? choose_partition_tc8(partition_size, max_context_len, units, slots)
+                          : choose_partition(partition_size, max_context_len, units, slots,
+                                             block_size);
         return c;
     }
     c.rows_tokens = kChunkCtaRows / group;

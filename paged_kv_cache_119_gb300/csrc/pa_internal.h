@@ -70,6 +70,16 @@ cudaError_t launch_decode_bf16(const DecodeParams& p, int head_dim, int block_si
 cudaError_t launch_decode_fp8(const DecodeParams& p, pa_dtype q_dtype, int head_dim,
                               int block_size, int gc, cudaStream_t stream);
 int occupancy_decode_fp8(pa_dtype q_dtype, int head_dim, int block_size, int gc);
+// Whether an E4M3 call with this head_dim and rows per CTA (query heads, or chunk rows)
+// runs on the E4M3 tcgen05 kernel (decode_tc8.cuh).  At 8 rows per CTA the mma.sync
+// kernel streams faster (measured on GB300: its four consumer warps work on separate
+// blocks and free each block on its own, against one 128-token tile chain per CTA).
+inline bool use_tc8(int head_dim, int rows) { return head_dim == 128 && rows <= 4; }
+// The E4M3 tensor-core decode at head_dim 128 (decode_tc8.cu): `rows` = query heads per
+// CTA (1, 2, 4 or 8); makes its own tensor maps.
+cudaError_t launch_decode_tc8(const DecodeParams& p, pa_dtype q_dtype, int block_size, int rows,
+                              cudaStream_t stream);
+int occupancy_decode_tc8(pa_dtype q_dtype, int block_size, int rows);
 
 // Resident decode CTAs per SM for this dtype / shape / heads-per-CTA (0 if unknown).
 int occupancy_decode_f32(int head_dim, int block_size, int gc);
@@ -197,6 +207,12 @@ cudaError_t launch_chunk_rows_fp8(const DecodeParams& p, const ChunkParams& cp, 
                                   int head_dim, int block_size, int nh, const CUtensorMap& tk,
                                   const CUtensorMap& tv, cudaStream_t stream);
 int occupancy_chunk_rows_fp8(pa_dtype q_dtype, int head_dim, int block_size, int nh);
+// E4M3 chunk rows at head_dim 128 on the E4M3 tensor-core decode (decode_tc8.cu), `rows`
+// (4 or 8) rows per CTA; tk / tv are the E4M3 tensor maps of the caches.
+cudaError_t launch_chunk_rows_tc8(const DecodeParams& p, const ChunkParams& cp, pa_dtype q_dtype,
+                                  int block_size, int rows, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, cudaStream_t stream);
+int occupancy_chunk_rows_tc8(pa_dtype q_dtype, int block_size, int rows);
 
 // Sets the dynamic shared-memory limit of a kernel once per device and process.
 inline cudaError_t configure_once(const void* kernel, int smem_bytes)
