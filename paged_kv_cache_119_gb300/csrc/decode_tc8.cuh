@@ -23,19 +23,23 @@
 // split the same way, 256 p = P0 + P1/16 + P2/256 + P3/4096, in rows 4r .. 4r+3 of Pt.
 // The fp32 results of the term columns are combined with the same weights.
 //
-// Roles (192 threads):
-//   * warp 0, producer: block-table entries and tensor-map TMA of the tile's blocks
-//     (box = B tokens x 128 bytes, 128-byte swizzle; the tensor map's third coordinate
-//     is block * Hkv + kv head) into an mbarrier ring of NST stages of K + V;
-//   * warp 1: allocates the tensor memory; one thread issues the MMAs: S of tile i+1
-//     as soon as its K is in, then P.V of tile i once its P is written;
+// Roles (224 threads):
+//   * warps 0 and 6, producers of K and of V: block-table entries and tensor-map TMA of
+//     the tile's blocks (box = B tokens x 128 bytes, 128-byte swizzle; the tensor map's
+//     third coordinate is block * Hkv + kv head) into rings of NST slots.  A K slot is
+//     released when the scores of its tile are computed, a V slot when P.V has read it,
+//     so the K loads of later tiles are in flight while a tile is still being softmaxed;
+//   * warp 1: allocates the tensor memory; one thread issues the MMAs, whichever is
+//     ready: S of the next tile once its K is in, P.V of a tile once its P is written
+//     and its V is in;
 //   * warps 2-5, one thread per tensor-memory lane: read the scores of their token,
 //     exchange per-row tile maxima through shared memory and an mbarrier, online
 //     softmax in base 2, write the four P terms, zero the V rows past the range on the
 //     last tile (unused slots may hold NaN, and 0 * NaN is NaN); then, as head dim d,
 //     read the P.V result of the previous tile and fold it into their accumulators.
 // S and O tensor-memory buffers and the Pt buffers alternate between tiles, so the
-// softmax of tile i+1 overlaps P.V of tile i.  Every wait is bounded.
+// softmax of tile i+1 overlaps P.V of tile i.  Every wait is bounded; an invalid
+// block id makes the CTA's rows NaN, decided after the final CTA barrier.
 #pragma once
 
 #include <cuda.h>
@@ -48,7 +52,7 @@ namespace pa {
 
 constexpr int kTc8Tok = 128;        // tokens per K/V tile (M of the score product)
 constexpr int kTc8Terms = 4;        // E4M3 terms per query row and per probability
-constexpr int kTc8Threads = 192;    // producer, MMA issuer, 4 softmax warps
+constexpr int kTc8Threads = 224;    // K producer, MMA issuer, 4 softmax warps, V producer
 
 template <int R, int NST>
 struct Tc8Smem {
@@ -60,10 +64,10 @@ struct Tc8Smem {
     static constexpr int kRedOff = kPOff + 2 * N * 128;                 // red_max[2][4][R]
     static constexpr int kLOff = kRedOff + 2 * 4 * R * 4;               // red_l[4][R]
     static constexpr int kBarOff = (kLOff + 4 * R * 4 + 7) / 8 * 8;
-    // full[NST], empty[NST], s_full[2], p_full[2], pv_done[2], red[2], mma_done
-    static constexpr int kNumBars = 2 * NST + 9;
-    static constexpr int kOkOff = kBarOff + 8 * kNumBars;               // stage_ok[NST]
-    static constexpr int kSlotOff = kOkOff + 4 * NST;                   // TMEM address
+    // kfull[NST], vfull[NST], kempty[NST], vempty[NST], s_full[2], p_full[2], pv_done[2],
+    // red[2], mma_done
+    static constexpr int kNumBars = 4 * NST + 9;
+    static constexpr int kSlotOff = kBarOff + 8 * kNumBars;             // TMEM address
     static constexpr int kPoisonOff = kSlotOff + 4;
     static constexpr int kBytes = kPoisonOff + 4;
     static constexpr int kAlloc = kBytes + 1024;                        // 1 KB alignment slack
@@ -175,7 +179,7 @@ __device__ __forceinline__ int sw128_byte(int row, int col)
 // row R0 + r = token (R0 + r) / group, head (R0 + r) % group).
 // grid = (partitions, num_kv_heads * chunks, num_seqs); kTc8Threads threads.
 template <typename T, int BS, int R, int NST, bool CH>
-__global__ void __launch_bounds__(kTc8Threads)
+__global__ void __launch_bounds__(kTc8Threads, 3)
     decode_tc8_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv)
 {
@@ -188,14 +192,15 @@ __global__ void __launch_bounds__(kTc8Threads)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sm::kBarOff);
-    uint64_t* empty = full + NST;
-    uint64_t* s_full = empty + NST;             // [S buffer]
+    uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + Sm::kBarOff);   // [stage]
+    uint64_t* vfull = kfull + NST;
+    uint64_t* kempty = vfull + NST;
+    uint64_t* vempty = kempty + NST;
+    uint64_t* s_full = vempty + NST;            // [S buffer]
     uint64_t* p_full = s_full + 2;              // [P buffer]
     uint64_t* pv_done = p_full + 2;             // [O buffer]
     uint64_t* red_bar = pv_done + 2;            // [exchange buffer]
     uint64_t* mma_done = red_bar + 2;
-    int* stage_ok = reinterpret_cast<int*>(smem + Sm::kOkOff);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Sm::kSlotOff);
     int* poison = reinterpret_cast<int*>(smem + Sm::kPoisonOff);
     float* red_max = reinterpret_cast<float*>(smem + Sm::kRedOff);   // [2][4][R]
@@ -257,8 +262,10 @@ __global__ void __launch_bounds__(kTc8Threads)
     if (threadIdx.x == 0) {
 #pragma unroll
         for (int s = 0; s < NST; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&kfull[s], 1);
+            mbar_init(&vfull[s], 1);
+            mbar_init(&kempty[s], 1);
+            mbar_init(&vempty[s], 1);
         }
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
@@ -277,16 +284,26 @@ __global__ void __launch_bounds__(kTc8Threads)
     }
     __syncthreads();
 
-    if (warp == 0) {
-        // ------------------------------------------------------------------ producer
-        // starts at once: it needs neither the tensor memory nor the query terms
+    // per-row results of the softmax warps, stored after the final CTA barrier
+    int64_t orow_e[R];
+    float acc_e[R], m_e[R], l_e[R];
+
+    if (warp == 0 || warp == 6) {
+        // ------------------------------------------------- producers: K (warp 0), V (warp 6)
+        // They start at once (they need neither the tensor memory nor the query terms) and
+        // run separately: a K slot is free again as soon as its scores are computed, a V
+        // slot only once P.V has read it, so K loads run ahead of V loads.
+        const bool is_k = warp == 0;
+        const CUtensorMap* map = is_k ? &tk : &tv;
+        uint64_t* fullb = is_k ? kfull : vfull;
+        uint64_t* emptyb = is_k ? kempty : vempty;
+        const int half = is_k ? 0 : Sm::kTile;
         const int32_t* bt_row = p.block_tables + (int64_t)seq * p.bt_stride;
         const uint64_t policy = l2_evict_first_policy();
         const int blk_first = t0 / BS;             // partitions start on block boundaries
         const int nblk = (t1 + BS - 1) / BS - blk_first;
         // block-table entries 32 at a time (4 or 8 tiles), the next 32 in flight while the
-        // current ones are used: a dependent table read per tile would put a memory
-        // latency between consecutive tiles' copies
+        // current ones are used
         int cur = lane < nblk ? __ldg(bt_row + blk_first + lane) : -1;
         int nxt = 32 + lane < nblk ? __ldg(bt_row + blk_first + 32 + lane) : -1;
         int issued = 0;
@@ -308,31 +325,34 @@ __global__ void __launch_bounds__(kTc8Threads)
             const unsigned vmask = __ballot_sync(kFullMask, valid);
             int ok = 1;
             if (lane == 0) {
-                if (it >= NST && !mbar_wait(&empty[st], ((it / NST) - 1) & 1)) {
+                if (it >= NST && !mbar_wait(&emptyb[st], ((it / NST) - 1) & 1)) {
                     atomicOr(p.err, PA_DEVERR_TIMEOUT);
                     ok = 0;
                 } else {
                     const int nvalid = __popc(vmask);
-                    stage_ok[st] = nvalid == nb ? 1 : 0;
-                    if (nvalid != nb)
+                    if (nvalid != nb) {                // the CTA's rows become NaN
                         atomicOr(p.err, PA_DEVERR_BLOCK_ID);
-                    mbar_arrive_expect_tx(&full[st], (uint32_t)nvalid * 2u * BS * 128u);
+                        *poison = 1;
+                    }
+                    mbar_arrive_expect_tx(&fullb[st], (uint32_t)nvalid * BS * 128u);
                 }
             }
-            if (!__shfl_sync(kFullMask, ok, 0))
+            if (!__shfl_sync(kFullMask, ok, 0)) {
+                if (lane == 0)
+                    *poison = 1;
                 break;
+            }
             if (valid) {
-                unsigned char* kdst = smem + st * Sm::kStage + lane * (BS * 128);
                 const int z = pbn * p.num_kv_heads + kvh;     // < 2^31 (checked on the host)
-                tma_load_3d(kdst, &tk, 0, 0, z, &full[st], policy);
-                tma_load_3d(kdst + Sm::kTile, &tv, 0, 0, z, &full[st], policy);
+                tma_load_3d(smem + st * Sm::kStage + half + lane * (BS * 128), map, 0, 0, z,
+                            &fullb[st], policy);
             }
             issued = it + 1;
         }
         // no copy may still be in flight into this CTA's shared memory at exit
         if (lane == 0)
             for (int it = max(0, issued - NST); it < issued; ++it)
-                mbar_wait(&full[it % NST], (it / NST) & 1);
+                mbar_wait(&fullb[it % NST], (it / NST) & 1);
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
@@ -354,6 +374,7 @@ __global__ void __launch_bounds__(kTc8Threads)
                     tc_mma_e4m3(dcol, sw128_desc(kb + kk * 32, 16, 1024),
                                 sw128_desc(qaddr + kk * 32, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
                 tc_commit(&s_full[it & 1]);
+                tc_commit(&kempty[it % NST]);  // K of the stage is consumed
             };
             auto issue_pv = [&](int it) {
                 const uint32_t vb = smem_addr(smem + (it % NST) * Sm::kStage + Sm::kTile);
@@ -365,10 +386,11 @@ __global__ void __launch_bounds__(kTc8Threads)
                     tc_mma_e4m3(ocol, sw128_desc(vb + kk * 4096, 16, 1024),
                                 sw128_desc(pb + kk * 32, 16, 1024), idesc_o, kk > 0 ? 1u : 0u);
                 tc_commit(&pv_done[it & 1]);
-                tc_commit(&empty[it % NST]);   // K and V of the stage are consumed
+                tc_commit(&vempty[it % NST]);  // V of the stage is consumed
             };
-            // Issue whichever product is ready: the scores of tile ns once its K and V
-            // are in, P.V of tile np once its P is written.  P.V never waits for the next
+            // Issue whichever product is ready: the scores of tile ns once its K is in,
+            // P.V of tile np once its P is written and its V is in (non-blocking tests:
+            // a suspended try_wait on one barrier would hide the other's completion).  P.V never waits for the next
             // tile's data, so a stage goes back to the producer as soon as it is used.
             // S buffer ns&1 is free once P of tile ns-2 was handed over (ns <= np + 1);
             // the O buffer of tile np was read back before P of tile np was.
@@ -377,12 +399,13 @@ __global__ void __launch_bounds__(kTc8Threads)
             uint64_t t_last = 0;
             uint32_t spins = 0;
             while (np < ntiles) {
-                if (ns < ntiles && ns <= np + 1 && mbar_try_wait(&full[ns % NST], (ns / NST) & 1)) {
+                if (ns < ntiles && ns <= np + 1 && mbar_test_wait(&kfull[ns % NST], (ns / NST) & 1)) {
                     tc_fence_after();
                     issue_scores(ns);
                     ++ns;
                     spins = 0;
-                } else if (np < ns && mbar_try_wait(&p_full[np & 1], (np >> 1) & 1)) {
+                } else if (np < ns && mbar_test_wait(&p_full[np & 1], (np >> 1) & 1) &&
+                           mbar_test_wait(&vfull[np % NST], (np / NST) & 1)) {
                     tc_fence_after();
                     issue_pv(np);
                     ++np;
@@ -502,14 +525,14 @@ __global__ void __launch_bounds__(kTc8Threads)
             const int b = it & 1;
             const int st = it % NST;
             const int tb = t0 + it * kTc8Tok;
-            if (!mbar_wait(&s_full[b], (it >> 1) & 1) || !mbar_wait(&full[st], (it / NST) & 1)) {
+            // the scores imply the tile's K (the K slot may already hold a later tile:
+            // neither kfull nor any per-stage word is read here)
+            if (!mbar_wait(&s_full[b], (it >> 1) & 1)) {
                 if (lane == 0)
                     atomicOr(p.err, PA_DEVERR_TIMEOUT);
                 poisoned = aborted = true;
                 break;
             }
-            if (!stage_ok[st])
-                poisoned = true;
             tc_fence_after();
             float sv[N];
             tmem_ldn<N>(lane_t + b * N, sv);
@@ -563,12 +586,22 @@ __global__ void __launch_bounds__(kTc8Threads)
 #pragma unroll
                 for (int k = 0; k < kTc8Terms; ++k)
                     pbuf[sw128_byte(kTc8Terms * r + k, tl)] = (unsigned char)pt[r][k];
-            if (tb + kTc8Tok > t1 && pos >= t1) {
-                // V row of a token past the range (unused slot, missing block, stale tile)
-                uint4* vrow = reinterpret_cast<uint4*>(smem + st * Sm::kStage + Sm::kTile + tl * 128);
+            if (tb + kTc8Tok > t1) {
+                // last tile: V rows of tokens past the range (unused slot, missing block,
+                // stale tile) become 0, once the tile's V is in (its slot is not reused
+                // before this tile's P.V)
+                if (!mbar_wait(&vfull[st], (it / NST) & 1)) {
+                    if (lane == 0)
+                        atomicOr(p.err, PA_DEVERR_TIMEOUT);
+                    poisoned = aborted = true;
+                    break;
+                }
+                if (pos >= t1) {
+                    uint4* vrow = reinterpret_cast<uint4*>(smem + st * Sm::kStage + Sm::kTile + tl * 128);
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    vrow[c] = make_uint4(0u, 0u, 0u, 0u);
+                    for (int c = 0; c < 8; ++c)
+                        vrow[c] = make_uint4(0u, 0u, 0u, 0u);
+                }
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -603,30 +636,40 @@ __global__ void __launch_bounds__(kTc8Threads)
         if (poisoned)
             *poison = 1;
         named_barrier(2, 128);
-        const bool bad = *poison != 0;
         const float vs = p.v_scale[kvh] * (1.f / 256.f);   // P carried 256 p
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            if (orow[r] < 0)
-                continue;                            // padding row
             const float l = (red_l[r] + red_l[R + r]) + (red_l[2 * R + r] + red_l[3 * R + r]);
-            float out = l == 0.f ? 0.f : acc[r] / l * vs;   // NaN scores keep l NaN
-            if (bad)
-                out = __int_as_float(0x7fc00000);
-            if (split) {
-                const int64_t prow = orow[r] * p.max_parts + part;
-                p.part_o[prow * D + tl] = out;
-                if (tl == 0) {
-                    p.part_ml[prow * 2 + 0] = m[r];
-                    p.part_ml[prow * 2 + 1] = l;
-                }
-            } else {
-                store_out<T>(p, orow[r] * D + tl, out);
-            }
+            orow_e[r] = orow[r];
+            m_e[r] = m[r];
+            l_e[r] = l;
+            acc_e[r] = l == 0.f ? 0.f : acc[r] / l * vs;    // NaN scores keep l NaN
         }
         tc_fence_before();
     }
+    // every role is done: the producers' invalid-block flags are visible, the tensor
+    // memory is no longer read
     __syncthreads();
+    if (warp >= 2 && warp < 6) {
+        const bool bad = *poison != 0;
+        const int tl = 32 * (warp & 3) + lane;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (orow_e[r] < 0)
+                continue;                            // padding row
+            const float out = bad ? __int_as_float(0x7fc00000) : acc_e[r];
+            if (split) {
+                const int64_t prow = orow_e[r] * p.max_parts + part;
+                p.part_o[prow * D + tl] = out;
+                if (tl == 0) {
+                    p.part_ml[prow * 2 + 0] = m_e[r];
+                    p.part_ml[prow * 2 + 1] = l_e[r];
+                }
+            } else {
+                store_out<T>(p, orow_e[r] * D + tl, out);
+            }
+        }
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(*tslot, Sm::kTmemCols);
