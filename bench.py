@@ -38,9 +38,9 @@ WORKLOADS = {
     "opt13b": "OPT-13B-shaped decode layer: 64 seqs, 40 q / 40 kv heads, head_dim 128, fp16, "
               "block_size 16, context uniform in [1, 2048], N(0, 1)",
     "long16": "long-context split decode: 8 seqs x 32768 tokens, 64 q / 8 kv heads, head_dim 128, "
-              "bf16, block_size 16, 512-token partitions + reduce",
+              "bf16, block_size 16, split into partitions by the library + reduce",
     "long32": "long-context split decode: 8 seqs x 32768 tokens, 64 q / 8 kv heads, head_dim 128, "
-              "bf16, block_size 32, 512-token partitions + reduce",
+              "bf16, block_size 32, split into partitions by the library + reduce",
     "prefix": "shared-prefix decode: 16 groups x 8 seqs, 32 q / 8 kv heads, head_dim 128, bf16, "
               "block_size 16, 1024-token shared prefix, CoW tail copies each step",
 }
@@ -59,9 +59,12 @@ WORKLOADS["long16_chunk512"] = (
     "rows), 64 q / 8 kv heads, head_dim 128, bf16, block_size 16, N(0, 1)")
 WORKLOADS["llama13b_verify4_fp8"] = WORKLOADS["llama13b_verify4"] + \
     "; KV cache in FP8 E4M3 with per-head scales"
+WORKLOADS["long16_chunk512_fp8"] = WORKLOADS["long16_chunk512"] + \
+    "; KV cache in FP8 E4M3 with per-head scales"
 CHUNK_METRIC = {"llama13b_verify4": "paged verify attention KV GB/s",
                 "llama13b_verify4_fp8": "paged verify attention KV GB/s",
-                "long16_chunk512": "paged chunk attention TFLOP/s"}
+                "long16_chunk512": "paged chunk attention TFLOP/s",
+                "long16_chunk512_fp8": "paged chunk attention TFLOP/s"}
 # swapping (pa_swap_blocks): a preempted group's blocks out to pinned CPU memory and back
 WORKLOADS["llama13b_swap"] = (
     "KV swapping on the LLaMA-13B batch: every block of the last 64 of 256 sequences "
@@ -269,6 +272,30 @@ def launched_split(pa, w) -> bool:
     return pa.pa_decode_partition_tokens(w.q.dtype, w.k_cache.dtype, w.num_seqs, w.num_q_heads,
                                          w.num_kv_heads, w.head_dim, w.block_size,
                                          w.max_context_len, 0) > 0
+
+
+def dominant_kernel(w) -> str:
+    """The attention kernel the library runs for this workload (its routing rules:
+    E4M3 at head_dim 128 with at most four rows per kv head on the tcgen05 E4M3 decode;
+    at least four query heads, or a short chunk, per kv head on the mma.sync decode;
+    long chunks on the tcgen05 chunk kernel; otherwise the CUDA-core decode)."""
+    group = w.num_q_heads // w.num_kv_heads
+    if w.query_start is not None:
+        rows = w.max_query_len * group
+        if w.fp8 or rows <= 32:
+            nh = 4 if rows <= 4 else 8
+            if w.fp8 and w.head_dim == 128 and nh <= 4:
+                return "decode_tc8_kernel (chunk rows)"
+            return "decode_mma_kernel (chunk rows)"
+        return "chunk_attn_kernel"
+    gc = next(g for g in (8, 4, 2, 1) if group % g == 0)
+    if w.fp8:
+        if w.head_dim == 128 and gc <= 4:
+            return "decode_tc8_kernel"
+        return "decode_mma_kernel" if gc >= 4 else "decode_kernel"
+    if w.dtype != torch.float32 and gc >= 4:
+        return "decode_mma_kernel"
+    return "decode_kernel"
 
 
 def step_ops(pa, w):
@@ -618,8 +645,7 @@ def run_ours(args, rank, world, local):
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": recorded_traffic(args.config),
-                "kernel": ("chunk_attn_kernel" if chunk else "decode_kernel")
-                + (" + reduce kernel" if split else ""),
+                "kernel": dominant_kernel(w) + (" + reduce kernel" if split else ""),
                 "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": nbytes["decode"]}
@@ -756,7 +782,8 @@ def _chunk_rows(h, w, s, j0, j1, threads) -> int:
                            h["block_tables"][s:s + 1],
                            torch.tensor([L - n + j1], dtype=torch.int32),
                            torch.tensor([0, j1 - j0], dtype=torch.int32), w.scale,
-                           w.num_kv_heads, w.block_size, num_threads=threads)
+                           w.num_kv_heads, w.block_size, num_threads=threads,
+                           k_scale=h.get("k_scale"), v_scale=h.get("v_scale"))
     return 4 * w.head_dim * w.num_q_heads * sum(L - n + j + 1 for j in range(j0, j1))
 
 

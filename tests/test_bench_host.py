@@ -59,3 +59,24 @@ def test_two_gloo_ranks_take_the_max():
         assert p.exitcode == 0
     assert [r[1] for r in res] == [1.5, 1.5]
     assert all(abs(r[2] - 200 / 1.5) < 1e-9 for r in res)
+
+
+def test_chunk_oracle_sample_runs_on_e4m3_caches():
+    """The CPU baseline of a chunk workload over E4M3 caches passes the per-head scales
+    (the oracle refuses an E4M3 cache without them)."""
+    w = workloads.to_fp8(workloads.make("long16_chunk512", num_seqs=1, context=300,
+                                        query_len=40))
+    value, unit, desc = bench._chunk_sample(w, bench._host_inputs(w), 0.2, 1)
+    assert value > 0 and unit in ("TFLOP/s", "GB/s") and "oracle" in desc
+
+
+def test_dominant_kernel_follows_the_library_routing():
+    def label(config, **kw):
+        return bench.dominant_kernel(bench.make_workload(config, "cpu", **kw))
+    assert label("llama13b", num_seqs=2) == "decode_kernel"                 # MHA, CUDA cores
+    assert label("long16", num_seqs=1) == "decode_mma_kernel"               # group 8
+    assert label("llama13b_fp8", num_seqs=2) == "decode_tc8_kernel"         # E4M3 MHA
+    assert label("long16_fp8", num_seqs=1) == "decode_mma_kernel"           # E4M3, 8 rows
+    assert label("llama13b_verify4_fp8", num_seqs=2) == "decode_tc8_kernel (chunk rows)"
+    assert label("llama13b_verify4", num_seqs=2) == "decode_mma_kernel (chunk rows)"
+    assert label("long16_chunk512", num_seqs=1) == "chunk_attn_kernel"
