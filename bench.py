@@ -278,16 +278,17 @@ def dominant_kernel(w) -> str:
     """The attention kernel the library runs for this workload (its routing rules:
     E4M3 at head_dim 128 with at most four rows per kv head on the tcgen05 E4M3 decode;
     at least four query heads, or a short chunk, per kv head on the mma.sync decode;
-    long chunks on the tcgen05 chunk kernel; otherwise the CUDA-core decode)."""
+    long chunks on the tcgen05 chunk kernel (over E4M3 caches at head_dim 128 through
+    an f16 conversion stage); otherwise the CUDA-core decode)."""
     group = w.num_q_heads // w.num_kv_heads
     if w.query_start is not None:
         rows = w.max_query_len * group
-        if w.fp8 or rows <= 32:
+        if rows <= 32 or (w.fp8 and w.head_dim != 128):
             nh = 4 if rows <= 4 else 8
             if w.fp8 and w.head_dim == 128 and nh <= 4:
                 return "decode_tc8_kernel (chunk rows)"
             return "decode_mma_kernel (chunk rows)"
-        return "chunk_attn_kernel"
+        return "chunk_attn_kernel" + (" (E4M3 tiles converted to f16)" if w.fp8 else "")
     gc = next(g for g in (8, 4, 2, 1) if group % g == 0)
     if w.fp8:
         if w.head_dim == 128 and gc <= 4:

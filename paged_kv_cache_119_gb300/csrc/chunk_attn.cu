@@ -1,17 +1,20 @@
-// chunk_attn.cu -- host launchers of chunk attention for f16 and bf16 caches
-// (head_dim 64 / 128, block_size 16 / 32): the tcgen05 kernel of chunk_attn.cuh
-// for long chunks, and the mma.sync decode kernel in its chunk-row mode
-// (decode_mma.cuh) when a kv head has only a few (token, head) rows.
+// chunk_attn.cu -- host launchers of chunk attention (head_dim 64 / 128, block_size
+// 16 / 32): the tcgen05 kernel of chunk_attn.cuh for long chunks (f16 and bf16 caches,
+// and E4M3 caches at head_dim 128 through an f16 conversion stage), and the decode
+// kernels' chunk-row modes when a kv head has only a few (token, head) rows.
 #include "chunk_attn.cuh"
 #include "decode_mma.cuh"
 
 namespace pa {
 
-template <typename T, int D, int BS>
+// F8: E4M3 caches (head_dim 128): three 16-bit stages and four raw one-byte stages.
+template <typename T, int D, int BS, bool F8 = false>
 struct ChunkVariant {
-    static constexpr int kStages = ChunkStages<D>::value;
-    using Sm = ChunkSmem<D, kStages>;
-    static constexpr auto kernel() { return chunk_attn_kernel<T, D, BS, kStages>; }
+    static constexpr int kStages = F8 ? 3 : ChunkStages<D>::value;
+    static constexpr int kRaw = F8 ? 4 : 0;
+    static constexpr int kThreads = F8 ? kChunkThreadsF8 : kChunkThreads;
+    using Sm = ChunkSmem<D, kStages, kRaw>;
+    static constexpr auto kernel() { return chunk_attn_kernel<T, D, BS, kStages, kRaw>; }
     static cudaError_t configure()
     {
         return configure_once(reinterpret_cast<const void*>(kernel()), Sm::kAlloc);
@@ -24,7 +27,7 @@ struct ChunkVariant {
             return err;
         const bool split = p.partition_tokens > 0;
         const dim3 grid(split ? p.max_parts : 1, p.num_kv_heads * p.m_tiles, p.num_seqs);
-        kernel()<<<grid, kChunkThreads, Sm::kAlloc, stream>>>(p, tk, tv);
+        kernel()<<<grid, kThreads, Sm::kAlloc, stream>>>(p, tk, tv);
         err = cudaGetLastError();
         if (err != cudaSuccess || !split)
             return err;
@@ -35,7 +38,7 @@ struct ChunkVariant {
     {
         int n = 0;
         if (configure() != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel(), kChunkThreads, Sm::kAlloc) !=
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel(), kThreads, Sm::kAlloc) !=
                 cudaSuccess)
             return 0;
         return n;
@@ -175,6 +178,35 @@ int occupancy_chunk_attention(pa_dtype dtype, int head_dim, int block_size)
         PA_CHUNK_VARIANTS(PA_CHUNK_OCC)
     }
 #undef PA_CHUNK_OCC
+    return 0;
+}
+
+cudaError_t launch_chunk_attention_fp8(const ChunkParams& p, pa_dtype q_dtype, int block_size,
+                                       const CUtensorMap& tk, const CUtensorMap& tv,
+                                       cudaStream_t stream)
+{
+#define PA_CHUNK_F8_CASE(BS_)                                                                   \
+    if (block_size == BS_)                                                                     \
+        return q_dtype == PA_BF16                                                              \
+                   ? ChunkVariant<__nv_bfloat16, 128, BS_, true>::launch(p, tk, tv, stream)    \
+                   : ChunkVariant<__half, 128, BS_, true>::launch(p, tk, tv, stream);
+    if (q_dtype == PA_BF16 || q_dtype == PA_F16) {
+        PA_CHUNK_F8_CASE(16) PA_CHUNK_F8_CASE(32)
+    }
+#undef PA_CHUNK_F8_CASE
+    return cudaErrorInvalidValue;
+}
+
+int occupancy_chunk_attention_fp8(pa_dtype q_dtype, int block_size)
+{
+#define PA_CHUNK_F8_OCC(BS_)                                                    \
+    if (block_size == BS_)                                                     \
+        return q_dtype == PA_BF16 ? ChunkVariant<__nv_bfloat16, 128, BS_, true>::occupancy() \
+                                  : ChunkVariant<__half, 128, BS_, true>::occupancy();
+    if (q_dtype == PA_BF16 || q_dtype == PA_F16) {
+        PA_CHUNK_F8_OCC(16) PA_CHUNK_F8_OCC(32)
+    }
+#undef PA_CHUNK_F8_OCC
     return 0;
 }
 

@@ -46,6 +46,8 @@
 
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 #include "tc_device.cuh"
@@ -57,10 +59,14 @@ constexpr int kChunkRows = 128;      // M of the tensor-core tile
 constexpr int kChunkTileTok = 64;    // tokens per K/V tile (N of the score product)
 constexpr int kChunkSoftmaxWarps = 4 * kChunkQTiles;
 // warps: 0 producer, 1 tensor-memory allocator + MMA issuer of query tile 0, 2-9
-// softmax, 10 MMA issuer of query tile 1
+// softmax, 10 MMA issuer of query tile 1; over E4M3 caches, 11-12 convert tiles to f16
 constexpr int kChunkThreads = 64 + 32 * kChunkSoftmaxWarps + 32;
+constexpr int kChunkConvWarps = 2;
+constexpr int kChunkThreadsF8 = kChunkThreads + 32 * kChunkConvWarps;
 
-template <int D, int NST>
+// NRAW > 0 (E4M3 caches): a ring of NRAW raw one-byte K + V tiles that the converter
+// warps turn into the 16-bit tiles of the NST-stage ring.
+template <int D, int NST, int NRAW = 0>
 struct ChunkSmem {
     static constexpr int kHalves = D / 64;                       // 128-byte column groups
     static constexpr int kQHalf = kChunkRows * 128;              // 16 KB
@@ -70,12 +76,15 @@ struct ChunkSmem {
     static constexpr int kStageBytes = 2 * kKBytes;              // K then V
     static constexpr int kQOff = 0;
     static constexpr int kStageOff = kQOff + kChunkQTiles * kQTile;
-    static constexpr int kBarOff = kStageOff + NST * kStageBytes;
+    static constexpr int kRawTile = kChunkTileTok * D;           // one E4M3 K (or V) tile
+    static constexpr int kRawStage = 2 * kRawTile;
+    static constexpr int kRawOff = kStageOff + NST * kStageBytes;
+    static constexpr int kBarOff = kRawOff + NRAW * kRawStage;
     // full[NST], empty[NST], s_full[2][2], p_full[2][2], pv_done[2], q_full, mma_done[2],
-    // v_zero
-    static constexpr int kNumBars = 2 * NST + 14;
-    static constexpr int kOkOff = kBarOff + 8 * kNumBars;        // stage_ok[NST]
-    static constexpr int kSlotOff = kOkOff + 4 * NST;            // TMEM address
+    // v_zero, raw_full[NRAW], raw_empty[NRAW]
+    static constexpr int kNumBars = 2 * NST + 14 + 2 * NRAW;
+    static constexpr int kOkOff = kBarOff + 8 * kNumBars;        // stage_ok[NST], raw_ok[NRAW]
+    static constexpr int kSlotOff = kOkOff + 4 * (NST + NRAW);   // TMEM address
     static constexpr int kBytes = kSlotOff + 16;
     static constexpr int kAlloc = kBytes + 1024;                 // 1 KB alignment slack
     // tensor memory: O of query tile q at column 128 q, its two S/P buffers at
@@ -83,6 +92,8 @@ struct ChunkSmem {
     static constexpr int kTmemCols = 512;
     static constexpr int kSCol = 256;
     static_assert(D <= 128, "O must fit in 128 columns");
+    static_assert(NRAW == 0 || D == 128, "E4M3 tiles need 128-byte rows");
+    static_assert(kRawTile % 1024 == 0, "swizzle atoms need 1 KB alignment");
     static_assert(kAlloc <= 227 * 1024, "shared memory");
 };
 
@@ -150,17 +161,23 @@ __device__ __forceinline__ void split_pair(float p0, float p1, uint32_t& hi, uin
     }
 }
 
-// grid = (partitions, num_kv_heads * m_tiles, num_seqs); kChunkThreads threads.
-template <typename T, int D, int BS, int NST>
-__global__ void __launch_bounds__(kChunkThreads, 1)
+// grid = (partitions, num_kv_heads * m_tiles, num_seqs); kChunkThreads threads, or
+// kChunkThreadsF8 over E4M3 caches (NRAW > 0).  T: query / native output type.  Over
+// E4M3 caches (value = code * per-kv-head scale) the tensor-core operands are f16: the
+// codes convert exactly, a bf16 query row is scaled into f16 range by a power of two
+// (exact), and the scales fold into the scores and the output.
+template <typename T, int D, int BS, int NST, int NRAW = 0>
+__global__ void __launch_bounds__(NRAW > 0 ? kChunkThreadsF8 : kChunkThreads, 1)
     chunk_attn_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv)
 {
-    using Sm = ChunkSmem<D, NST>;
+    using Sm = ChunkSmem<D, NST, NRAW>;
+    constexpr bool kF8 = NRAW > 0;
+    using TM = std::conditional_t<kF8, __half, T>;   // tensor-core operand type
     constexpr int NT = kChunkTileTok;
     constexpr int BPT = NT / BS;                 // cache blocks per K/V tile
     constexpr int KS = D / 16;                   // k-steps of the score product
-    constexpr bool kBf16 = DType<T>::id == PA_BF16;
+    constexpr bool kBf16 = DType<TM>::id == PA_BF16;
     static_assert(NT % BS == 0 && D % 64 == 0, "block_size 16/32, head_dim 64/128");
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -174,7 +191,10 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     uint64_t* q_full = pv_done + 2;
     uint64_t* mma_done = q_full + 1;             // [query tile]
     uint64_t* v_zero = mma_done + 2;             // the last tile's V rows past the range are 0
+    uint64_t* raw_full = v_zero + 1;             // [raw slot] (E4M3 caches)
+    uint64_t* raw_empty = raw_full + NRAW;
     int* stage_ok = reinterpret_cast<int*>(smem + Sm::kOkOff);
+    int* raw_ok = stage_ok + NST;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Sm::kSlotOff);
 
     const int warp = threadIdx.x >> 5;
@@ -231,8 +251,13 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
     if (threadIdx.x == 0) {
 #pragma unroll
         for (int s = 0; s < NST; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], kF8 ? kChunkConvWarps : 1);   // converters, or the TMA
             mbar_init(&empty[s], kChunkQTiles);          // one commit per issuer
+        }
+#pragma unroll
+        for (int s = 0; s < NRAW; ++s) {
+            mbar_init(&raw_full[s], 1);
+            mbar_init(&raw_empty[s], kChunkConvWarps);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -266,9 +291,14 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         const int32_t* bt_row = p.block_tables + (int64_t)seq * p.bt_stride;
         const uint64_t policy = l2_evict_first_policy();
         const int blk_end = (t1 + BS - 1) / BS;
+        // 16-bit caches fill the MMA ring directly; E4M3 caches fill the raw ring
+        constexpr int NP = kF8 ? NRAW : NST;
+        uint64_t* pfull = kF8 ? raw_full : full;
+        uint64_t* pempty = kF8 ? raw_empty : empty;
+        int* pok = kF8 ? raw_ok : stage_ok;
         int issued = 0;
         for (int it = 0; it < ntiles; ++it) {
-            const int st = it % NST;
+            const int st = it % NP;
             const int b0 = (t0 + it * NT) / BS;
             const int nb = min(BPT, blk_end - b0);
             int pbn = -1;
@@ -280,20 +310,27 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
             const unsigned vmask = __ballot_sync(kFullMask, valid);
             int ok = 1;
             if (lane == 0) {
-                if (it >= NST && !mbar_wait(&empty[st], ((it / NST) - 1) & 1)) {
+                if (it >= NP && !mbar_wait(&pempty[st], ((it / NP) - 1) & 1)) {
                     atomicOr(p.err, PA_DEVERR_TIMEOUT);
                     ok = 0;
                 } else {
                     const int nvalid = __popc(vmask);
-                    stage_ok[st] = nvalid == nb ? 1 : 0;
+                    pok[st] = nvalid == nb ? 1 : 0;
                     if (nvalid != nb)
                         atomicOr(p.err, PA_DEVERR_BLOCK_ID);
-                    mbar_arrive_expect_tx(&full[st], (uint32_t)nvalid * 2u * Sm::kHalves * BS * 128u);
+                    // a block is one 128-byte-row box per 64 dims (16-bit) or per 128 codes
+                    mbar_arrive_expect_tx(&pfull[st],
+                                          (uint32_t)nvalid * 2u * (kF8 ? 1 : Sm::kHalves) * BS * 128u);
                 }
             }
             if (!__shfl_sync(kFullMask, ok, 0))
                 break;
-            if (valid) {
+            if (kF8 && valid) {
+                unsigned char* kdst = smem + Sm::kRawOff + st * Sm::kRawStage + lane * (BS * 128);
+                const int z = pbn * p.num_kv_heads + kvh;     // < 2^31 (checked on the host)
+                tma_load_3d(kdst, &tk, 0, 0, z, &pfull[st], policy);
+                tma_load_3d(kdst + Sm::kRawTile, &tv, 0, 0, z, &pfull[st], policy);
+            } else if (valid) {
                 unsigned char* kdst = smem + Sm::kStageOff + st * Sm::kStageBytes + lane * (BS * 128);
                 const int z = pbn * p.num_kv_heads + kvh;     // < 2^31 (checked on the host)
 #pragma unroll
@@ -307,9 +344,59 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         }
         // no copy may still be in flight into this CTA's shared memory at exit
         if (lane == 0)
-            for (int it = max(0, issued - NST); it < issued; ++it)
-                mbar_wait(&full[it % NST], (it / NST) & 1);
+            for (int it = max(0, issued - NP); it < issued; ++it)
+                mbar_wait(&pfull[it % NP], (it / NP) & 1);
         __syncwarp();
+    } else if (kF8 && warp > 2 + kChunkSoftmaxWarps) {
+        // ------------------------------------------------ E4M3 -> f16 tile conversion
+        // A raw tile row is 128 codes in 128-byte-swizzled order (16-byte chunk c of row
+        // t at c ^ (t & 7)); the f16 tile is two 64-dim halves of 128-byte rows in the
+        // same swizzle.  Each (token, 16-code chunk) item becomes two f16 chunks.
+        if constexpr (kF8) {
+            const int ct = threadIdx.x - kChunkThreads;      // 0 .. 32 * kChunkConvWarps - 1
+            constexpr int kItems = NT * 8;                   // per K (or V) tile
+            for (int it = 0; it < ntiles; ++it) {
+                const int r = it % NRAW;
+                const int st = it % NST;
+                bool ok = mbar_wait(&raw_full[r], (it / NRAW) & 1);
+                if (ok && it >= NST)
+                    ok = mbar_wait(&empty[st], ((it / NST) - 1) & 1);   // both issuers' P.V
+                if (!ok) {
+                    if (lane == 0)
+                        atomicOr(p.err, PA_DEVERR_TIMEOUT);
+                    break;
+                }
+                const unsigned char* raw = smem + Sm::kRawOff + r * Sm::kRawStage;
+                unsigned char* dst = smem + Sm::kStageOff + st * Sm::kStageBytes;
+#pragma unroll
+                for (int kv = 0; kv < 2; ++kv) {
+#pragma unroll 4
+                    for (int item = ct; item < kItems; item += 32 * kChunkConvWarps) {
+                        const int t = item >> 3;
+                        const int c = item & 7;
+                        const uint4 w = *reinterpret_cast<const uint4*>(
+                            raw + kv * Sm::kRawTile + t * 128 + ((c ^ (t & 7)) << 4));
+                        unsigned char* row =
+                            dst + kv * Sm::kKBytes + (c >> 2) * Sm::kKVHalf + t * 128;
+                        const int c0 = 2 * (c & 3);
+                        *reinterpret_cast<uint4*>(row + ((c0 ^ (t & 7)) << 4)) =
+                            make_uint4(e4m3x2_to_f16x2(w.x), e4m3x2_to_f16x2(w.x >> 16),
+                                       e4m3x2_to_f16x2(w.y), e4m3x2_to_f16x2(w.y >> 16));
+                        *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (t & 7)) << 4)) =
+                            make_uint4(e4m3x2_to_f16x2(w.z), e4m3x2_to_f16x2(w.z >> 16),
+                                       e4m3x2_to_f16x2(w.w), e4m3x2_to_f16x2(w.w >> 16));
+                    }
+                }
+                fence_proxy_async_smem();                    // f16 tiles -> tensor core
+                __syncwarp();
+                if (lane == 0) {
+                    if (warp == 3 + kChunkSoftmaxWarps)
+                        stage_ok[st] = raw_ok[r];
+                    mbar_arrive(&full[st]);
+                    mbar_arrive(&raw_empty[r]);
+                }
+            }
+        }
     } else if (warp == 1 || warp == 2 + kChunkSoftmaxWarps) {
         // ------------------------------------------- MMA issue, one query tile per warp
         const int q = warp == 1 ? 0 : 1;
@@ -386,21 +473,57 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         const int pos = pos_first + tok;
         const int64_t qrow = (int64_t)(qs0 + j0 + tok) * p.num_q_heads + (int64_t)kvh * G + g;
         // scores are used as s * sl2 with sl2 > 0: a negative scale flips the sign of q
-        // (exact), a zero scale makes q zero (every score 0)
-        const float sl2_raw = p.scale_log2;
+        // (exact), a zero scale makes q zero (every score 0); over E4M3 caches the K scale
+        // of the kv head joins the softmax scale
+        const float sl2_raw = kF8 ? p.scale_log2 * p.k_scale[kvh] : p.scale_log2;
         const uint32_t qflip = sl2_raw < 0.f ? 0x80008000u : 0u;
         const bool qzero = sl2_raw == 0.f;
-        const float sl2 = qzero ? 1.f : fabsf(sl2_raw);
+        float sl2 = qzero ? 1.f : fabsf(sl2_raw);
         {
             // Q rows into the 128-byte-swizzled operand layout; rows past the chunk are 0
             const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
                                                               (row_valid ? qrow : 0) * D);
             unsigned char* qdst = smem + Sm::kQOff + q * Sm::kQTile + rr * 128;
+            constexpr bool kToF16 = kF8 && DType<T>::id == PA_BF16;
+            float down = 1.f;
+            if constexpr (kToF16) {
+                // a bf16 row becomes f16 operands: a power of two 2^-e puts its largest
+                // |q| in [2^14, 2^15), so the 8-bit mantissas convert exactly; 2^e goes
+                // into the row's score scale
+                float amax = 0.f;
+                if (row_valid && !qzero) {
+#pragma unroll 4
+                    for (int c = 0; c < D / 8; ++c) {
+                        const uint4 v = __ldg(src + c);
+                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[j] << 16)),
+                                                     fabsf(__uint_as_float(w[j] & 0xffff0000u))));
+                    }
+                }
+                const int ex = (__float_as_int(amax) >> 23) & 0xff;   // biased exponent
+                // amax in [2^(ex-127), 2^(ex-126)): scale by 2^(141 - ex); rows of zeros,
+                // tiny rows and a NaN / infinite row keep the scale 1
+                const int sh = (ex == 0 || ex == 255) ? 0 : max(-100, min(100, 141 - ex));
+                down = __int_as_float((127 + sh) << 23);
+                sl2 *= __int_as_float((127 - sh) << 23);
+            }
 #pragma unroll
             for (int c = 0; c < D / 8; ++c) {
                 uint4 v = make_uint4(0u, 0u, 0u, 0u);
                 if (row_valid && !qzero) {
                     v = __ldg(src + c);
+                    if constexpr (kToF16) {
+                        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const __half2 h = __floats2half2_rn(__uint_as_float(w[j] << 16) * down,
+                                                                __uint_as_float(w[j] & 0xffff0000u) * down);
+                            w[j] = *reinterpret_cast<const uint32_t*>(&h);
+                        }
+                        v = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
                     v.x ^= qflip;
                     v.y ^= qflip;
                     v.z ^= qflip;
@@ -505,7 +628,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
                 uint32_t hl[NT];
 #pragma unroll
                 for (int k = 0; k < NT / 2; ++k)
-                    split_pair<T>(s[2 * k], s[2 * k + 1], hl[k], hl[NT / 2 + k]);
+                    split_pair<TM>(s[2 * k], s[2 * k + 1], hl[k], hl[NT / 2 + k]);
                 tmem_st64_raw(sp_col, hl);
             }
             if (tb + NT > t1) {
@@ -545,7 +668,8 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
         }
         tc_fence_after();
         if (warp_live) {
-            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            // over E4M3 caches the V scale of the kv head multiplies the output
+            const float inv = lsum > 0.f ? (kF8 ? p.v_scale[kvh] : 1.f) / lsum : 0.f;
             const int which = (split || p.out_f32) ? 0 : (DType<T>::id == PA_F16 ? 1 : 2);
 #pragma unroll 1
             for (int c4 = 0; c4 < D / 32; ++c4) {

@@ -55,14 +55,6 @@ __device__ __forceinline__ uint32_t lds_u32(uint32_t addr)
     return v;
 }
 
-// Two E4M3 codes (low 16 bits, low byte first) as an f16x2 operand word; exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
-{
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xffffu),
-                                                     __NV_E4M3);
-    return *reinterpret_cast<const uint32_t*>(&h);
-}
-
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
 {
     uint32_t y;

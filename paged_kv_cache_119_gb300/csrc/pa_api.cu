@@ -310,10 +310,11 @@ int decode_partition(pa_dtype q_dtype, pa_dtype kv_dtype, int num_seqs, int num_
                             (int64_t)device_sm_count() * occ, block_size);
 }
 
-// How pa_chunk_attention runs a call: few (token, head) rows per kv head go to the
-// mma.sync decode kernel in chunk-row mode (nh rows per CTA), longer chunks to the
-// tcgen05 kernel (rows_tokens chunk tokens per CTA); partition = split length.  E4M3
-// caches always take the chunk-row path (its kernel reads E4M3 tiles directly).
+// How pa_chunk_attention runs a call: few (token, head) rows per kv head go to a decode
+// kernel in chunk-row mode (nh rows per CTA), longer chunks to the tcgen05 chunk kernel
+// (rows_tokens chunk tokens per CTA; over E4M3 caches with an f16 conversion stage, at
+// head_dim 128 -- E4M3 at head_dim 64 always takes the chunk-row path); partition =
+// split length.
 struct ChunkPlan {
     bool rows_path;
     int nh;          // rows per CTA on the decode kernel
@@ -330,7 +331,7 @@ ChunkPlan chunk_plan(pa_dtype q_dtype, pa_dtype kv_dtype, int num_seqs, int num_
     const int group = num_q_heads / num_kv_heads;
     const int64_t rows = (int64_t)max_query_len * group;
     const bool fp8 = kv_dtype == PA_FP8_E4M3;
-    if (rows <= kChunkRowsMax || fp8) {
+    if (rows <= kChunkRowsMax || (fp8 && head_dim != 128)) {
         c.rows_path = true;
         c.nh = rows <= 4 ? 4 : 8;
         c.chunks = (int)std::min<int64_t>((rows + c.nh - 1) / c.nh, INT32_MAX);
@@ -350,7 +351,8 @@ ChunkPlan chunk_plan(pa_dtype q_dtype, pa_dtype kv_dtype, int num_seqs, int num_
     c.chunks = (max_query_len + c.rows_tokens - 1) / c.rows_tokens;
     int occ = 0;
     if (partition_size == 0)
-        occ = occupancy_chunk_attention(kv_dtype, head_dim, block_size);
+        occ = fp8 ? occupancy_chunk_attention_fp8(q_dtype, block_size)
+                  : occupancy_chunk_attention(kv_dtype, head_dim, block_size);
     c.partition = choose_chunk_partition(partition_size, max_context_len,
                                          (int64_t)num_seqs * num_kv_heads * c.chunks,
                                          (int64_t)device_sm_count() * occ);
@@ -626,6 +628,8 @@ static int chunk_impl(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_d
         p.part_o = static_cast<float*>(workspace);
         p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ml_off);
     }
+    p.k_scale = fp8 ? k_scale : nullptr;
+    p.v_scale = fp8 ? v_scale : nullptr;
     p.err = device_error_word();
     if (!p.err)
         return PA_ERR_CUDA;
@@ -673,6 +677,9 @@ static int chunk_impl(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_d
                                         static_cast<cudaStream_t>(stream))
                 : launch_chunk_rows(d, p, kv_dtype, head_dim, block_size, plan.nh, tk, tv,
                                     static_cast<cudaStream_t>(stream));
+    } else if (fp8) {
+        e = launch_chunk_attention_fp8(p, q_dtype, block_size, tk, tv,
+                                       static_cast<cudaStream_t>(stream));
     } else {
         e = launch_chunk_attention(p, kv_dtype, head_dim, block_size, tk, tv,
                                    static_cast<cudaStream_t>(stream));

@@ -171,6 +171,8 @@ struct ChunkParams {
     const int32_t* query_start;  // [num_seqs + 1]
     float* part_o;               // [num_rows][Hq][max_parts][D] (split only)
     float* part_ml;              // [num_rows][Hq][max_parts][2]
+    const float* k_scale;        // [Hkv] scales of E4M3 caches, else null
+    const float* v_scale;
     unsigned* err;
     int64_t num_blocks;
     int64_t bt_stride;
@@ -193,6 +195,13 @@ cudaError_t launch_chunk_attention(const ChunkParams& p, pa_dtype dtype, int hea
                                    cudaStream_t stream);
 // Resident chunk-attention CTAs per SM (0 if unknown).
 int occupancy_chunk_attention(pa_dtype dtype, int head_dim, int block_size);
+// The same kernel over E4M3 caches (head_dim 128; q_dtype F16 or BF16; p.k_scale and
+// p.v_scale set): the tiles are converted to f16 in shared memory; tk / tv are the
+// E4M3 tensor maps.
+cudaError_t launch_chunk_attention_fp8(const ChunkParams& p, pa_dtype q_dtype, int block_size,
+                                       const CUtensorMap& tk, const CUtensorMap& tv,
+                                       cudaStream_t stream);
+int occupancy_chunk_attention_fp8(pa_dtype q_dtype, int block_size);
 // Few rows per kv head: the mma.sync decode kernel in chunk-row mode, `nh` (4 or 8)
 // rows per CTA; p carries the chunk fields (query_start, num_rows, max_query_len)
 // and p.chunks = row chunks per kv head; cp describes the same call for the merge.

@@ -80,3 +80,5 @@ def test_dominant_kernel_follows_the_library_routing():
     assert label("llama13b_verify4_fp8", num_seqs=2) == "decode_tc8_kernel (chunk rows)"
     assert label("llama13b_verify4", num_seqs=2) == "decode_mma_kernel (chunk rows)"
     assert label("long16_chunk512", num_seqs=1) == "chunk_attn_kernel"
+    assert label("long16_chunk512_fp8", num_seqs=1) == \
+        "chunk_attn_kernel (E4M3 tiles converted to f16)"

@@ -324,3 +324,39 @@ def test_fp8_chunks(Hq, Hkv, nmax, D, B, qdtype):
 def test_fp8_chunk_splits_and_native_output(part):
     w = make_case(41, 3, 32, 8, 128, 16, torch.bfloat16, [2500, 300, 40], [4, 2, 4])
     run_and_compare_fp8(workloads.to_fp8(w), out_dtype=torch.bfloat16, partition_size=part)
+
+
+# ------------------------------------- long chunks over E4M3 caches (tcgen05, f16 stage)
+
+@pytest.mark.parametrize("Hq,Hkv,nmax", [(32, 4, 100), (64, 8, 70), (40, 40, 40)])
+@pytest.mark.parametrize("B", [16, 32])
+@pytest.mark.parametrize("qdtype", [torch.bfloat16, torch.float16])
+def test_fp8_long_chunks_on_tensor_cores(Hq, Hkv, nmax, B, qdtype):
+    """More than 32 (token, head) rows per kv head over an E4M3 cache at head_dim 128:
+    the tcgen05 chunk kernel with its E4M3 -> f16 conversion stage (ragged chunks,
+    several 128-row query tiles, contexts from one tile to many)."""
+    rng = np.random.default_rng(Hq + 7 * nmax + B)
+    lens = [nmax, 3000, 700, 130, 64, 65]
+    chunks = [nmax, nmax, int(rng.integers(33, nmax + 1)), nmax // 2, 40, 1]
+    chunks = [min(c, L) for c, L in zip(chunks, lens)]
+    w = make_case(int(rng.integers(1 << 30)), len(lens), Hq, Hkv, 128, B, qdtype, lens, chunks)
+    run_and_compare_fp8(workloads.to_fp8(w))
+
+
+@pytest.mark.parametrize("part", [0, 64, 192, -1])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_fp8_long_chunk_splits_and_native_output(part, out_dtype):
+    w = make_case(43, 3, 64, 8, 128, 16, torch.bfloat16, [4100, 900, 200], [96, 64, 40])
+    run_and_compare_fp8(workloads.to_fp8(w), out_dtype=out_dtype, partition_size=part)
+
+
+def test_fp8_long_chunk_query_magnitudes():
+    """Rows of very different size: each bf16 row is scaled into f16 by its own power
+    of two before it meets the converted E4M3 tiles."""
+    w = workloads.to_fp8(make_case(47, 2, 32, 4, 128, 16, torch.bfloat16, [600, 300], [80, 50]))
+    q = w.q.float()
+    q[:10] *= 3e4
+    q[10:20] *= 1e-6
+    w.q.copy_(q.to(torch.bfloat16))
+    w.scale = w.scale / 3e4 * 10        # keep the large rows' scores moderate
+    run_and_compare_fp8(w)
