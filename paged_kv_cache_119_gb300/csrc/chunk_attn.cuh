@@ -59,9 +59,9 @@ constexpr int kChunkRows = 128;      // M of the tensor-core tile
 constexpr int kChunkTileTok = 64;    // tokens per K/V tile (N of the score product)
 constexpr int kChunkSoftmaxWarps = 4 * kChunkQTiles;
 // warps: 0 producer, 1 tensor-memory allocator + MMA issuer of query tile 0, 2-9
-// softmax, 10 MMA issuer of query tile 1; over E4M3 caches, 11-12 convert tiles to f16
+// softmax, 10 MMA issuer of query tile 1; over E4M3 caches, 11-14 convert tiles to f16
 constexpr int kChunkThreads = 64 + 32 * kChunkSoftmaxWarps + 32;
-constexpr int kChunkConvWarps = 2;
+constexpr int kChunkConvWarps = 4;
 constexpr int kChunkThreadsF8 = kChunkThreads + 32 * kChunkConvWarps;
 
 // NRAW > 0 (E4M3 caches): a ring of NRAW raw one-byte K + V tiles that the converter
