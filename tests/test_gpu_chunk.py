@@ -360,3 +360,50 @@ def test_fp8_long_chunk_query_magnitudes():
     w.q.copy_(q.to(torch.bfloat16))
     w.scale = w.scale / 3e4 * 10        # keep the large rows' scores moderate
     run_and_compare_fp8(w)
+
+
+def _sampled_rows_fp8(w, picks):
+    """Checks rows (s, j) of a chunk step over E4M3 caches one by one against the oracle,
+    each as a one-row chunk ending at its position."""
+    ks, vs = w.meta["k_scale"], w.meta["v_scale"]
+    P.pa_reshape_and_cache_fp8(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping, ks, vs)
+    out = torch.empty(w.q.shape, dtype=torch.float32, device="cuda")
+    P.pa_chunk_attention_fp8(out, w.q, w.k_cache, w.v_cache, ks, vs, w.block_tables,
+                             w.context_lens, w.query_start, w.scale, w.num_kv_heads, w.block_size,
+                             max_query_len=w.max_query_len, max_context_len=w.max_context_len)
+    torch.cuda.synchronize()
+    assert P.pa_get_device_error() == 0
+    qs = w.query_start.cpu().tolist()
+    kc, vc = w.k_cache.view(torch.uint8).cpu(), w.v_cache.view(torch.uint8).cpu()
+    bt, cl = w.block_tables.cpu(), w.context_lens.cpu()
+    for s, j in picks:
+        L = int(cl[s]) - (qs[s + 1] - qs[s]) + j + 1
+        ref = oracle.chunk_attention(w.q[qs[s] + j:qs[s] + j + 1].cpu(), kc, vc, bt[s:s + 1],
+                                     torch.tensor([L], dtype=torch.int32),
+                                     torch.tensor([0, 1], dtype=torch.int32), w.scale,
+                                     w.num_kv_heads, w.block_size,
+                                     num_threads=oracle.max_threads(), k_scale=ks.cpu(),
+                                     v_scale=vs.cpu())
+        err = np.abs(out[qs[s] + j].double().cpu().numpy() - ref[0]).max()
+        assert err <= ATOL, (s, j, err)
+
+
+def test_fp8_chunk512_full_size_sampled_rows():
+    """The full 8 x 32768-token, 512-token chunk step over E4M3 caches (the tcgen05
+    kernel with its f16 conversion stage) at the benchmark's launch configuration."""
+    w = workloads.to_fp8(workloads.make("long16_chunk512", device="cuda"))
+    rng = np.random.default_rng(8)
+    picks = [(s, j) for s in rng.choice(w.num_seqs, size=2, replace=False).tolist()
+             for j in sorted(rng.choice(512, size=3, replace=False).tolist()) + [0, 511]]
+    _sampled_rows_fp8(w, picks)
+
+
+def test_fp8_verify4_full_batch_sampled_rows():
+    """The full 256-sequence verification step over E4M3 caches (decode_tc8_kernel's
+    chunk-row mode) at the benchmark's launch configuration."""
+    w = workloads.to_fp8(workloads.make("llama13b_verify4", device="cuda"))
+    rng = np.random.default_rng(9)
+    qs = w.query_start.cpu().tolist()
+    picks = [(s, j) for s in rng.choice(w.num_seqs, size=10, replace=False).tolist()
+             for j in range(qs[s + 1] - qs[s])]
+    _sampled_rows_fp8(w, picks)

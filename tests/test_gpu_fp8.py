@@ -130,3 +130,11 @@ def test_fp8_cache_write_rounds_and_saturates(src):
     nan_v = (vo & 0x7F) == 0x7F
     assert torch.equal(nan_v, (got_v & 0x7F) == 0x7F)
     assert torch.equal(got_v[~nan_v], vo[~nan_v])
+
+
+@pytest.mark.parametrize("name", ["llama13b", "opt13b", "prefix", "long16", "long32"])
+def test_fp8_config_full_size(name):
+    """The full workloads over E4M3 caches at the launch configuration the benchmark
+    times (automatic split), every output against the oracle."""
+    w = workloads.to_fp8(workloads.make(name, device="cuda"))
+    step_and_compare(w)
