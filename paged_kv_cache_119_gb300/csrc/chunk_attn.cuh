@@ -657,14 +657,13 @@ __global__ void __launch_bounds__(NRAW > 0 ? kChunkThreadsF8 : kChunkThreads, 1)
         }
 
         // ---------------------------------------------------------------- epilogue
-        // P.V of the last two tiles may both be pending (the loop waits for P.V only to
-        // rescale): wait for them in order, so no parity wait runs two phases behind
-        for (int it = max(0, ntiles - 2); it < ntiles; ++it) {
-            if (!mbar_wait(&pv_done[q], it & 1)) {
-                if (lane == 0)
-                    atomicOr(p.err, PA_DEVERR_TIMEOUT);
-                poisoned = true;
-            }
+        // every MMA of this query tile has completed once its issuer's final commit has
+        // (one phase, so no parity wait can alias: P.V of the last two tiles may be pending
+        // or done in any combination when a warp gets here)
+        if (!mbar_wait(&mma_done[q], 0)) {
+            if (lane == 0)
+                atomicOr(p.err, PA_DEVERR_TIMEOUT);
+            poisoned = true;
         }
         tc_fence_after();
         if (warp_live) {

@@ -350,16 +350,30 @@ def test_fp8_long_chunk_splits_and_native_output(part, out_dtype):
     run_and_compare_fp8(workloads.to_fp8(w), out_dtype=out_dtype, partition_size=part)
 
 
-def test_fp8_long_chunk_query_magnitudes():
-    """Rows of very different size: each bf16 row is scaled into f16 by its own power
-    of two before it meets the converted E4M3 tiles."""
-    w = workloads.to_fp8(make_case(47, 2, 32, 4, 128, 16, torch.bfloat16, [600, 300], [80, 50]))
+def _magnitude_case(fp8):
+    w = make_case(47, 2, 32, 4, 128, 16, torch.bfloat16, [600, 300], [80, 50])
+    if fp8:
+        w = workloads.to_fp8(w)
     q = w.q.float()
     q[:10] *= 3e4
     q[10:20] *= 1e-6
     w.q.copy_(q.to(torch.bfloat16))
     w.scale = w.scale / 3e4 * 10        # keep the large rows' scores moderate
-    run_and_compare_fp8(w)
+    return w
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_long_chunk_query_magnitudes(fp8):
+    """Rows of very different size (over E4M3 caches each bf16 row is scaled into f16 by
+    its own power of two).  The huge rows make their softmax warps rescale O on the last
+    tile and reach the epilogue late, when P.V of the last two tiles may both be done;
+    three runs, since that timing varies."""
+    for _ in range(3):
+        w = _magnitude_case(fp8)
+        if fp8:
+            run_and_compare_fp8(w)
+        else:
+            run_and_compare(w)
 
 
 def _sampled_rows_fp8(w, picks):
