@@ -175,3 +175,30 @@ def test_block_manager_drives_swap_out_and_in():
                                  torch.as_tensor(l1), 0.1, Hkv, B)
     assert np.abs(out1.double().cpu().numpy() - ref).max() <= 2e-3
     assert P.pa_get_device_error() == 0
+
+
+def test_swap_full_size_benchmark_step():
+    """The benchmark's swap step at full size: every block of the last 64 of 256
+    LLaMA-13B-shaped sequences, K and V, out to a pinned CPU pool in one launch and back
+    in one launch; every byte against the oracle's moves, and the pool unchanged after
+    the round trip."""
+    import bench
+    w = workloads.make("llama13b", device="cuda")
+    blocks, bb = bench.swap_plan(w, 64)
+    n = len(blocks)
+    cpu_k = torch.full((n,) + tuple(w.k_cache.shape[1:]), 7.0, dtype=w.dtype).pin_memory()
+    cpu_v = torch.full_like(cpu_k, 7.0).pin_memory()
+    out_pairs = torch.tensor([(b, i) for i, b in enumerate(blocks)], dtype=torch.int64)
+    before_k, before_v = w.k_cache.cpu(), w.v_cache.cpu()
+    want_k, want_v = cpu_k.clone(), cpu_v.clone()
+    oracle.swap_blocks([before_k, before_v], [want_k, want_v], out_pairs.numpy())
+    P.pa_swap_blocks([w.k_cache, w.v_cache], [cpu_k, cpu_v], out_pairs)
+    torch.cuda.synchronize()
+    assert torch.equal(raw(cpu_k), raw(want_k)) and torch.equal(raw(cpu_v), raw(want_v))
+    w.k_cache[blocks] = float("nan")              # the GPU blocks are reused meanwhile
+    w.v_cache[blocks] = float("nan")
+    P.pa_swap_blocks([cpu_k, cpu_v], [w.k_cache, w.v_cache], out_pairs.flip(1).contiguous())
+    torch.cuda.synchronize()
+    assert torch.equal(raw(w.k_cache.cpu()), raw(before_k))
+    assert torch.equal(raw(w.v_cache.cpu()), raw(before_v))
+    assert P.pa_get_device_error() == 0
