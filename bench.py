@@ -704,22 +704,37 @@ def run_ours(args, rank, world, local):
 
 def measure_e2e(args, pa, w, out, ws, part, dev):
     """Same step through the public API with per-step inputs in pinned host memory:
-    H2D of q, new K/V, slots, block tables and context lengths, the kernels, and a
-    D2H read of the output, all inside the timed region."""
+    q, new K/V, slots, block tables and context lengths are packed in one pinned
+    buffer and copied host->device as one transfer every step (an engine stages its
+    step inputs the same way), then the kernels run on views of the device copy, and
+    the output is read back device->host; all inside the timed region."""
     names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
     if w.query_start is not None:
         names = names + ("query_start",)
-    host = {n: getattr(w, n).cpu().pin_memory() for n in names}
-    devb = {n: torch.empty_like(getattr(w, n)) for n in names}
+    offsets, total = {}, 0
+    for n in names:
+        t = getattr(w, n)
+        offsets[n] = total
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
+
+    def view(buf, n):
+        t = getattr(w, n)
+        nbytes = t.numel() * t.element_size()
+        return buf[offsets[n]:offsets[n] + nbytes].view(t.dtype).view(t.shape)
+
+    for n in names:
+        view(host_buf, n).copy_(getattr(w, n).cpu())
+    devb = {n: view(dev_buf, n) for n in names}
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = total
     d2h = out_host.numel() * out_host.element_size()
 
     write, decode = step_ops(pa, w)
 
     def step():
-        for n in names:
-            devb[n].copy_(host[n], non_blocking=True)
+        dev_buf.copy_(host_buf, non_blocking=True)
         write(devb["k_new"], devb["v_new"], devb["slot_mapping"])
         if w.query_start is not None:
             decode(out, devb["q"], devb["block_tables"], devb["context_lens"], part, ws,
