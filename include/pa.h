@@ -233,8 +233,13 @@ int pa_reshape_and_cache_fp8(const void* k, const void* v, pa_dtype src_dtype, v
  * pa_decode_fp8: pa_decode over E4M3 caches.  q (and a native-dtype out) have
  * q_dtype, PA_F16 or PA_BF16; out_dtype is PA_F32 or q_dtype.  Scores use the
  * dequantised keys (q . (c_k * k_scale[h])) and the output the dequantised values;
- * accumulation is fp32 as in pa_decode.  All other arguments, the split rules and
- * the workspace are those of pa_decode (pa_decode_workspace_bytes gives the size).
+ * accumulation is fp32 as in pa_decode.  At head_dim 128 with up to 4 query heads per
+ * kv head the products run on the tensor cores with the codes as operands: each query
+ * row enters as four E4M3 terms after a power-of-two scaling (exact for bf16 queries,
+ * for f16 queries exact but for elements below about 2^-22 of the row's largest) and
+ * each probability as four terms (2^-16 relative).  All other arguments, the split
+ * rules and the workspace are those of pa_decode (pa_decode_workspace_bytes gives the
+ * size).
  */
 int pa_decode_fp8(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
                   const void* k_cache, const void* v_cache, const float* k_scale,
@@ -296,8 +301,12 @@ int pa_chunk_attention(void* out, pa_dtype out_dtype, const void* q, const void*
  * pa_chunk_attention_fp8: pa_chunk_attention over E4M3 caches (the FP8 cache of
  * pa_decode_fp8: value = code * per-kv-head scale, k_scale / v_scale DEVICE [Hkv]).
  * q (and a native-dtype out) have q_dtype, PA_F16 or PA_BF16; out_dtype is PA_F32 or
- * q_dtype.  Every chunk length runs on the decode kernel's multi-row mode, which reads
- * the one-byte tiles directly; all other arguments, rules and errors are those of
+ * q_dtype.  Short chunks (at most 32 (token, head) rows per kv head) run on a decode
+ * kernel's multi-row mode, which reads the one-byte tiles directly.  Longer chunks at
+ * head_dim 128 run on the tcgen05 chunk kernel, whose converter warps turn each tile
+ * into f16 operands (exact) in shared memory; a bf16 query row is scaled into f16
+ * range by a power of two (exact).  At head_dim 64 every chunk length takes the
+ * multi-row mode.  All other arguments, rules and errors are those of
  * pa_chunk_attention (returns PA_ERR_UNSUPPORTED when called with an E4M3 kv_dtype).
  */
 int pa_chunk_attention_fp8(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
