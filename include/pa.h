@@ -235,9 +235,10 @@ int pa_reshape_and_cache_fp8(const void* k, const void* v, pa_dtype src_dtype, v
  * dequantised keys (q . (c_k * k_scale[h])) and the output the dequantised values;
  * accumulation is fp32 as in pa_decode.  At head_dim 128 with up to 4 query heads per
  * kv head the products run on the tensor cores with the codes as operands: each query
- * row enters as four E4M3 terms after a power-of-two scaling (exact for bf16 queries,
- * for f16 queries exact but for elements below about 2^-22 of the row's largest) and
- * each probability as four terms (2^-16 relative).  All other arguments, the split
+ * row enters as four E4M3 terms after a power-of-two scaling (exact for elements down
+ * to about 2^-21 of the row's largest magnitude for bf16 queries, 2^-18 for f16; the
+ * smaller ones keep an absolute error below 2^-29 of it) and each probability as four
+ * terms (2^-16 relative).  All other arguments, the split
  * rules and the workspace are those of pa_decode (pa_decode_workspace_bytes gives the
  * size).
  */

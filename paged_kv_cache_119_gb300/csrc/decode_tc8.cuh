@@ -19,7 +19,9 @@
 // is written as four E4M3 terms, q * sigma_r = Q0 + Q1/16 + Q2/256 + Q3/4096 (sigma_r a
 // power of two that puts max |q| in [128, 256)), in columns 4r .. 4r+3 of Qt; each
 // term is the previous remainder times 16, rounded to nearest even, so the four carry
-// about 16 significant bits (a bf16 query is exact in two).  The probabilities are
+// about 16 significant bits; the last resolves 2^-21 of the scaled row, so a query
+// element is exact down to about 2^-21 (bf16) or 2^-18 (f16) of the row's largest, and
+// smaller ones keep an error below 2^-29 of it.  The probabilities are
 // split the same way, 256 p = P0 + P1/16 + P2/256 + P3/4096, in rows 4r .. 4r+3 of Pt.
 // The fp32 results of the term columns are combined with the same weights.
 //
