@@ -43,24 +43,17 @@ __device__ __forceinline__ void fence_mbar_init()
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// (the arrival's phase state is not needed: the sink operand `_` discards it)
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
 {
-    uint64_t state;
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 %0, [%1], %2;"
-                 : "=l"(state)
-                 : "r"(smem_addr(bar)), "r"(bytes)
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
                  : "memory");
-    (void)state;
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
 {
-    uint64_t state;
-    asm volatile("mbarrier.arrive.shared::cta.b64 %0, [%1];"
-                 : "=l"(state)
-                 : "r"(smem_addr(bar))
-                 : "memory");
-    (void)state;
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
