@@ -100,7 +100,7 @@ cudaError_t launch_chunk_rows(const DecodeParams& p, const ChunkParams& cp, pa_d
     return cudaErrorInvalidValue;
 }
 
-// E4M3 caches: always the chunk-row path (q_dtype F16 or BF16; p.k_scale, p.v_scale set);
+// E4M3 caches on the chunk-row path (q_dtype F16 or BF16; p.k_scale, p.v_scale set);
 // the E4M3 tcgen05 kernel where use_tc8 says so, else the mma.sync kernel.
 cudaError_t launch_chunk_rows_fp8(const DecodeParams& p, const ChunkParams& cp, pa_dtype q_dtype,
                                   int head_dim, int block_size, int nh, const CUtensorMap& tk,

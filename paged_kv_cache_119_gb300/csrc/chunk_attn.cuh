@@ -42,6 +42,16 @@
 // cost up to 2^-9 relative per weight).
 // Long contexts with few CTAs are split into partitions merged by
 // chunk_reduce_kernel, as in the decode path.
+// The epilogue reads O once its issuer's one-phase completion barrier has fired (P.V of
+// the last two tiles may be pending or done in any combination when a warp gets there,
+// which a wait on the per-tile parity barrier cannot tell apart).
+//
+// E4M3 caches (NRAW > 0, head_dim 128): the producer's TMA fills a ring of raw one-byte
+// K + V tiles, and four converter warps (11-14) turn each into the f16 swizzled tiles of
+// the ring above (E4M3 -> f16 is exact), then hand it to the issuers and release the raw
+// slot.  The operands are f16: a bf16 query row is scaled into f16 range by a power of
+// two (exact) that joins the row's score scale together with the kv head's K scale, and
+// the V scale multiplies the output.
 #pragma once
 
 #include <cuda.h>

@@ -211,7 +211,8 @@ cudaError_t launch_chunk_rows(const DecodeParams& p, const ChunkParams& cp, pa_d
                               int head_dim, int block_size, int nh, const CUtensorMap& tk,
                               const CUtensorMap& tv, cudaStream_t stream);
 int occupancy_chunk_rows(pa_dtype dtype, int head_dim, int block_size, int nh);
-// E4M3 caches: every chunk length runs on the chunk-row path.
+// E4M3 caches, chunk rows: short chunks at head_dim 128 and every chunk at head_dim 64
+// (long chunks at 128 take launch_chunk_attention_fp8).
 cudaError_t launch_chunk_rows_fp8(const DecodeParams& p, const ChunkParams& cp, pa_dtype q_dtype,
                                   int head_dim, int block_size, int nh, const CUtensorMap& tk,
                                   const CUtensorMap& tv, cudaStream_t stream);
