@@ -284,8 +284,9 @@ int pa_decode_fp8(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype
  * multi-row mode; longer chunks run on the tcgen05 kernel (256 rows per CTA).
  * Errors: invalid arguments return a negative pa_status with nothing launched.  On
  * the device, n_s > L_s, L_s > max_context_len, n_s > max_query_len or rows beyond
- * query_start[num_seqs] set PA_DEVERR_CONTEXT_LEN (that sequence's rows become NaN);
- * a block id outside the pool sets PA_DEVERR_BLOCK_ID.
+ * query_start[num_seqs] set PA_DEVERR_CONTEXT_LEN (the offending sequence's rows
+ * become NaN; rows that no sequence owns are left unwritten); a block id outside the
+ * pool sets PA_DEVERR_BLOCK_ID.
  */
 size_t pa_chunk_workspace_bytes(int64_t num_query_tokens, int32_t num_q_heads, int32_t head_dim,
                                 int32_t max_context_len, int32_t partition_size);

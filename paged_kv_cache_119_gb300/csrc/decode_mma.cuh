@@ -258,6 +258,9 @@ __global__ void __launch_bounds__(kDecodeThreads)
     }
     int t_end = L;
     if constexpr (CH) {
+        if (seq == p.num_seqs - 1 && part == 0 && blockIdx.y == 0 && threadIdx.x == 0 &&
+            (int64_t)qs0 + n != p.num_rows)
+            atomicOr(p.err, PA_DEVERR_CONTEXT_LEN);   // rows after the last chunk belong to no one
         if (R0 / p.group >= n)
             return;                                // no chunk token in this row chunk
         t_end = L - n + min(n - 1, (R0 + NH - 1) / p.group) + 1;   // last row's position + 1

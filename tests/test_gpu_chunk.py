@@ -421,3 +421,43 @@ def test_fp8_verify4_full_batch_sampled_rows():
     picks = [(s, j) for s in rng.choice(w.num_seqs, size=10, replace=False).tolist()
              for j in range(qs[s + 1] - qs[s])]
     _sampled_rows_fp8(w, picks)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("Hq,Hkv,nmax", [(8, 8, 40), (16, 4, 8), (8, 8, 4)])
+def test_rows_beyond_the_last_chunk_are_flagged(fp8, Hq, Hkv, nmax):
+    """q with rows after query_start[num_seqs] (owned by no sequence) sets the
+    context-length error bit on every path (the tcgen05 chunk kernel, and both decode
+    kernels' chunk-row modes); the owned rows are still the oracle's."""
+    w = make_case(53 + nmax, 3, Hq, Hkv, 128, 16, torch.bfloat16, [300, 90, 200],
+                  [nmax, nmax // 2 + 1, nmax])
+    if fp8:
+        w = workloads.to_fp8(w)
+    ks = w.meta["k_scale"] if fp8 else None
+    vs = w.meta["v_scale"] if fp8 else None
+    if fp8:
+        P.pa_reshape_and_cache_fp8(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping, ks, vs)
+    else:
+        P.pa_reshape_and_cache(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping)
+    R = w.q.shape[0]
+    q2 = torch.cat([w.q, torch.zeros_like(w.q[:3])])
+    out = torch.zeros((R + 3,) + tuple(w.q.shape[1:]), dtype=torch.float32, device="cuda")
+    args = (w.block_tables, w.context_lens, w.query_start, w.scale, w.num_kv_heads, w.block_size)
+    kw = dict(max_query_len=w.max_query_len, max_context_len=w.max_context_len)
+    P.pa_get_device_error()
+    if fp8:
+        P.pa_chunk_attention_fp8(out, q2, w.k_cache, w.v_cache, ks, vs, *args, **kw)
+    else:
+        P.pa_chunk_attention(out, q2, w.k_cache, w.v_cache, *args, **kw)
+    torch.cuda.synchronize()
+    assert P.pa_get_device_error() & 0x2
+    kc, vc = w.k_cache.cpu(), w.v_cache.cpu()
+    if fp8:
+        kc, vc = kc.view(torch.uint8), vc.view(torch.uint8)
+    ref = oracle.chunk_attention(w.q.cpu(), kc, vc, w.block_tables.cpu(), w.context_lens.cpu(),
+                                 w.query_start.cpu(), w.scale, w.num_kv_heads, w.block_size,
+                                 num_threads=oracle.max_threads(),
+                                 k_scale=None if ks is None else ks.cpu(),
+                                 v_scale=None if vs is None else vs.cpu())
+    err = np.abs(out[:R].double().cpu().numpy() - ref).max()
+    assert err <= ATOL, err
