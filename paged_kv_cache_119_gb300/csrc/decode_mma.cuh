@@ -185,6 +185,12 @@ struct MmaSmem {
     static_assert(kHalfBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
 };
 
+// Four CTAs per SM (at most 96 registers a thread) keep the 16-bit and block-size-16
+// E4M3 forms resident; the block-size-32 E4M3 form converts wider tiles and runs
+// faster at 128 registers and three CTAs.
+template <typename TK, int BS>
+constexpr int mma_min_blocks() { return (sizeof(TK) == 1 && BS == 32) ? 3 : 4; }
+
 // T: query / native output type (the mma operand type).  TK: cache element type,
 // T itself (tiles by tensor-map TMA) or __nv_fp8_e4m3 (raw tiles by 1-D bulk copy,
 // converted exactly to T in shared memory; the value is code * per-kv-head scale).
@@ -193,7 +199,7 @@ struct MmaSmem {
 // sequence attended causally, each row masked at its own position (speculative
 // verification, short chunks) -- instead of NH query heads of one token.
 template <typename T, typename TK, int D, int BS, int NH, int NSTAGE, bool CH = false>
-__global__ void __launch_bounds__(kDecodeThreads)
+__global__ void __launch_bounds__(kDecodeThreads, mma_min_blocks<TK, BS>())
     decode_mma_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv)
 {
@@ -524,7 +530,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
                 tmax = fmaxf(tmax, __shfl_xor_sync(kFullMask, tmax, 8));
                 tmax = fmaxf(tmax, __shfl_xor_sync(kFullMask, tmax, 16));
                 const float mnew = fmaxf(m[j], tmax);       // -inf only for padded heads
-                alpha[j] = (mnew == -INFINITY) ? 1.f : exp2f(m[j] - mnew);
+                alpha[j] = (mnew == m[j]) ? 1.f : exp2f(m[j] - mnew);   // 1: max unchanged
                 m[j] = mnew;
                 const float pa = (mnew == -INFINITY) ? 0.f : exp2f(x[j] - mnew);
                 const float pb = (mnew == -INFINITY) ? 0.f : exp2f(x[j + 2] - mnew);
@@ -532,12 +538,16 @@ __global__ void __launch_bounds__(kDecodeThreads)
                 x[j + 2] = pb;
                 lsum[j] = fmaf(lsum[j], alpha[j], pa + pb);
             }
+            // once the running maxima settle (most tiles of a long context) no row of the
+            // warp rescales, and the 4 x KS multiplies by 1 are skipped
+            if (__any_sync(kFullMask, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
-            for (int i = 0; i < KS; ++i) {
-                o[i][0] *= alpha[0];
-                o[i][1] *= alpha[1];
-                o[i][2] *= alpha[0];
-                o[i][3] *= alpha[1];
+                for (int i = 0; i < KS; ++i) {
+                    o[i][0] *= alpha[0];
+                    o[i][1] *= alpha[1];
+                    o[i][2] *= alpha[0];
+                    o[i][3] *= alpha[1];
+                }
             }
             // ---- P^T (hi + lo) into B fragments: transpose each 8x8 block in registers
             const uint32_t hi_a = Mma<TM>::pack(x[0], x[1]);
