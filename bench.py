@@ -642,11 +642,18 @@ def run_ours(args, rank, world, local):
     split = part > 0 and w.max_context_len > part
     if part == 0:
         split = launched_split(pa, w)
-    launches_per_step = 2 + (1 if split else 0) + (1 if cow_src is not None else 0)
+    # an automatic one-pass decode of several waves first builds its longest-first order
+    ordered = (not chunk and part == 0 and not split and
+               pa.pa_decode_orders_sequences(w.q.dtype, w.k_cache.dtype, w.num_seqs,
+                                             w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                             w.block_size, w.max_context_len, 0))
+    launches_per_step = (2 + (1 if split else 0) + (1 if ordered else 0)
+                         + (1 if cow_src is not None else 0))
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": recorded_traffic(args.config),
-                "kernel": dominant_kernel(w) + (" + reduce kernel" if split else ""),
+                "kernel": dominant_kernel(w) + (" + reduce kernel" if split else "")
+                + (" (after the order kernel)" if ordered else ""),
                 "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": nbytes["decode"]}

@@ -75,12 +75,13 @@ typedef enum {
 #define PA_DEVERR_TIMEOUT     0x8u  /* a bounded pipeline wait gave up */
 
 /*
- * Bytes of device workspace pa_decode needs when it splits contexts into
- * partitions of partition_size tokens (0 = the automatic choice, which never
- * needs more than this; < 0 = never split, returns 0).  The workspace holds,
- * per (sequence, query head, partition), one fp32 partial output row of head_dim
- * values plus its running max and sum.  Pure host arithmetic; no CUDA call.
- * Returns 0 for invalid sizes.
+ * Bytes of device workspace a pa_decode call with these sizes uses: when it splits
+ * contexts into partitions of partition_size tokens (0 = the automatic choice, which
+ * never needs more than this; < 0 = never split, returns 0), per (sequence, query
+ * head, partition) one fp32 partial output row of head_dim values plus its running
+ * max and sum; with the automatic choice, at least 8 bytes per sequence (rounded up
+ * to 256) for the longest-first dispatch order of a one-pass call (see pa_decode).
+ * Pure host arithmetic; no CUDA call.  Returns 0 for invalid sizes.
  */
 size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                                  int32_t max_context_len, int32_t block_size,
@@ -105,10 +106,19 @@ size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t 
  *   partition_size    0 = automatic; < 0 = one pass per (sequence, kv head);
  *                     > 0 = split each context into partitions of this many tokens
  *                     (a multiple of block_size) and merge them in a second kernel.
- *   workspace         device buffer of workspace_bytes, only used (and only
- *                     required) when the call splits; see pa_decode_workspace_bytes.
+ *   workspace         device buffer of workspace_bytes; required only when the
+ *                     call splits (see pa_decode_workspace_bytes).  An automatic
+ *                     (partition_size 0) one-pass call on the CUDA-core kernel (fewer
+ *                     than 4 query heads per kv head; over E4M3 caches, head_dim
+ *                     64 only) whose grid holds more CTAs
+ *                     than fit on the GPU at once uses its first 8 * S bytes, when
+ *                     given, for a longest-first order of the sequences (one more
+ *                     small launch; pa_decode_orders_sequences tells): a long
+ *                     context started in the last wave would stretch the kernel's
+ *                     tail.  Results are bitwise the same in either order.
  *   stream            cudaStream_t (as void*).
- * out must not overlap q, the caches or the workspace.
+ * out must not overlap q, the caches or the workspace; the workspace must not
+ * overlap context_lens.
  */
 int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
               const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
@@ -330,6 +340,16 @@ int pa_chunk_attention_fp8(void* out, pa_dtype out_dtype, const void* q, pa_dtyp
  * PA_ERR_CUDA when the automatic choice cannot query the device.
  */
 int32_t pa_decode_partition_tokens(pa_dtype q_dtype, pa_dtype kv_dtype, int32_t num_seqs,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t block_size, int32_t max_context_len,
+                                   int32_t partition_size);
+/*
+ * 1 when a pa_decode / pa_decode_fp8 call with these arguments and a workspace of
+ * pa_decode_workspace_bytes(...) builds the longest-first dispatch order (one more
+ * launch before the decode), else 0; a negative pa_status as for
+ * pa_decode_partition_tokens.
+ */
+int32_t pa_decode_orders_sequences(pa_dtype q_dtype, pa_dtype kv_dtype, int32_t num_seqs,
                                    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                    int32_t block_size, int32_t max_context_len,
                                    int32_t partition_size);

@@ -20,6 +20,7 @@ __version__ = "0.1.0"
 _API = ("pa_decode", "pa_decode_noalloc", "pa_decode_fp8", "pa_reshape_and_cache",
         "pa_reshape_and_cache_fp8", "pa_copy_blocks", "pa_decode_workspace_bytes",
         "pa_chunk_attention", "pa_chunk_workspace_bytes", "pa_decode_partition_tokens",
+        "pa_decode_orders_sequences",
         "pa_chunk_partition_tokens", "pa_swap_blocks", "pa_chunk_attention_fp8",
         "pa_get_device_error", "pa_version")
 

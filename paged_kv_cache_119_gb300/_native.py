@@ -37,6 +37,8 @@ SIGNATURES = {
                                               _vp]),
     "pa_decode_partition_tokens": (_i32, [ctypes.c_int, ctypes.c_int, _i32, _i32, _i32, _i32, _i32,
                                           _i32, _i32]),
+    "pa_decode_orders_sequences": (_i32, [ctypes.c_int, ctypes.c_int, _i32, _i32, _i32, _i32, _i32,
+                                          _i32, _i32]),
     "pa_chunk_partition_tokens": (_i32, [ctypes.c_int, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                          _i32]),
     "pa_chunk_attention": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp, _vp, ctypes.c_int, _i64, _vp,

@@ -423,6 +423,21 @@ def pa_decode_partition_tokens(q_dtype: torch.dtype, kv_dtype: torch.dtype, num_
     return r
 
 
+def pa_decode_orders_sequences(q_dtype: torch.dtype, kv_dtype: torch.dtype, num_seqs: int,
+                               num_q_heads: int, num_kv_heads: int, head_dim: int,
+                               block_size: int, max_context_len: int,
+                               partition_size: int = 0) -> bool:
+    """Whether pa_decode / pa_decode_fp8 (given its workspace) first builds the
+    longest-first dispatch order of the sequences (one more launch)."""
+    kv = N.PA_FP8_E4M3 if kv_dtype == torch.float8_e4m3fn else _DT[kv_dtype]
+    r = int(N.load().pa_decode_orders_sequences(_DT[q_dtype], kv, num_seqs, num_q_heads,
+                                                num_kv_heads, head_dim, block_size,
+                                                max_context_len, partition_size))
+    if r < 0:
+        N.check("pa_decode_orders_sequences", r)
+    return r == 1
+
+
 def pa_chunk_partition_tokens(kv_dtype: torch.dtype, num_seqs: int, num_q_heads: int,
                               num_kv_heads: int, head_dim: int, block_size: int,
                               max_query_len: int, max_context_len: int,

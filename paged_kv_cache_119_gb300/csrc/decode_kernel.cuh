@@ -109,6 +109,18 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, int64_t idx, fl
         store_as(reinterpret_cast<T*>(p.out) + idx, x);
 }
 
+// The sequence a decode CTA serves (x) and its context length (y): CTA row z serves
+// sequence z, or the z-th of the longest-first order when the call built one.
+__device__ __forceinline__ int2 decode_seq(const DecodeParams& p)
+{
+    if (p.seq_order) {
+        const int2 e = p.seq_order[blockIdx.z];
+        if ((unsigned)e.x < (unsigned)p.num_seqs)   // always, unless the lengths were
+            return e;                               // changed while the order was built
+    }
+    return make_int2((int)blockIdx.z, p.context_lens[blockIdx.z]);
+}
+
 // T: query / native output type.  TK: cache element type (T itself, or
 // __nv_fp8_e4m3 for a quantised cache whose value is code * per-kv-head scale).
 template <typename T, typename TK, int D, int BS, int GC, int NSTAGE>
@@ -140,13 +152,14 @@ __global__ void __launch_bounds__(kDecodeThreads)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int seq = blockIdx.z;
+    const int2 seq_len = decode_seq(p);
+    const int seq = seq_len.x;
     const int kvh = blockIdx.y / p.chunks;
     const int h0 = kvh * p.group + (blockIdx.y % p.chunks) * GC;
     const int part = blockIdx.x;
     const bool split = p.partition_tokens > 0;
 
-    const int L = p.context_lens[seq];
+    const int L = seq_len.y;
     if (L < 0 || L > p.max_context_len) {
         if (part == 0 && blockIdx.y == 0 && threadIdx.x == 0)
             atomicOr(p.err, PA_DEVERR_CONTEXT_LEN);

@@ -276,21 +276,31 @@ size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t 
     if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0 ||
         block_size <= 0 || partition_size < 0)
         return 0;
+    // an automatic one-pass call's dispatch order
+    const size_t order = partition_size == 0 ? seq_order_bytes(num_seqs) : 0;
     const int P = partition_size > 0 ? partition_size : kAutoPartitionTokens;
     if (max_context_len <= P)
-        return 0;
+        return order;
     const int max_parts = (max_context_len + P - 1) / P;
-    return workspace_layout((int64_t)num_seqs * num_q_heads, max_parts, head_dim, nullptr);
+    return std::max(order, workspace_layout((int64_t)num_seqs * num_q_heads, max_parts,
+                                            head_dim, nullptr));
 }
 
 }  // extern "C"
 
 namespace {
 
-// The partition length pa_decode uses for these arguments (0: one pass).
+// The partition length pa_decode uses for these arguments (0: one pass).  *order_out
+// (optional): whether a one-pass call builds the longest-first dispatch order -- an
+// automatic call on the CUDA-core decode kernel whose grid holds more CTAs than one
+// wave.  Measured on GB300: the LLaMA-13B and OPT-13B batches decode 2.5 % faster in
+// that order.  The other kernels are slower in it: the E4M3 tcgen05 decode by 8-10 %
+// (its CTAs' fixed start-up and epilogue work no longer hides behind long streams once
+// only short sequences are left), the shared-prefix mma.sync batch by 2.5 % (sequences
+// that share prefix blocks no longer run side by side).
 int decode_partition(pa_dtype q_dtype, pa_dtype kv_dtype, int num_seqs, int num_kv_heads,
                      int group, int head_dim, int block_size, int max_context_len,
-                     int partition_size)
+                     int partition_size, bool* order_out = nullptr)
 {
     const int gc = heads_per_cta(group);
     int occ = 0;
@@ -303,11 +313,15 @@ int decode_partition(pa_dtype q_dtype, pa_dtype kv_dtype, int num_seqs, int num_
         }
     }
     const int64_t units = (int64_t)num_seqs * num_kv_heads * (group / gc);
+    const int64_t slots = (int64_t)device_sm_count() * occ;
+    const bool fp8 = kv_dtype == PA_FP8_E4M3;
+    const bool cuda_core = !(fp8 && use_tc8(head_dim, gc)) &&
+                           gc < (fp8 ? kMmaMinHeadsFp8 : kMmaMinHeads);
+    if (order_out)
+        *order_out = partition_size == 0 && cuda_core && slots > 0 && units > slots;
     if (kv_dtype == PA_FP8_E4M3 && use_tc8(head_dim, gc))
-        return choose_partition_tc8(partition_size, max_context_len, units,
-                                    (int64_t)device_sm_count() * occ);
-    return choose_partition(partition_size, max_context_len, units,
-                            (int64_t)device_sm_count() * occ, block_size);
+        return choose_partition_tc8(partition_size, max_context_len, units, slots);
+    return choose_partition(partition_size, max_context_len, units, slots, block_size);
 }
 
 // How pa_chunk_attention runs a call: few (token, head) rows per kv head go to a decode
@@ -406,8 +420,9 @@ int decode_impl(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
         overlaps(out, out_bytes, v_cache, pool_bytes))
         return PA_ERR_INVALID;
 
+    bool order_seqs = false;
     const int P = decode_partition(q_dtype, kv_dtype, num_seqs, num_kv_heads, group, head_dim,
-                                   block_size, max_context_len, partition_size);
+                                   block_size, max_context_len, partition_size, &order_seqs);
     DecodeParams p{};
     p.out = out;
     p.q = q;
@@ -446,6 +461,17 @@ int decode_impl(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
         return PA_ERR_CUDA;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // a one-pass CUDA-core grid of several waves starts the longest sequences first, when
+    // the workspace has room for the order and touches none of the inputs it is built from
+    const size_t order_bytes = seq_order_bytes(num_seqs);
+    if (P == 0 && order_seqs && workspace && aligned16(workspace) &&
+        workspace_bytes >= order_bytes && !overlaps(out, out_bytes, workspace, order_bytes) &&
+        !overlaps(context_lens, (size_t)num_seqs * 4, workspace, order_bytes)) {
+        int2* order = static_cast<int2*>(workspace);
+        if (launch_seq_order(context_lens, num_seqs, max_context_len, order, st) != cudaSuccess)
+            return PA_ERR_CUDA;
+        p.seq_order = order;
+    }
     cudaError_t e = cudaErrorInvalidValue;
     switch (kv_dtype) {
     case PA_F32: e = launch_decode_f32(p, head_dim, block_size, gc, st); break;
@@ -506,6 +532,22 @@ int32_t pa_decode_partition_tokens(pa_dtype q_dtype, pa_dtype kv_dtype, int32_t 
         return PA_ERR_CUDA;
     return decode_partition(q_dtype, kv_dtype, num_seqs, num_kv_heads, num_q_heads / num_kv_heads,
                             head_dim, block_size, max_context_len, partition_size);
+}
+
+int32_t pa_decode_orders_sequences(pa_dtype q_dtype, pa_dtype kv_dtype, int32_t num_seqs,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t block_size, int32_t max_context_len,
+                                   int32_t partition_size)
+{
+    const int32_t P = pa_decode_partition_tokens(q_dtype, kv_dtype, num_seqs, num_q_heads,
+                                                 num_kv_heads, head_dim, block_size,
+                                                 max_context_len, partition_size);
+    if (P != 0)
+        return P < 0 ? P : 0;
+    bool order_seqs = false;
+    decode_partition(q_dtype, kv_dtype, num_seqs, num_kv_heads, num_q_heads / num_kv_heads,
+                     head_dim, block_size, max_context_len, partition_size, &order_seqs);
+    return order_seqs && num_seqs > 0 ? 1 : 0;
 }
 
 int32_t pa_chunk_partition_tokens(pa_dtype kv_dtype, int32_t num_seqs, int32_t num_q_heads,

@@ -33,6 +33,10 @@ struct DecodeParams {
     const void* v_cache;
     const int32_t* block_tables;
     const int32_t* context_lens;
+    // one-pass CUDA-core decode, optional: CTA row z serves sequence seq_order[z].x,
+    // whose context length is seq_order[z].y (the longest-first order seq_order.cu
+    // builds); null: row z serves sequence z
+    const int2* seq_order;
     float* part_o;       // [S][Hq][max_parts][D] normalised partial outputs (split only)
     float* part_ml;      // [S][Hq][max_parts][2] (running max in log2 units, sum)
     const float* k_scale;  // [Hkv] per-head scales of a quantised (E4M3) cache, else null
@@ -55,6 +59,19 @@ struct DecodeParams {
     int64_t num_rows;
     int max_query_len;
 };
+
+// Longest-first dispatch of a one-pass CUDA-core decode with more CTAs than one wave:
+// a CTA that starts late on a long context stretches the kernel's tail.  seq_order.cu
+// sorts the sequences into kOrderClasses length classes, longest class first, stably
+// (index order within a class, so neighbouring sequences, e.g. ones sharing a prefix,
+// stay close).  The order takes 8 bytes per sequence of the call's workspace.
+constexpr int kOrderClasses = 8;
+inline size_t seq_order_bytes(int64_t num_seqs)
+{
+    return (size_t)((num_seqs * 8 + 255) / 256 * 256);
+}
+cudaError_t launch_seq_order(const int32_t* context_lens, int num_seqs, int max_context_len,
+                             int2* order, cudaStream_t stream);
 
 // Per-dtype decode launchers (one translation unit each).  `gc` is the number of
 // query heads one CTA serves (1, 2, 4 or 8).  Return cudaErrorInvalidValue for

@@ -50,6 +50,11 @@ def test_workspace_bytes(lib):
     assert lib.pa_decode_workspace_bytes(8, 64, 128, 512, 16, 512) == 0      # never splits
     assert lib.pa_decode_workspace_bytes(8, 64, 128, 4096, 16, 0) > 0         # auto upper bound
     assert lib.pa_decode_workspace_bytes(-1, 64, 128, 4096, 16, 0) == 0
+    # automatic calls that cannot split still get room for the dispatch order:
+    # 8 bytes per sequence, rounded up to 256
+    assert lib.pa_decode_workspace_bytes(8, 64, 128, 512, 16, 0) == 256
+    assert lib.pa_decode_workspace_bytes(33, 64, 128, 512, 16, 0) == 512
+    assert lib.pa_decode_workspace_bytes(8, 64, 128, 512, 16, -1) == 0
 
 
 FAKE = 1 << 20        # a 16-byte-aligned non-null address; never dereferenced here
@@ -213,6 +218,13 @@ def test_partition_queries_for_explicit_sizes(lib):
     assert lib.pa_decode_partition_tokens(N.PA_BF16, N.PA_BF16, 8, 64, 8, 128, 16, 512, 512) == 0
     assert lib.pa_decode_partition_tokens(N.PA_BF16, N.PA_BF16, 8, 64, 8, 128, 16, 4096, -1) == 0
     assert lib.pa_decode_partition_tokens(N.PA_BF16, N.PA_BF16, 8, 64, 8, 128, 16, 4096, 24) \
+        == N.PA_ERR_INVALID
+    # only the automatic choice reorders sequences
+    assert lib.pa_decode_orders_sequences(N.PA_BF16, N.PA_BF16, 256, 40, 40, 128, 16, 2048, 512) \
+        == 0
+    assert lib.pa_decode_orders_sequences(N.PA_BF16, N.PA_BF16, 256, 40, 40, 128, 16, 2048, -1) \
+        == 0
+    assert lib.pa_decode_orders_sequences(N.PA_BF16, N.PA_BF16, 256, 40, 40, 128, 16, 2048, 24) \
         == N.PA_ERR_INVALID
     assert lib.pa_chunk_partition_tokens(N.PA_BF16, 8, 64, 8, 128, 16, 512, 32768, 1024) == 1024
     assert lib.pa_chunk_partition_tokens(N.PA_BF16, 8, 64, 8, 128, 16, 512, 32768, 1000) \
