@@ -23,7 +23,8 @@ namespace pa {
 
 // One thread per 16-byte vector of a (token, head) row, for K and for V.
 // Consecutive threads cover consecutive vectors of one row, so both the read of
-// k[i][h][:] and the write to the cache slot are fully coalesced.
+// k[i][h][:] and the write to the cache slot are fully coalesced.  64-bit grid-stride
+// form, for calls of more than 2^31 - 1 vectors per tensor.
 __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const ReshapeParams p)
 {
     const int64_t per_tensor = p.num_tokens * p.num_kv_heads * p.row_vecs;
@@ -54,11 +55,49 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const ReshapePar
     }
 }
 
+// The usual form: one thread per 16-byte vector i of the step's (token, head) rows,
+// moving vector i of K and vector i of V.  Index arithmetic is 32-bit (the launcher
+// takes this form when the vector count fits), both source loads are issued before
+// the slot is read, and a decode step's rows fit one resident wave (256 new tokens x
+// 40 heads of LLaMA-13B: 640 CTAs).
+__global__ void __launch_bounds__(256) reshape_and_cache_pair_kernel(const ReshapeParams p,
+                                                                     int items)
+{
+    const int i = blockIdx.x * 256 + threadIdx.x;
+    if (i >= items)
+        return;
+    const uint4 kx = p.k[i];
+    const uint4 vx = p.v[i];
+    const int th = i / p.row_vecs;                   // token * num_kv_heads + head
+    const int c = i - th * p.row_vecs;
+    const int tok = th / p.num_kv_heads;
+    const int h = th - tok * p.num_kv_heads;
+    const int64_t slot = p.slot_mapping[tok];
+    if (slot < 0)
+        return;                                      // padding token
+    if (slot >= p.num_blocks * p.block_size) {
+        if (c == 0 && h == 0)
+            atomicOr(p.err, PA_DEVERR_SLOT);
+        return;
+    }
+    const int64_t blk = slot / p.block_size;
+    const int64_t off = slot - blk * p.block_size;
+    const int64_t dst = ((blk * p.num_kv_heads + h) * p.block_size + off) * p.row_vecs + c;
+    p.k_cache[dst] = kx;
+    p.v_cache[dst] = vx;
+}
+
 cudaError_t launch_reshape_and_cache(const ReshapeParams& p, cudaStream_t stream)
 {
-    const int64_t total = 2 * p.num_tokens * p.num_kv_heads * p.row_vecs;
-    if (total == 0)
+    const int64_t items = p.num_tokens * p.num_kv_heads * p.row_vecs;
+    if (items == 0)
         return cudaSuccess;
+    if (items <= INT32_MAX) {
+        reshape_and_cache_pair_kernel<<<(int)((items + 255) / 256), 256, 0, stream>>>(p,
+                                                                                     (int)items);
+        return cudaGetLastError();
+    }
+    const int64_t total = 2 * items;
     const int sms = device_sm_count();
     const int64_t want = (total + 255) / 256;
     const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 16;
@@ -70,7 +109,9 @@ cudaError_t launch_reshape_and_cache(const ReshapeParams& p, cudaStream_t stream
 // Quantising cache write: one thread per 16 consecutive elements of a (token, head)
 // row, for K and for V; each element becomes e4m3(fp32(x) / scale[head]) (IEEE fp32
 // division, round to nearest even, saturating at +-448) and the 16 codes are stored
-// with one 16-byte store.
+// with one 16-byte store.  (One thread for K and V together, as in the 16-bit write,
+// measured slower here: the fp32 divisions make each thread's work long, and half as
+// many threads hide less of it.)
 template <typename TS>
 __global__ void __launch_bounds__(256) reshape_and_cache_fp8_kernel(const ReshapeFp8Params p)
 {
