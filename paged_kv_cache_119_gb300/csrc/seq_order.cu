@@ -19,6 +19,7 @@ namespace pa {
 namespace {
 
 constexpr int kOrderThreads = 1024;
+constexpr int kOrderWarps = kOrderThreads / 32;
 constexpr unsigned kFull = 0xffffffffu;
 
 // class 0 holds the longest contexts (within max_len / kOrderClasses of max_len);
@@ -43,8 +44,9 @@ __device__ __forceinline__ int warp_inclusive_scan(int x, int lane)
 __global__ void __launch_bounds__(kOrderThreads)
     seq_order_kernel(const int32_t* __restrict__ lens, int n, int max_len, int2* __restrict__ order)
 {
-    static_assert(kOrderClasses <= kOrderThreads / 32, "one warp scans each class");
-    __shared__ int warp_base[kOrderClasses][kOrderThreads / 32];
+    static_assert(kOrderClasses <= kOrderWarps, "one warp scans each class");
+    static_assert(kOrderWarps <= 32, "one lane per warp total");
+    __shared__ int warp_base[kOrderClasses][kOrderWarps];
     __shared__ int class_base[kOrderClasses];
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int per = (n + kOrderThreads - 1) / kOrderThreads;
@@ -71,10 +73,12 @@ __global__ void __launch_bounds__(kOrderThreads)
             warp_base[k][warp] = x;
     }
     __syncthreads();
-    if (warp < kOrderClasses) {                    // warp k: the 32 warp totals of class k
-        const int own = warp_base[warp][lane];
+    if (warp < kOrderClasses) {                    // warp k: the warp totals of class k
+        const bool mine = lane < kOrderWarps;      // lanes past the warp count add 0
+        const int own = mine ? warp_base[warp][lane] : 0;
         const int x = warp_inclusive_scan(own, lane);
-        warp_base[warp][lane] = x - own;
+        if (mine)
+            warp_base[warp][lane] = x - own;
         if (lane == 31)
             class_base[warp] = x;                  // the class total, for now
     }
