@@ -1,5 +1,6 @@
-// cache_ops.cu -- the two cache-maintenance kernels: reshape_and_cache and
-// copy_blocks.  Both are bit-exact 16-byte vector copies; neither touches a value.
+// cache_ops.cu -- the cache-maintenance kernels: reshape_and_cache (and its E4M3
+// quantising form), copy_blocks and swap_blocks.  All but the E4M3 write are bit-exact
+// 16-byte vector copies that touch no value.
 //
 // reshape_and_cache ("PagedAttention 完全拆解", section 原理详解（三）：kernel 实现,
 // item 1, fused reshape and block write; Figure 6 decode steps): the row of each

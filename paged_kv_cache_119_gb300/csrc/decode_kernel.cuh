@@ -12,7 +12,9 @@
 // GB300 design:
 //   * CTA = (partition, kv head x query-head chunk, sequence).  All GC query
 //     heads of a chunk share one pass over the kv head's blocks, so with GQA a
-//     K/V tile is read from HBM once per group, not once per query head.
+//     K/V tile is read from HBM once per group, not once per query head.  A
+//     one-pass grid of several waves may take its sequences from a longest-first
+//     order (seq_order.cu): CTA row z then serves the z-th sequence of it.
 //   * Warp NCW is the producer: it prefetches the CTA's block-table slice
 //     (int32, 32 entries per coalesced load, one round ahead), turns each entry
 //     into an int64 address and issues one 1-D bulk TMA copy per K tile and per

@@ -1,5 +1,6 @@
 // decode_mma.cuh -- paged decode attention for grouped-query heads on the tensor
-// cores (sm_103a), fp16/bf16 caches.
+// cores (sm_103a), over fp16/bf16 caches and E4M3 caches (codes converted exactly to
+// the 16-bit operand type).
 //
 // Same result as decode_kernel (the block-wise attention of "PagedAttention
 // 完全拆解", section 原理详解（二）, evaluated with a running max), organised for
@@ -15,7 +16,8 @@
 //   * Consumer warps (tile i -> warp i % 4, each stage owned by one warp):
 //       S^T[16 tok x 8 heads] = K[16 x D] . Q^T  -- mma.sync m16n8k16, K from
 //         ldmatrix on the swizzled tile, Q^T fragments held in registers;
-//       running max / sum per head in fp32 (base 2);
+//       running max / sum per head in fp32 (base 2); the accumulator is rescaled
+//         only when some head's max rose (a warp vote);
 //       P^T is split into hi + lo halves of the cache dtype (P = hi + lo to
 //         ~2^-16 relative), and each 8x8 block is transposed in registers with
 //         movmatrix into the B operand of the second product;

@@ -1,5 +1,6 @@
 // pa_api.cu -- the C ABI of libpa.so (declared in include/pa.h): argument
-// validation, the split-context decision, workspace carving and kernel dispatch.
+// validation, the split-context and dispatch-order decisions, workspace carving and
+// kernel dispatch.
 // Everything here is host code except the device error word.
 #include <algorithm>
 #include <cmath>
