@@ -117,8 +117,8 @@ size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t 
  *                     context started in the last wave would stretch the kernel's
  *                     tail.  Results are bitwise the same in either order.
  *   stream            cudaStream_t (as void*).
- * out must not overlap q, the caches or the workspace; the workspace must not
- * overlap context_lens.
+ * out must not overlap q or the caches, and the workspace none of out, q, the
+ * caches, block_tables or context_lens (PA_ERR_INVALID, nothing launched).
  */
 int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
               const void* v_cache, pa_dtype kv_dtype, int64_t num_blocks,
@@ -285,7 +285,9 @@ int pa_decode_fp8(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype
  *   partition_size   0 = automatic split of long contexts, < 0 never split, > 0 that
  *                    many tokens per partition (a multiple of 64)
  *   workspace        DEVICE scratch of pa_chunk_workspace_bytes(...) when a split
- *                    happens (16-byte aligned, caller-owned), else may be NULL
+ *                    happens (16-byte aligned, caller-owned), else may be NULL; it
+ *                    must not overlap out, q, the caches, block_tables,
+ *                    context_lens or query_start (PA_ERR_INVALID)
  * Supported: head_dim 64 / 128, block_size 16 / 32, num_q_heads / num_kv_heads <= 128.
  * Accumulation is fp32 on the tensor cores; probabilities enter the P.V product as
  * hi + lo halves of the 16-bit type, so they keep fp32-level accuracy.  A kv head with

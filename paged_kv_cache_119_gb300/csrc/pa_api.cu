@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <initializer_list>
 #include <mutex>
 #include <vector>
 
@@ -35,6 +36,20 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb)
 {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
     return na && nb && x < y + nb && y < x + na;
+}
+
+// Whether [ws, ws + n) shares a byte with any of the buffers: a workspace the kernels
+// write while they read the call's inputs must be disjoint from all of them.
+struct Span {
+    const void* p;
+    size_t n;
+};
+bool overlaps_any(const void* ws, size_t n, std::initializer_list<Span> bufs)
+{
+    for (const Span& b : bufs)
+        if (overlaps(ws, n, b.p, b.n))
+            return true;
+    return false;
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -420,6 +435,10 @@ int decode_impl(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
     if (overlaps(out, out_bytes, q, q_bytes) || overlaps(out, out_bytes, k_cache, pool_bytes) ||
         overlaps(out, out_bytes, v_cache, pool_bytes))
         return PA_ERR_INVALID;
+    const std::initializer_list<Span> inputs = {
+        {out, out_bytes}, {q, q_bytes}, {k_cache, pool_bytes}, {v_cache, pool_bytes},
+        {block_tables, (size_t)num_seqs * (size_t)block_table_stride * 4},
+        {context_lens, (size_t)num_seqs * 4}};
 
     bool order_seqs = false;
     const int P = decode_partition(q_dtype, kv_dtype, num_seqs, num_kv_heads, group, head_dim,
@@ -452,7 +471,7 @@ int decode_impl(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
                                              head_dim, &ml_off);
         if (!workspace || workspace_bytes < need || !aligned16(workspace))
             return PA_ERR_WORKSPACE;
-        if (overlaps(out, out_bytes, workspace, need))
+        if (overlaps_any(workspace, need, inputs))
             return PA_ERR_INVALID;
         p.part_o = static_cast<float*>(workspace);
         p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ml_off);
@@ -466,8 +485,7 @@ int decode_impl(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
     // the workspace has room for the order and touches none of the inputs it is built from
     const size_t order_bytes = seq_order_bytes(num_seqs);
     if (P == 0 && order_seqs && workspace && aligned16(workspace) &&
-        workspace_bytes >= order_bytes && !overlaps(out, out_bytes, workspace, order_bytes) &&
-        !overlaps(context_lens, (size_t)num_seqs * 4, workspace, order_bytes)) {
+        workspace_bytes >= order_bytes && !overlaps_any(workspace, order_bytes, inputs)) {
         int2* order = static_cast<int2*>(workspace);
         if (launch_seq_order(context_lens, num_seqs, max_context_len, order, st) != cudaSuccess)
             return PA_ERR_CUDA;
@@ -636,6 +654,10 @@ static int chunk_impl(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_d
     if (overlaps(out, out_bytes, q, q_bytes) || overlaps(out, out_bytes, k_cache, pool_bytes) ||
         overlaps(out, out_bytes, v_cache, pool_bytes))
         return PA_ERR_INVALID;
+    const std::initializer_list<Span> inputs = {
+        {out, out_bytes}, {q, q_bytes}, {k_cache, pool_bytes}, {v_cache, pool_bytes},
+        {block_tables, (size_t)num_seqs * (size_t)block_table_stride * 4},
+        {context_lens, (size_t)num_seqs * 4}, {query_start, (size_t)(num_seqs + 1) * 4}};
 
     const int P = plan.partition;
     ChunkParams p{};
@@ -666,7 +688,7 @@ static int chunk_impl(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_d
                                              head_dim, &ml_off);
         if (!workspace || workspace_bytes < need || !aligned16(workspace))
             return PA_ERR_WORKSPACE;
-        if (overlaps(out, out_bytes, workspace, need))
+        if (overlaps_any(workspace, need, inputs))
             return PA_ERR_INVALID;
         p.part_o = static_cast<float*>(workspace);
         p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ml_off);

@@ -94,6 +94,16 @@ def test_decode_split_needs_workspace(lib):
     assert lib.pa_decode(*decode_args(part=16, max_ctx=64)) == N.PA_ERR_WORKSPACE
 
 
+def test_decode_workspace_must_not_overlap_inputs(lib):
+    # the split writes partial rows into the workspace while it reads the inputs
+    need = lib.pa_decode_workspace_bytes(2, 4, 128, 64, 16, 16)
+    assert need > 0
+    for name, base in (("out", FAKE), ("q", FAKE * 2), ("k_cache", FAKE * 3),
+                       ("block_tables", FAKE * 5), ("context_lens", FAKE * 6)):
+        args = decode_args(part=16, max_ctx=64, ws=base, ws_bytes=need)
+        assert lib.pa_decode(*args) == N.PA_ERR_INVALID, name
+
+
 def test_decode_empty_batch_is_a_no_op(lib):
     assert lib.pa_decode(*decode_args(S=0)) == N.PA_OK
 
@@ -194,6 +204,14 @@ def chunk_args(**kw):
 def test_chunk_attention_rejects(lib, kw, status):
     assert lib.pa_chunk_attention(*chunk_args(**kw)) == status
 
+
+def test_chunk_workspace_must_not_overlap_inputs(lib):
+    need = lib.pa_chunk_workspace_bytes(12, 8, 128, 256, 64)
+    assert need > 0
+    for name, base in (("out", FAKE), ("q", FAKE * 16), ("block_tables", FAKE * 130),
+                       ("context_lens", FAKE * 131), ("query_start", FAKE * 132)):
+        args = chunk_args(part=64, max_ctx=256, bt_stride=16, ws=base, ws_bytes=need)
+        assert lib.pa_chunk_attention(*args) == N.PA_ERR_INVALID, name
 
 def test_chunk_attention_empty_is_a_no_op(lib):
     assert lib.pa_chunk_attention(*chunk_args(S=0)) == N.PA_OK
