@@ -56,8 +56,9 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache
     out [S, Hq, D] (float32 or q's dtype), q [S, Hq, D], k_cache / v_cache
     [N, Hkv, B, D], block_tables [S, W] int32, context_lens [S] int32.
     max_context_len defaults to W * block_size (an upper bound needing no
-    device-to-host read).  A workspace is allocated with torch if the call
-    splits and none is given.
+    device-to-host read).  When no workspace is given, one of
+    pa_decode_workspace_bytes(...) is allocated with torch: the split's partial
+    rows, or for an automatic one-pass call the longest-first dispatch order.
     """
     for name, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
                     ("block_tables", block_tables), ("context_lens", context_lens)):
