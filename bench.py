@@ -71,11 +71,18 @@ WORKLOADS["llama13b_swap"] = (
     "(all-or-nothing per sequence), one layer's K and V pools (160 KB blocks), out to a "
     "pinned CPU pool and back into the GPU pool, one pa_swap_blocks launch each way")
 SWAP_METRIC = "paged KV swap GB/s (out + in)"
+# every workload above, each measured briefly in the default run's `configs` object
+CONFIG_ROWS = ("opt13b", "llama13b", "prefix", "long16", "long32", "opt13b_fp8",
+               "llama13b_fp8", "prefix_fp8", "long16_fp8", "long32_fp8", "llama13b_verify4",
+               "llama13b_verify4_fp8", "long16_chunk512", "long16_chunk512_fp8",
+               "llama13b_swap")
 DTYPE_NAME = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32",
               torch.float8_e4m3fn: "fp8_e4m3"}
 METRIC = "paged decode attention KV GB/s"
 KERNEL_SRC = os.path.join(ROOT, "paged_kv_cache_119_gb300", "csrc", "decode_kernel.cuh")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.md")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+# nominal GB300 HBM3e bandwidth, context for the measured fractions
+NOMINAL_HBM_GBS = 7900.0
 
 
 def parse_args(argv=None):
@@ -95,6 +102,13 @@ def parse_args(argv=None):
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the short runs of the other workloads (the `configs` object)")
+    ap.add_argument("--config-steps", type=int, default=10,
+                    help="timed steps of each workload in the `configs` object")
+    ap.add_argument("--config-warmup", type=int, default=3)
+    ap.add_argument("--no-read-probe", action="store_true",
+                    help="skip the read-only bandwidth probe reported beside the copy peak")
     return ap.parse_args(argv)
 
 
@@ -155,21 +169,16 @@ def kernel_hash() -> str:
 
 
 def recorded_traffic(config: str):
-    """ncu DRAM bytes per decode launch, if recorded for the current kernel source
-    (a row of the markdown table in profiles/decode_traffic.md)."""
+    """ncu DRAM bytes per attention launch, if recorded for the current kernel sources
+    (profiles/decode_traffic.json, one row per config)."""
     try:
         with open(TRAFFIC_FILE, encoding="utf-8") as f:
-            lines = f.read().splitlines()
-    except OSError:
+            row = json.load(f)["rows"][config]
+    except (OSError, KeyError, ValueError):
         return None
-    for line in lines:
-        cells = [c.strip() for c in line.strip().strip("|").split("|")]
-        if len(cells) >= 3 and cells[0] == config and cells[1] == kernel_hash():
-            try:
-                return int(cells[2])
-            except ValueError:
-                return None
-    return None
+    if row.get("kernel_hash") != kernel_hash():
+        return None
+    return int(row["dram_bytes_per_launch"])
 
 
 def algorithmic_bytes(w) -> dict:
@@ -274,29 +283,40 @@ def launched_split(pa, w) -> bool:
                                          w.max_context_len, 0) > 0
 
 
-def dominant_kernel(w) -> str:
-    """The attention kernel the library runs for this workload (its routing rules:
-    E4M3 at head_dim 128 with at most four rows per kv head on the tcgen05 E4M3 decode;
-    at least four query heads, or a short chunk, per kv head on the mma.sync decode;
-    long chunks on the tcgen05 chunk kernel (over E4M3 caches at head_dim 128 through
-    an f16 conversion stage); otherwise the CUDA-core decode)."""
-    group = w.num_q_heads // w.num_kv_heads
+def dominant_kernel(pa, w) -> str:
+    """The attention kernel the library runs for this workload, as the library itself
+    reports it (pa_decode_kernel_name / pa_chunk_kernel_name: the launchers' own rule)."""
+    kv = w.k_cache.dtype
     if w.query_start is not None:
-        rows = w.max_query_len * group
-        if rows <= 32 or (w.fp8 and w.head_dim != 128):
-            nh = 4 if rows <= 4 else 8
-            if w.fp8 and w.head_dim == 128 and nh <= 4:
-                return "decode_tc8_kernel (chunk rows)"
-            return "decode_mma_kernel (chunk rows)"
-        return "chunk_attn_kernel" + (" (E4M3 tiles converted to f16)" if w.fp8 else "")
-    gc = next(g for g in (8, 4, 2, 1) if group % g == 0)
-    if w.fp8:
-        if w.head_dim == 128 and gc <= 4:
-            return "decode_tc8_kernel"
-        return "decode_mma_kernel" if gc >= 4 else "decode_kernel"
-    if w.dtype != torch.float32 and gc >= 4:
-        return "decode_mma_kernel"
-    return "decode_kernel"
+        return pa.pa_chunk_kernel_name(kv, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                       w.max_query_len)
+    return pa.pa_decode_kernel_name(kv, w.num_q_heads, w.num_kv_heads, w.head_dim)
+
+
+def percentiles(vals) -> dict:
+    """p10 / p50 / p90 of a list (nearest rank)."""
+    v = sorted(vals)
+    pick = lambda f: v[min(len(v) - 1, max(0, int(math.ceil(f * len(v))) - 1))]
+    return {"p10": pick(0.1), "p50": pick(0.5), "p90": pick(0.9)}
+
+
+def read_probe_gbs(pa, dev, nbytes=4 << 30, reps=10) -> float:
+    """Read-only bandwidth of this GPU: pa_stream_read over a 4 GiB buffer (larger than
+    L2), median of `reps` launches timed with CUDA events on the current stream."""
+    buf = torch.ones(nbytes // 4, dtype=torch.int32, device=dev)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        pa.pa_stream_read(buf, sink)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for b, e in ev:
+        b.record()
+        pa.pa_stream_read(buf, sink)
+        e.record()
+    torch.cuda.synchronize()
+    ms = percentiles([b.elapsed_time(e) for b, e in ev])["p50"]
+    del buf
+    return nbytes / (ms / 1e3) / 1e9
 
 
 def step_ops(pa, w):
@@ -520,6 +540,49 @@ def run_swap(args, rank, world, local):
     return line
 
 
+def swap_row(pa, dev, steps, warmup, local) -> dict:
+    """The swap step of the LLaMA-13B batch (last 64 sequences' blocks out to a pinned
+    CPU pool and back, one launch each way) for the `configs` object."""
+    w = make_workload("llama13b", dev)
+    blocks, bb = swap_plan(w, 64)
+    n = len(blocks)
+    cpu_k = torch.empty((n,) + tuple(w.k_cache.shape[1:]), dtype=w.dtype).pin_memory()
+    cpu_v = torch.empty_like(cpu_k).pin_memory()
+    out_pairs = torch.tensor([(b, i) for i, b in enumerate(blocks)], dtype=torch.int64)
+    in_pairs = out_pairs.flip(1).contiguous()
+    for _ in range(warmup):
+        pa.pa_swap_blocks([w.k_cache, w.v_cache], [cpu_k, cpu_v], out_pairs)
+        pa.pa_swap_blocks([cpu_k, cpu_v], [w.k_cache, w.v_cache], in_pairs)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for e in ev:
+        e[0].record()
+        pa.pa_swap_blocks([w.k_cache, w.v_cache], [cpu_k, cpu_v], out_pairs)
+        e[1].record()
+        pa.pa_swap_blocks([cpu_k, cpu_v], [w.k_cache, w.v_cache], in_pairs)
+        e[2].record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop(t0, time.time())
+    step = percentiles([e[0].elapsed_time(e[2]) for e in ev])
+    mean_ms = sum(e[0].elapsed_time(e[2]) for e in ev) / steps
+    peaks = link_peak_gbs(dev)
+    peak = max((peaks["d2h_dma"] + peaks["h2d_dma"]) / 2, (peaks["d2h_sm"] + peaks["h2d_sm"]) / 2)
+    achieved = 4 * n * bb / (mean_ms / 1e3) / 1e9
+    del w, cpu_k, cpu_v
+    torch.cuda.empty_cache()
+    return {"kernel": "swap_blocks_kernel", "bound": "link", "achieved": round(achieved, 1),
+            "unit": "GB/s", "peak": round(peak, 1), "frac": round(achieved / peak, 4),
+            "traffic": None, "step_us_p50": round(step["p50"] * 1e3, 2),
+            "step_us_p10": round(step["p10"] * 1e3, 2), "step_us_p90": round(step["p90"] * 1e3, 2),
+            "step_us_mean": round(mean_ms * 1e3, 2), "steps": steps, "warmup": warmup,
+            "peak_kind": "measured in this run: faster of the copy engines' and one SM streaming "
+                         "launch's pinned<->device rate, mean of both directions",
+            "clocks": clocks}
+
+
 def swap_cpu_baseline(w, blocks, bb, budget_s):
     """The oracle's byte moves on host copies of the same pools and pairs."""
     import oracle
@@ -540,6 +603,158 @@ def swap_cpu_baseline(w, blocks, bb, budget_s):
                       f"{len(blocks)} blocks x K, V, {el:.1f} s"}
 
 
+def workspace_for(pa, w, part, dev):
+    """The workspace a call with this partition_size needs (one byte when none)."""
+    if w.query_start is not None:
+        n = pa.pa_chunk_workspace_bytes(w.q.shape[0], w.num_q_heads, w.head_dim,
+                                        w.max_context_len, max(part, 0)) if part >= 0 else 0
+    else:
+        n = pa.pa_decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.head_dim,
+                                         w.max_context_len, w.block_size, max(part, 0)) \
+            if part >= 0 else 0
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+
+
+def timed_steps(pa, w, steps, warmup, part, dev, flush=None, barrier=None, sampler=None):
+    """Runs `warmup` untimed steps, then exactly `steps` timed ones bracketed by CUDA
+    events on the launching stream, with events between the step's kernels.  Returns
+    the total time, per-step times and the buffers the e2e leg reuses."""
+    out = torch.empty(w.q.shape, dtype=w.dtype, device=dev)
+    ws = workspace_for(pa, w, part, dev)
+    cow_src = None
+    if w.copy_pairs is not None:
+        # the CoW copy reads the original tails and writes scratch destinations each step,
+        # so the decoded state stays the same from step to step
+        pa.pa_copy_blocks([w.k_cache], [w.v_cache], w.copy_pairs)
+        cow_src = w.copy_pairs.copy()
+    write, decode = step_ops(pa, w)
+
+    def step(e=None):
+        if e is not None:
+            e[0].record()
+        if cow_src is not None:
+            pa.pa_copy_blocks([w.k_cache], [w.v_cache], cow_src)
+        if e is not None:
+            e[1].record()
+        write(w.k_new, w.v_new, w.slot_mapping)
+        if e is not None:
+            e[2].record()
+        decode(out, w.q, w.block_tables, w.context_lens, part, ws)
+        if e is not None:
+            e[3].record()
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if pa.pa_get_device_error():
+        raise RuntimeError("device error word set during warm-up")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    begin, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if sampler is not None:
+        sampler.start()
+    if barrier is not None:
+        barrier()
+    torch.cuda.synchronize()
+    t0_wall = time.time()
+    if flush is None:
+        begin.record()
+        for i in range(steps):
+            step(ev[i])
+        end.record()
+        torch.cuda.synchronize()
+        total_ms = begin.elapsed_time(end)
+    else:
+        total_ms = 0.0
+        for i in range(steps):
+            flush.fill_(i & 0xff)
+            begin.record()
+            step(ev[i])
+            end.record()
+            torch.cuda.synchronize()
+            total_ms += begin.elapsed_time(end)
+    if barrier is not None:
+        barrier()
+    t1_wall = time.time()
+    clocks = sampler.stop(t0_wall, t1_wall) if sampler is not None else None
+    torch.cuda.synchronize()
+    if pa.pa_get_device_error():
+        raise RuntimeError("device error word set during the timed steps")
+    return {"total_ms": total_ms,
+            "step_ms": [e[0].elapsed_time(e[3]) for e in ev],
+            "copy_ms": [e[0].elapsed_time(e[1]) for e in ev],
+            "reshape_ms": [e[1].elapsed_time(e[2]) for e in ev],
+            "decode_ms": [e[2].elapsed_time(e[3]) for e in ev],
+            "clocks": clocks, "out": out, "ws": ws, "copies": cow_src is not None}
+
+
+def attention_summary(pa, w, config, part, t) -> dict:
+    """Roofline of the attention launch and the step's launch count, from one
+    timed_steps result: achieved bytes (or flops for long chunks) per average launch."""
+    nbytes = algorithmic_bytes(w)
+    chunk = w.query_start is not None
+    decode_ms = sum(t["decode_ms"]) / len(t["decode_ms"])
+    peak, peak_kind = load_peaks()
+    achieved = nbytes["decode"] / (decode_ms / 1e3) / 1e9
+    split = part > 0 and w.max_context_len > part
+    if part == 0:
+        split = launched_split(pa, w)
+    # an automatic one-pass decode of several waves first builds its longest-first order
+    ordered = (not chunk and part == 0 and not split and
+               pa.pa_decode_orders_sequences(w.q.dtype, w.k_cache.dtype, w.num_seqs,
+                                             w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                             w.block_size, w.max_context_len, 0))
+    launches = 2 + (1 if split else 0) + (1 if ordered else 0) + (1 if t["copies"] else 0)
+    kernel = (dominant_kernel(pa, w) + (" + reduce kernel" if split else "")
+              + (" (after the order kernel)" if ordered else ""))
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": recorded_traffic(config), "kernel": kernel,
+                "peak_kind": ("measured copy bandwidth (MEASURED_PEAKS.json hbm_gbs: read + "
+                              "write)" if peak_kind == "measured" else "fallback 6.8 TB/s"),
+                "algorithmic_bytes_per_launch": nbytes["decode"],
+                "nominal_gbs": NOMINAL_HBM_GBS,
+                "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4)}
+    flops = algorithmic_flops(w)
+    tpeak, tpeak_kind = load_tensor_peak()
+    if chunk and flops / (tpeak * 1e12) > nbytes["decode"] / (peak * 1e9):
+        # bound by the tensor cores: a long chunk makes every K/V byte feed many rows
+        tflops = flops / (decode_ms / 1e3) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(tflops, 1), "peak": tpeak,
+                    "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
+                    "traffic": recorded_traffic(config), "kernel": kernel,
+                    "peak_kind": f"{tpeak_kind} dense bf16 (MEASURED_PEAKS.json)",
+                    "algorithmic_flops_per_launch": flops,
+                    "algorithmic_bytes_per_launch": nbytes["decode"]}
+    return {"roofline": roofline, "launches_per_step": launches, "flops": flops,
+            "bytes": nbytes, "decode_ms_mean": decode_ms}
+
+
+def config_row(pa, config, dev, steps, warmup, local) -> dict:
+    """One workload's throughput for the bench line's `configs` object: a short run of
+    its step with its own clock sample."""
+    if config == "llama13b_swap":
+        return swap_row(pa, dev, steps, warmup, local)
+    w = make_workload(config, dev)
+    sampler = ClockSampler(local)
+    t = timed_steps(pa, w, steps, warmup, 0, dev, sampler=sampler)
+    a = attention_summary(pa, w, config, 0, t)
+    r = a["roofline"]
+    dec, stp = percentiles(t["decode_ms"]), percentiles(t["step_ms"])
+    row = {"kernel": r["kernel"], "bound": r["bound"], "achieved": r["achieved"],
+           "unit": r["unit"], "peak": r["peak"], "frac": r["frac"], "traffic": r["traffic"],
+           "decode_us_p50": round(dec["p50"] * 1e3, 2),
+           "decode_us_p10": round(dec["p10"] * 1e3, 2),
+           "decode_us_p90": round(dec["p90"] * 1e3, 2),
+           "step_us_p50": round(stp["p50"] * 1e3, 2),
+           "step_us_mean": round(t["total_ms"] / steps * 1e3, 2),
+           "steps": steps, "warmup": warmup, "clocks": t["clocks"]}
+    if r["bound"] == "hbm":
+        row["frac_of_nominal"] = r["frac_of_nominal"]
+    del w, t
+    torch.cuda.empty_cache()
+    return row
+
+
 def run_ours(args, rank, world, local):
     import paged_kv_cache_119_gb300 as pa
     from paged_kv_cache_119_gb300 import build as pa_build
@@ -554,126 +769,38 @@ def run_ours(args, rank, world, local):
     pa_build.build()
     w = make_workload(args.config, dev, args.num_seqs)
     part = 0 if args.partition_size is None else args.partition_size
-    nbytes = algorithmic_bytes(w)
     chunk = w.query_start is not None
-    out = torch.empty(w.q.shape, dtype=w.dtype, device=dev)
-    if chunk:
-        ws_bytes = pa.pa_chunk_workspace_bytes(w.q.shape[0], w.num_q_heads, w.head_dim,
-                                               w.max_context_len, max(part, 0)) \
-            if part >= 0 else 0
-    else:
-        ws_bytes = pa.pa_decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.head_dim,
-                                                w.max_context_len, w.block_size, max(part, 0)) \
-            if part >= 0 else 0
-    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if args.flush_l2 else None
-    cow_src = None
-    if w.copy_pairs is not None:
-        # the CoW copy reads the original tails and writes scratch destinations each step,
-        # so the decoded state stays the same from step to step
-        pa.pa_copy_blocks([w.k_cache], [w.v_cache], w.copy_pairs)
-        cow_src = w.copy_pairs.copy()
-
-    write, decode = step_ops(pa, w)
-
-    def step(e=None):
-        if cow_src is not None:
-            pa.pa_copy_blocks([w.k_cache], [w.v_cache], cow_src)
-        if e is not None:
-            e[0].record()
-        write(w.k_new, w.v_new, w.slot_mapping)
-        if e is not None:
-            e[1].record()
-        decode(out, w.q, w.block_tables, w.context_lens, part, ws)
-        if e is not None:
-            e[2].record()
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if pa.pa_get_device_error():
-        raise RuntimeError("device error word set during warm-up")
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    begin, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local)
-    if rank == 0:
-        sampler.start()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    t0_wall = time.time()
-    if flush is None:
-        begin.record()
-        for i in range(args.steps):
-            step(ev[i])
-        end.record()
-        torch.cuda.synchronize()
-        total_ms = begin.elapsed_time(end)
-    else:
-        total_ms = 0.0
-        for i in range(args.steps):
-            flush.fill_(i & 0xff)
-            begin.record()
-            step(ev[i])
-            end.record()
-            torch.cuda.synchronize()
-            total_ms += begin.elapsed_time(end)
-    if world > 1:
-        torch.distributed.barrier()
-    t1_wall = time.time()
-    clocks = sampler.stop(t0_wall, t1_wall) if rank == 0 else None
-    torch.cuda.synchronize()
-    reshape_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
-    decode_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
-    if pa.pa_get_device_error():
-        raise RuntimeError("device error word set during the timed steps")
-
+    sampler = ClockSampler(local) if rank == 0 else None
+    barrier = torch.distributed.barrier if world > 1 else None
+    t = timed_steps(pa, w, args.steps, args.warmup, part, dev, flush=flush, barrier=barrier,
+                    sampler=sampler)
+    total_ms = t["total_ms"]
     sec = max_over_ranks(total_ms / 1e3, dev) if world > 1 else total_ms / 1e3
+    a = attention_summary(pa, w, args.config, part, t)
+    nbytes = a["bytes"]
     value, _ = aggregate([sec], [nbytes["kv"] * args.steps * world])
     value /= 1e9
 
-    e2e = None if args.no_e2e else measure_e2e(args, pa, w, out, ws, part, dev)
+    e2e = None if args.no_e2e else measure_e2e(args, pa, w, t["out"], t["ws"], part, dev)
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank != 0:
         return None
-    peak, peak_kind = load_peaks()
-    achieved = nbytes["decode"] / (decode_ms / 1e3) / 1e9
-    split = part > 0 and w.max_context_len > part
-    if part == 0:
-        split = launched_split(pa, w)
-    # an automatic one-pass decode of several waves first builds its longest-first order
-    ordered = (not chunk and part == 0 and not split and
-               pa.pa_decode_orders_sequences(w.q.dtype, w.k_cache.dtype, w.num_seqs,
-                                             w.num_q_heads, w.num_kv_heads, w.head_dim,
-                                             w.block_size, w.max_context_len, 0))
-    launches_per_step = (2 + (1 if split else 0) + (1 if ordered else 0)
-                         + (1 if cow_src is not None else 0))
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": recorded_traffic(args.config),
-                "kernel": dominant_kernel(w) + (" + reduce kernel" if split else "")
-                + (" (after the order kernel)" if ordered else ""),
-                "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
-                if peak_kind == "measured" else "fallback 6.8 TB/s",
-                "algorithmic_bytes_per_launch": nbytes["decode"]}
+    roofline = a["roofline"]
+    if roofline["bound"] == "hbm" and not args.no_read_probe:
+        rp = read_probe_gbs(pa, dev)
+        roofline["read_probe_gbs"] = round(rp, 1)
+        roofline["frac_of_read_probe"] = round(roofline["achieved"] / rp, 4)
     metric, unit = METRIC, "GB/s"
-    flops = algorithmic_flops(w)
-    tpeak, tpeak_kind = load_tensor_peak()
-    if chunk and flops / (tpeak * 1e12) > nbytes["decode"] / (peak * 1e9):
-        # bound by the tensor cores: a long chunk makes every K/V byte feed many rows
-        tflops = flops / (decode_ms / 1e3) / 1e12
-        roofline = {"bound": "tensor", "achieved": round(tflops, 1), "peak": tpeak,
-                    "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
-                    "traffic": recorded_traffic(args.config),
-                    "kernel": roofline["kernel"],
-                    "peak_kind": f"{tpeak_kind} dense bf16 (MEASURED_PEAKS.json)",
-                    "algorithmic_flops_per_launch": flops,
-                    "algorithmic_bytes_per_launch": nbytes["decode"]}
+    flops = a["flops"]
+    if roofline["bound"] == "tensor":
         value = flops * args.steps * world / sec / 1e12
         metric, unit = CHUNK_METRIC[args.config], "TFLOP/s"
     elif chunk:
         metric = CHUNK_METRIC[args.config]
+    decode_ms = a["decode_ms_mean"]
+    dec, stp = percentiles(t["decode_ms"]), percentiles(t["step_ms"])
     line = {
         "metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -689,12 +816,17 @@ def run_ours(args, rank, world, local):
                           "is larger than the 129 MB L2"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "us_per_step": round(total_ms / args.steps * 1e3, 2),
-        "decode_us": round(decode_ms * 1e3, 2), "reshape_us": round(reshape_ms * 1e3, 2),
+        "decode_us": round(decode_ms * 1e3, 2),
+        "reshape_us": round(sum(t["reshape_ms"]) / args.steps * 1e3, 2),
+        "step_us_p10": round(stp["p10"] * 1e3, 2), "step_us_p50": round(stp["p50"] * 1e3, 2),
+        "step_us_p90": round(stp["p90"] * 1e3, 2),
+        "decode_us_p10": round(dec["p10"] * 1e3, 2),
+        "decode_us_p50": round(dec["p50"] * 1e3, 2),
+        "decode_us_p90": round(dec["p90"] * 1e3, 2),
         "decode_kv_gbs": round(nbytes["kv"] / (decode_ms / 1e3) / 1e9, 1),
-        "pct_of_hbm_peak": round(100 * achieved / peak, 1),
         "roofline": roofline,
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks,
+        "gpu_launches": a["launches_per_step"] * args.steps,
+        "clocks": t["clocks"],
     }
     if chunk:
         line["query_rows"] = int(w.q.shape[0])
@@ -704,6 +836,11 @@ def run_ours(args, rank, world, local):
             e2e["value"] = round(flops / (e2e["ms_per_step"] / 1e3) / 1e12, 2)
             e2e["unit"] = "TFLOP/s"
         line["e2e"] = e2e
+    if not args.no_configs and args.num_seqs is None and world == 1:
+        del t
+        torch.cuda.empty_cache()
+        line["configs"] = {c: config_row(pa, c, dev, args.config_steps, args.config_warmup, local)
+                           for c in CONFIG_ROWS if c != args.config}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
     return line
@@ -845,8 +982,10 @@ def cpu_baseline(w, budget_s: float) -> dict:
     if w.query_start is not None:
         threads = oracle.max_threads()
         value, unit, sample = _chunk_sample(w, h, budget_s, threads)
+        v1, _, sample1 = _chunk_sample(w, h, budget_s / 3, 1)
         return {"value": round(value, 4), "unit": unit, "cores": threads, "kind": "oracle",
-                "sample": sample}
+                "sample": sample, "one_thread": {"value": round(v1, 5), "unit": unit,
+                                                 "cores": 1, "sample": sample1}}
     threads = oracle.max_threads()
     # calibrate on the first 8 sequences, then size the sample to the budget
     t = time.perf_counter()
@@ -864,9 +1003,19 @@ def cpu_baseline(w, budget_s: float) -> dict:
         _decode_slice(h, w, 0, seqs, threads)
     elapsed = time.perf_counter() - t
     gbs = passes * _sample_bytes(w, seqs) / elapsed / 1e9
+    # the same oracle on one thread: leading sequences until about budget_s / 3 seconds
+    n1, t = 0, time.perf_counter()
+    while n1 < w.num_seqs and (n1 == 0 or time.perf_counter() - t < budget_s / 3):
+        _decode_slice(h, w, n1, n1 + 1, 1)
+        n1 += 1
+    el1 = time.perf_counter() - t
     return {"value": round(gbs, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"fp64 C oracle (OpenMP, {threads} threads): {passes} pass(es) over the "
-                      f"first {seqs} of {w.num_seqs} sequences, all heads, {elapsed:.1f} s"}
+                      f"first {seqs} of {w.num_seqs} sequences, all heads, {elapsed:.1f} s",
+            "one_thread": {"value": round(_sample_bytes(w, n1) / el1 / 1e9, 4), "unit": "GB/s",
+                           "cores": 1,
+                           "sample": f"fp64 C oracle, 1 thread: the first {n1} of {w.num_seqs} "
+                                     f"sequences, all heads, {el1:.1f} s"}}
 
 
 def _decode_slice(h, w, s0, s1, threads):

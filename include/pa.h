@@ -47,6 +47,11 @@
  *     skips the access and, for pa_decode, writes NaN to the affected outputs.
  *     Kernels never trap.
  *   - A context length of 0 yields an all-zero output row.
+ *   - Per-device state (the SM count, the error word, encoded tensor maps and the
+ *     no-alloc scratch address) is looked up once per device and process.  Do not
+ *     call cudaDeviceReset on a device the library has been used on while the
+ *     process still uses the library: the cached addresses would then point into
+ *     the destroyed context.
  */
 #ifndef PA_H_
 #define PA_H_
@@ -81,7 +86,10 @@ typedef enum {
  * head, partition) one fp32 partial output row of head_dim values plus its running
  * max and sum; with the automatic choice, at least 8 bytes per sequence (rounded up
  * to 256) for the longest-first dispatch order of a one-pass call (see pa_decode).
- * Pure host arithmetic; no CUDA call.  Returns 0 for invalid sizes.
+ * Passing a workspace of this size to an automatic (partition_size 0) call is what
+ * turns that order on: a call without a workspace that does not split runs the
+ * sequences in index order, with the same results but a longer tail on mixed-length
+ * batches.  Pure host arithmetic; no CUDA call.  Returns 0 for invalid sizes.
  */
 size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                                  int32_t max_context_len, int32_t block_size,
@@ -359,6 +367,33 @@ int32_t pa_chunk_partition_tokens(pa_dtype kv_dtype, int32_t num_seqs, int32_t n
                                   int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                                   int32_t max_query_len, int32_t max_context_len,
                                   int32_t partition_size);
+
+/*
+ * Name of the attention kernel a pa_decode / pa_decode_fp8 call with these arguments
+ * launches: "decode_kernel" (CUDA cores), "decode_mma_kernel" (mma.sync tensor cores)
+ * or "decode_tc8_kernel" (tcgen05 over E4M3 codes); NULL for arguments those calls
+ * reject.  The launchers route by the same rule.  A static string; no CUDA call.
+ */
+const char* pa_decode_kernel_name(pa_dtype kv_dtype, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim);
+/*
+ * The same for pa_chunk_attention (kv_dtype PA_F16 / PA_BF16) and
+ * pa_chunk_attention_fp8 (kv_dtype PA_FP8_E4M3): "chunk_attn_kernel" (tcgen05, long
+ * chunks; over E4M3 caches with an f16 conversion stage) or a decode kernel's chunk-row
+ * mode; NULL for arguments those calls reject.
+ */
+const char* pa_chunk_kernel_name(pa_dtype kv_dtype, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t max_query_len);
+
+/*
+ * Measurement helper, outside the attention path: reads every byte of buf once with
+ * streaming 16-byte loads (8 CTAs of 128 threads per SM) and XORs a checksum into
+ * *sink, so that a caller timing it on `stream` learns the read-only bandwidth a
+ * kernel that reads a buffer and writes almost nothing can reach (a copy benchmark
+ * also writes).  buf: device, 16-byte aligned, bytes a nonzero multiple of 16;
+ * sink: device uint32, caller-owned.  Asynchronous; PA_ERR_INVALID on bad arguments.
+ */
+int pa_stream_read(const void* buf, size_t bytes, uint32_t* sink, void* stream);
 
 /*
  * Reads and clears the calling device's error word (PA_DEVERR_* bits).

@@ -454,6 +454,43 @@ def pa_chunk_partition_tokens(kv_dtype: torch.dtype, num_seqs: int, num_q_heads:
     return r
 
 
+def _kv_code(kv_dtype: torch.dtype) -> int:
+    return N.PA_FP8_E4M3 if kv_dtype in (torch.float8_e4m3fn, torch.uint8) else _DT[kv_dtype]
+
+
+def pa_decode_kernel_name(kv_dtype: torch.dtype, num_q_heads: int, num_kv_heads: int,
+                          head_dim: int) -> str:
+    """The attention kernel pa_decode (or, for an E4M3 kv_dtype, pa_decode_fp8) runs for
+    these shapes, as the library routes it."""
+    r = N.load().pa_decode_kernel_name(_kv_code(kv_dtype), num_q_heads, num_kv_heads, head_dim)
+    if r is None:
+        raise ValueError("pa_decode_kernel_name: arguments the decode calls reject")
+    return r.decode()
+
+
+def pa_chunk_kernel_name(kv_dtype: torch.dtype, num_q_heads: int, num_kv_heads: int,
+                         head_dim: int, max_query_len: int) -> str:
+    """The attention kernel pa_chunk_attention (or pa_chunk_attention_fp8) runs for these
+    shapes, as the library routes it."""
+    r = N.load().pa_chunk_kernel_name(_kv_code(kv_dtype), num_q_heads, num_kv_heads, head_dim,
+                                      max_query_len)
+    if r is None:
+        raise ValueError("pa_chunk_kernel_name: arguments the chunk calls reject")
+    return r.decode()
+
+
+def pa_stream_read(buf: torch.Tensor, sink: torch.Tensor, stream=None) -> None:
+    """Measurement helper: stream every byte of buf once (the read-only bandwidth
+    ceiling); a checksum is XORed into sink (a one-element int32 CUDA tensor)."""
+    _cuda("buf", buf)
+    _cuda("sink", sink)
+    if sink.dtype != torch.int32 or sink.numel() < 1:
+        raise TypeError("sink must be an int32 CUDA tensor")
+    N.check("pa_stream_read", N.load().pa_stream_read(buf.data_ptr(),
+                                                       buf.numel() * buf.element_size(),
+                                                       sink.data_ptr(), _stream(stream)))
+
+
 def pa_get_device_error(stream=None) -> int:
     """Read and clear the device error word (PA_DEVERR_* bits).  Synchronises."""
     flags = ctypes.c_uint32(0)

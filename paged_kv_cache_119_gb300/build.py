@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(BUILD_DIR, "libpa.so")
 
 SOURCES = ["pa_api.cu", "cache_ops.cu", "decode_f32.cu", "decode_f16.cu", "decode_bf16.cu",
            "decode_fp8.cu", "decode_tc8.cu", "decode_noalloc.cu", "chunk_attn.cu", "seq_order.cu",
-           "block_manager.cpp"]
+           "probe.cu", "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC,-O2",
               "-Xptxas", "-v", "-I", INCLUDE, "-I", CSRC]

@@ -8,14 +8,14 @@ namespace pa {
 cudaError_t launch_decode_f16(const DecodeParams& p, int head_dim, int block_size, int gc,
                               cudaStream_t stream)
 {
-    if (gc >= kMmaMinHeads)
+    if (decode_kernel_for(PA_F16, head_dim, gc) == DecodeKernel::kMmaSync)
         return launch_decode_mma<__half>(p, head_dim, block_size, gc, stream);
     return launch_decode_typed<__half>(p, head_dim, block_size, gc, stream);
 }
 
 int occupancy_decode_f16(int head_dim, int block_size, int gc)
 {
-    if (gc >= kMmaMinHeads)
+    if (decode_kernel_for(PA_F16, head_dim, gc) == DecodeKernel::kMmaSync)
         return occupancy_decode_mma<__half>(head_dim, block_size, gc);
     return occupancy_decode_typed<__half>(head_dim, block_size, gc);
 }

@@ -13,7 +13,7 @@ template <typename T>
 cudaError_t launch_fp8(const DecodeParams& p, int head_dim, int block_size, int gc,
                        cudaStream_t stream)
 {
-    if (gc >= kMmaMinHeadsFp8)
+    if (decode_kernel_for(PA_FP8_E4M3, head_dim, gc) == DecodeKernel::kMmaSync)
         return launch_decode_mma<T, __nv_fp8_e4m3>(p, head_dim, block_size, gc, stream);
     return launch_decode_typed<T, __nv_fp8_e4m3>(p, head_dim, block_size, gc, stream);
 }
@@ -21,7 +21,7 @@ cudaError_t launch_fp8(const DecodeParams& p, int head_dim, int block_size, int 
 template <typename T>
 int occupancy_fp8(int head_dim, int block_size, int gc)
 {
-    if (gc >= kMmaMinHeadsFp8)
+    if (decode_kernel_for(PA_FP8_E4M3, head_dim, gc) == DecodeKernel::kMmaSync)
         return occupancy_decode_mma<T, __nv_fp8_e4m3>(head_dim, block_size, gc);
     return occupancy_decode_typed<T, __nv_fp8_e4m3>(head_dim, block_size, gc);
 }
@@ -31,7 +31,7 @@ int occupancy_fp8(int head_dim, int block_size, int gc)
 cudaError_t launch_decode_fp8(const DecodeParams& p, pa_dtype q_dtype, int head_dim,
                               int block_size, int gc, cudaStream_t stream)
 {
-    if (use_tc8(head_dim, gc))
+    if (decode_kernel_for(PA_FP8_E4M3, head_dim, gc) == DecodeKernel::kTc8)
         return launch_decode_tc8(p, q_dtype, block_size, gc, stream);
     if (q_dtype == PA_F16)
         return launch_fp8<__half>(p, head_dim, block_size, gc, stream);
@@ -42,7 +42,7 @@ cudaError_t launch_decode_fp8(const DecodeParams& p, pa_dtype q_dtype, int head_
 
 int occupancy_decode_fp8(pa_dtype q_dtype, int head_dim, int block_size, int gc)
 {
-    if (use_tc8(head_dim, gc))
+    if (decode_kernel_for(PA_FP8_E4M3, head_dim, gc) == DecodeKernel::kTc8)
         return occupancy_decode_tc8(q_dtype, block_size, gc);
     if (q_dtype == PA_F16)
         return occupancy_fp8<__half>(head_dim, block_size, gc);

@@ -330,12 +330,11 @@ int decode_partition(pa_dtype q_dtype, pa_dtype kv_dtype, int num_seqs, int num_
     }
     const int64_t units = (int64_t)num_seqs * num_kv_heads * (group / gc);
     const int64_t slots = (int64_t)device_sm_count() * occ;
-    const bool fp8 = kv_dtype == PA_FP8_E4M3;
-    const bool cuda_core = !(fp8 && use_tc8(head_dim, gc)) &&
-                           gc < (fp8 ? kMmaMinHeadsFp8 : kMmaMinHeads);
+    const DecodeKernel kernel = decode_kernel_for(kv_dtype, head_dim, gc);
     if (order_out)
-        *order_out = partition_size == 0 && cuda_core && slots > 0 && units > slots;
-    if (kv_dtype == PA_FP8_E4M3 && use_tc8(head_dim, gc))
+        *order_out = partition_size == 0 && kernel == DecodeKernel::kCudaCore && slots > 0 &&
+                     units > slots;
+    if (kernel == DecodeKernel::kTc8)
         return choose_partition_tc8(partition_size, max_context_len, units, slots);
     return choose_partition(partition_size, max_context_len, units, slots, block_size);
 }
@@ -586,6 +585,40 @@ int32_t pa_chunk_partition_tokens(pa_dtype kv_dtype, int32_t num_seqs, int32_t n
                       num_q_heads, num_kv_heads, head_dim, block_size, max_query_len,
                       max_context_len, partition_size)
         .partition;
+}
+
+const char* pa_decode_kernel_name(pa_dtype kv_dtype, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim)
+{
+    if (!(valid_dtype(kv_dtype) || kv_dtype == PA_FP8_E4M3) || num_q_heads <= 0 ||
+        num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
+        !(head_dim == 64 || head_dim == 128))
+        return nullptr;
+    switch (decode_kernel_for(kv_dtype, head_dim, heads_per_cta(num_q_heads / num_kv_heads))) {
+    case DecodeKernel::kTc8: return "decode_tc8_kernel";
+    case DecodeKernel::kMmaSync: return "decode_mma_kernel";
+    default: return "decode_kernel";
+    }
+}
+
+const char* pa_chunk_kernel_name(pa_dtype kv_dtype, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t max_query_len)
+{
+    if (!(kv_dtype == PA_F16 || kv_dtype == PA_BF16 || kv_dtype == PA_FP8_E4M3) ||
+        num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
+        num_q_heads / num_kv_heads > 128 || !(head_dim == 64 || head_dim == 128) ||
+        max_query_len <= 0)
+        return nullptr;
+    // the route does not depend on the split: a never-split plan needs no device query
+    const ChunkPlan plan = chunk_plan(kv_dtype == PA_FP8_E4M3 ? PA_BF16 : kv_dtype, kv_dtype, 1,
+                                      num_q_heads, num_kv_heads, head_dim, 16, max_query_len,
+                                      max_query_len, -1);
+    if (plan.rows_path)
+        return kv_dtype == PA_FP8_E4M3 && use_tc8(head_dim, plan.nh)
+                   ? "decode_tc8_kernel (chunk rows)"
+                   : "decode_mma_kernel (chunk rows)";
+    return kv_dtype == PA_FP8_E4M3 ? "chunk_attn_kernel (E4M3 tiles converted to f16)"
+                                   : "chunk_attn_kernel";
 }
 
 size_t pa_chunk_workspace_bytes(int64_t num_query_tokens, int32_t num_q_heads, int32_t head_dim,

@@ -94,6 +94,22 @@ int occupancy_decode_fp8(pa_dtype q_dtype, int head_dim, int block_size, int gc)
 // kernel streams faster (measured on GB300: its four consumer warps work on separate
 // blocks and free each block on its own, against one 128-token tile chain per CTA).
 inline bool use_tc8(int head_dim, int rows) { return head_dim == 128 && rows <= 4; }
+
+// The attention kernel a decode call runs, from the cache type, head_dim and the query
+// heads one CTA serves (gc).  The per-dtype launchers route by this function, and
+// pa_decode_kernel_name reports it, so the two cannot disagree.
+enum class DecodeKernel { kCudaCore, kMmaSync, kTc8 };
+inline DecodeKernel decode_kernel_for(pa_dtype kv_dtype, int head_dim, int gc)
+{
+    if (kv_dtype == PA_FP8_E4M3) {
+        if (use_tc8(head_dim, gc))
+            return DecodeKernel::kTc8;
+        return gc >= kMmaMinHeadsFp8 ? DecodeKernel::kMmaSync : DecodeKernel::kCudaCore;
+    }
+    if (kv_dtype != PA_F32 && gc >= kMmaMinHeads)
+        return DecodeKernel::kMmaSync;
+    return DecodeKernel::kCudaCore;
+}
 // The E4M3 tensor-core decode at head_dim 128 (decode_tc8.cu): `rows` = query heads per
 // CTA (1, 2, 4 or 8); makes its own tensor maps.
 cudaError_t launch_decode_tc8(const DecodeParams& p, pa_dtype q_dtype, int block_size, int rows,

@@ -70,9 +70,14 @@ def test_chunk_oracle_sample_runs_on_e4m3_caches():
     assert value > 0 and unit in ("TFLOP/s", "GB/s") and "oracle" in desc
 
 
-def test_dominant_kernel_follows_the_library_routing():
+def test_dominant_kernel_is_the_library_routing():
+    """The roofline's kernel label comes from the library's own routing query."""
+    from paged_kv_cache_119_gb300 import build
+    build.build()
+    import paged_kv_cache_119_gb300 as pa
+
     def label(config, **kw):
-        return bench.dominant_kernel(bench.make_workload(config, "cpu", **kw))
+        return bench.dominant_kernel(pa, bench.make_workload(config, "cpu", **kw))
     assert label("llama13b", num_seqs=2) == "decode_kernel"                 # MHA, CUDA cores
     assert label("long16", num_seqs=1) == "decode_mma_kernel"               # group 8
     assert label("llama13b_fp8", num_seqs=2) == "decode_tc8_kernel"         # E4M3 MHA
@@ -82,3 +87,28 @@ def test_dominant_kernel_follows_the_library_routing():
     assert label("long16_chunk512", num_seqs=1) == "chunk_attn_kernel"
     assert label("long16_chunk512_fp8", num_seqs=1) == \
         "chunk_attn_kernel (E4M3 tiles converted to f16)"
+    assert pa.pa_decode_kernel_name(torch.float32, 64, 8, 128) == "decode_kernel"
+
+
+def test_percentiles_nearest_rank():
+    p = bench.percentiles(list(range(1, 21)))
+    assert (p["p10"], p["p50"], p["p90"]) == (2, 10, 18)
+    assert bench.percentiles([7.0]) == {"p10": 7.0, "p50": 7.0, "p90": 7.0}
+
+
+def test_traffic_rows_count_only_for_current_sources(tmp_path, monkeypatch):
+    import json
+    f = tmp_path / "t.json"
+    f.write_text(json.dumps({"rows": {"a": {"kernel_hash": bench.kernel_hash(),
+                                            "dram_bytes_per_launch": 123},
+                                      "b": {"kernel_hash": "0" * 16,
+                                            "dram_bytes_per_launch": 456}}}))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.recorded_traffic("a") == 123
+    assert bench.recorded_traffic("b") is None           # stale: captured from other sources
+    assert bench.recorded_traffic("c") is None
+
+
+def test_bench_reads_no_markdown():
+    src = open(bench.__file__, encoding="utf-8").read()
+    assert ".md" not in src
