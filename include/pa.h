@@ -387,7 +387,7 @@ const char* pa_chunk_kernel_name(pa_dtype kv_dtype, int32_t num_q_heads, int32_t
 
 /*
  * Measurement helper, outside the attention path: reads every byte of buf once with
- * streaming 16-byte loads (8 CTAs of 128 threads per SM) and XORs a checksum into
+ * 16-byte loads (8 CTAs of 128 threads per SM) and XORs a checksum into
  * *sink, so that a caller timing it on `stream` learns the read-only bandwidth a
  * kernel that reads a buffer and writes almost nothing can reach (a copy benchmark
  * also writes).  buf: device, 16-byte aligned, bytes a nonzero multiple of 16;

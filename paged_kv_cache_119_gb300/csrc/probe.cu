@@ -1,7 +1,7 @@
 // probe.cu -- a streaming read of one device buffer, the read-only bandwidth
 // ceiling the decode kernels are measured against (they read the cache and write
 // almost nothing, so a copy benchmark, which also writes, understates what they can
-// reach).  Every 16-byte vector is loaded once with a streaming load; a checksum
+// reach).  Every 16-byte vector is loaded once through the read-only path; a checksum
 // goes to the caller's sink word so the loads cannot be dropped.
 #include <algorithm>
 
@@ -20,15 +20,20 @@ __global__ void __launch_bounds__(kProbeThreads) stream_read_kernel(const uint4*
 {
     const int64_t stride = (int64_t)gridDim.x * kProbeThreads;
     uint32_t acc = 0;
-    for (int64_t i = (int64_t)blockIdx.x * kProbeThreads + threadIdx.x; i < n;
-         i += kProbeUnroll * stride) {
+    int64_t i = (int64_t)blockIdx.x * kProbeThreads + threadIdx.x;
+    // kProbeUnroll independent 16-byte loads in flight per thread, no per-load branch
+    for (; i + (kProbeUnroll - 1) * stride < n; i += kProbeUnroll * stride) {
         uint4 v[kProbeUnroll];
 #pragma unroll
         for (int u = 0; u < kProbeUnroll; ++u)
-            v[u] = i + u * stride < n ? __ldcs(p + i + u * stride) : make_uint4(0u, 0u, 0u, 0u);
+            v[u] = __ldg(p + i + u * stride);
 #pragma unroll
         for (int u = 0; u < kProbeUnroll; ++u)
             acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+    }
+    for (; i < n; i += stride) {
+        const uint4 v = __ldg(p + i);
+        acc ^= v.x ^ v.y ^ v.z ^ v.w;
     }
     // one atomic per warp
 #pragma unroll
