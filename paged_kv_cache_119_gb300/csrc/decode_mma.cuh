@@ -532,10 +532,10 @@ __global__ void __launch_bounds__(kDecodeThreads, mma_min_blocks<TK, BS>())
                 tmax = fmaxf(tmax, __shfl_xor_sync(kFullMask, tmax, 8));
                 tmax = fmaxf(tmax, __shfl_xor_sync(kFullMask, tmax, 16));
                 const float mnew = fmaxf(m[j], tmax);       // -inf only for padded heads
-                alpha[j] = (mnew == m[j]) ? 1.f : exp2f(m[j] - mnew);   // 1: max unchanged
+                alpha[j] = (mnew == m[j]) ? 1.f : ex2_approx(m[j] - mnew);   // 1: max unchanged
                 m[j] = mnew;
-                const float pa = (mnew == -INFINITY) ? 0.f : exp2f(x[j] - mnew);
-                const float pb = (mnew == -INFINITY) ? 0.f : exp2f(x[j + 2] - mnew);
+                const float pa = (mnew == -INFINITY) ? 0.f : ex2_approx(x[j] - mnew);
+                const float pb = (mnew == -INFINITY) ? 0.f : ex2_approx(x[j + 2] - mnew);
                 x[j] = pa;
                 x[j + 2] = pb;
                 lsum[j] = fmaf(lsum[j], alpha[j], pa + pb);

@@ -52,15 +52,6 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// 2^x on the MUFU unit (relative error about 2^-22; the tensor-core kernels' operand
-// splits are far coarser).
-__device__ __forceinline__ float ex2_approx(float x)
-{
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 // ------------------------------------------------------------------ descriptors
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand (the layout the
 // tensor-map TMA writes with CU_TENSOR_MAP_SWIZZLE_128B: rows of 128 bytes, the
