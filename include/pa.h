@@ -386,6 +386,21 @@ const char* pa_chunk_kernel_name(pa_dtype kv_dtype, int32_t num_q_heads, int32_t
                                  int32_t head_dim, int32_t max_query_len);
 
 /*
+ * Test hook for the bounded pipeline waits; off unless armed, and not for production
+ * use.  Arms a one-shot fault that the calling thread's next pa_decode / pa_decode_fp8
+ * call consumes (whichever kernel it runs; only the CUDA-core decode kernel,
+ * "decode_kernel" in pa_decode_kernel_name, acts on it).  In that call the CTA with
+ * linear block index cta_index (blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y *
+ * blockIdx.z), grid = (partitions, kv heads x head chunks, sequences)) issues no copy of
+ * the cache at all, so nothing is ever in flight for it, and its waits give up after
+ * wait_limit_us microseconds instead of 2 s: the device error word gets
+ * PA_DEVERR_TIMEOUT and that CTA's output rows become NaN, while every other CTA
+ * computes as usual.  No GPU fault, trap or hang is involved.  Returns PA_ERR_INVALID
+ * for cta_index < 0 or wait_limit_us outside [1, 1000000].
+ */
+int pa_test_arm_wait_timeout(int32_t cta_index, uint32_t wait_limit_us);
+
+/*
  * Measurement helper, outside the attention path: reads every byte of buf once with
  * 16-byte loads (8 CTAs of 128 threads per SM) and XORs a checksum into
  * *sink, so that a caller timing it on `stream` learns the read-only bandwidth a

@@ -193,8 +193,19 @@ __global__ void __launch_bounds__(kDecodeThreads)
     }
     __syncthreads();
 
+    // test hook (off unless armed on the host): the chosen CTA's producer issues no copy
+    // at all, so nothing is ever in flight for it, and its consumers' waits give up after
+    // fault_wait_ns; every other CTA runs as usual
+    const bool fault = p.fault_cta > 0 &&
+                       (int64_t)blockIdx.x + (int64_t)gridDim.x *
+                                                 ((int64_t)blockIdx.y + (int64_t)gridDim.y * blockIdx.z) ==
+                           (int64_t)p.fault_cta - 1;
+    const uint64_t wait_limit = fault ? (uint64_t)p.fault_wait_ns : kWaitLimitNs;
+
     if (warp == NCW) {
         // ------------------------------------------------------------------ producer
+        if (fault)
+            return;
         const int32_t* bt_row = p.block_tables + (int64_t)seq * p.bt_stride + jb;
         const TK* kpool = reinterpret_cast<const TK*>(p.k_cache) + (int64_t)kvh * kTile;
         const TK* vpool = reinterpret_cast<const TK*>(p.v_cache) + (int64_t)kvh * kTile;
@@ -269,7 +280,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
 
     for (int it = warp; it < ntiles; it += NCW) {
         const int stage = it % NSTAGE;
-        if (!mbar_wait(&full[stage], (it / NSTAGE) & 1)) {
+        if (!mbar_wait(&full[stage], (it / NSTAGE) & 1, wait_limit)) {
             if (lane == 0)
                 atomicOr(p.err, PA_DEVERR_TIMEOUT);
             poisoned = true;

@@ -388,6 +388,11 @@ ChunkPlan chunk_plan(pa_dtype q_dtype, pa_dtype kv_dtype, int num_seqs, int num_
     return c;
 }
 
+// One-shot wait-timeout test hook armed by pa_test_arm_wait_timeout, consumed by the
+// calling thread's next decode call: (chosen CTA's linear index + 1, wait limit in ns).
+thread_local int g_fault_cta = 0;
+thread_local uint32_t g_fault_wait_ns = 0;
+
 // Shared body of pa_decode and pa_decode_fp8.  q_dtype is the type of q (and of a
 // native out); kv_dtype the cache's, PA_FP8_E4M3 with k_scale / v_scale.
 int decode_impl(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
@@ -400,6 +405,10 @@ int decode_impl(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
                 void* stream)
 {
     const bool fp8 = kv_dtype == PA_FP8_E4M3;
+    const int fault_cta = g_fault_cta;           // the test hook lasts one call
+    const uint32_t fault_wait_ns = g_fault_wait_ns;
+    g_fault_cta = 0;
+    g_fault_wait_ns = 0;
     if (!valid_dtype(q_dtype) || !(out_dtype == PA_F32 || out_dtype == q_dtype))
         return PA_ERR_INVALID;
     if (num_seqs < 0 || num_seqs > 65535 || num_q_heads <= 0 || num_kv_heads <= 0 ||
@@ -463,6 +472,8 @@ int decode_impl(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype,
     p.max_parts = 1;
     p.out_f32 = out_dtype == PA_F32 ? 1 : 0;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);  // log2(e)
+    p.fault_cta = fault_cta;
+    p.fault_wait_ns = fault_wait_ns;
     if (P > 0) {
         p.max_parts = (max_context_len + P - 1) / P;
         size_t ml_off = 0;
@@ -585,6 +596,15 @@ int32_t pa_chunk_partition_tokens(pa_dtype kv_dtype, int32_t num_seqs, int32_t n
                       num_q_heads, num_kv_heads, head_dim, block_size, max_query_len,
                       max_context_len, partition_size)
         .partition;
+}
+
+int pa_test_arm_wait_timeout(int32_t cta_index, uint32_t wait_limit_us)
+{
+    if (cta_index < 0 || cta_index == INT32_MAX || wait_limit_us < 1 || wait_limit_us > 1000000)
+        return PA_ERR_INVALID;
+    g_fault_cta = cta_index + 1;
+    g_fault_wait_ns = wait_limit_us * 1000u;
+    return PA_OK;
 }
 
 const char* pa_decode_kernel_name(pa_dtype kv_dtype, int32_t num_q_heads, int32_t num_kv_heads,

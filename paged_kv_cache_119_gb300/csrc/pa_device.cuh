@@ -85,8 +85,9 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity)
 }
 
 // Waits for the phase with the given parity to complete.  Returns false (and
-// stops waiting) once kWaitLimitNs has passed.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
+// stops waiting) once limit_ns (by default kWaitLimitNs) has passed.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -96,7 +97,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity))
                 return true;
-        if (global_timer_ns() - t0 > kWaitLimitNs)
+        if (global_timer_ns() - t0 > limit_ns)
             return false;
     }
 }

@@ -58,6 +58,10 @@ struct DecodeParams {
     const int32_t* query_start;
     int64_t num_rows;
     int max_query_len;
+    // test hook of the CUDA-core decode (0 = off): CTA (linear block index) fault_cta - 1
+    // issues no copy and waits fault_wait_ns at most, so its bounded waits give up
+    int fault_cta;
+    uint32_t fault_wait_ns;
 };
 
 // Longest-first dispatch of a one-pass CUDA-core decode with more CTAs than one wave:

@@ -279,3 +279,12 @@ def test_swap_blocks_rejects_host_memory_that_is_not_pinned(lib):
     dst = (ctypes.c_void_p * 1)(b.ctypes.data)
     arr = (ctypes.c_int64 * 2)(0, 1)
     assert lib.pa_swap_blocks(src, dst, 1, arr, 1, 64, 4, 6, None) == N.PA_ERR_INVALID
+
+
+def test_wait_timeout_hook_validates_and_lasts_one_call(lib):
+    assert lib.pa_test_arm_wait_timeout(-1, 5000) == N.PA_ERR_INVALID
+    assert lib.pa_test_arm_wait_timeout(0, 0) == N.PA_ERR_INVALID
+    assert lib.pa_test_arm_wait_timeout(0, 1000001) == N.PA_ERR_INVALID
+    assert lib.pa_test_arm_wait_timeout(5, 5000) == N.PA_OK
+    # the next decode call consumes the arm, even one rejected on the host
+    assert lib.pa_decode(*decode_args(D=96)) == N.PA_ERR_UNSUPPORTED
