@@ -107,6 +107,8 @@ def parse_args(argv=None):
     ap.add_argument("--config-steps", type=int, default=10,
                     help="timed steps of each workload in the `configs` object")
     ap.add_argument("--config-warmup", type=int, default=3)
+    ap.add_argument("--eager", action="store_true",
+                    help="time eager steps instead of replays of the captured step graph")
     ap.add_argument("--no-read-probe", action="store_true",
                     help="skip the read-only bandwidth probe reported beside the copy peak")
     return ap.parse_args(argv)
@@ -615,10 +617,14 @@ def workspace_for(pa, w, part, dev):
     return torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
 
 
-def timed_steps(pa, w, steps, warmup, part, dev, flush=None, barrier=None, sampler=None):
+def timed_steps(pa, w, steps, warmup, part, dev, flush=None, barrier=None, sampler=None,
+                graph=True):
     """Runs `warmup` untimed steps, then exactly `steps` timed ones bracketed by CUDA
-    events on the launching stream, with events between the step's kernels.  Returns
-    the total time, per-step times and the buffers the e2e leg reuses."""
+    events on the launching stream.  With `graph`, the step (its kernels, in order) is
+    captured once into a CUDA graph and the timed steps are replays of it, as a serving
+    loop replays its captured step; the per-kernel times then come from `steps` more
+    eager steps with events between the kernels.  Returns the total time, per-step times
+    and the buffers the e2e leg reuses."""
     out = torch.empty(w.q.shape, dtype=w.dtype, device=dev)
     ws = workspace_for(pa, w, part, dev)
     cow_src = None
@@ -643,13 +649,25 @@ def timed_steps(pa, w, steps, warmup, part, dev, flush=None, barrier=None, sampl
         if e is not None:
             e[3].record()
 
-    for _ in range(warmup):
-        step()
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(warmup):
+            step()
+    torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
     if pa.pa_get_device_error():
         raise RuntimeError("device error word set during warm-up")
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
-    begin, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g = None
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        torch.cuda.synchronize()
+        g.replay()                                   # one untimed replay
+        torch.cuda.synchronize()
+    run = g.replay if g is not None else step
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     if sampler is not None:
         sampler.start()
     if barrier is not None:
@@ -657,21 +675,22 @@ def timed_steps(pa, w, steps, warmup, part, dev, flush=None, barrier=None, sampl
     torch.cuda.synchronize()
     t0_wall = time.time()
     if flush is None:
-        begin.record()
         for i in range(steps):
-            step(ev[i])
-        end.record()
+            marks[i].record()
+            run()
+        marks[steps].record()
         torch.cuda.synchronize()
-        total_ms = begin.elapsed_time(end)
+        step_ms = [marks[i].elapsed_time(marks[i + 1]) for i in range(steps)]
     else:
-        total_ms = 0.0
+        end = torch.cuda.Event(enable_timing=True)
+        step_ms = []
         for i in range(steps):
             flush.fill_(i & 0xff)
-            begin.record()
-            step(ev[i])
+            marks[i].record()
+            run()
             end.record()
             torch.cuda.synchronize()
-            total_ms += begin.elapsed_time(end)
+            step_ms.append(marks[i].elapsed_time(end))
     if barrier is not None:
         barrier()
     t1_wall = time.time()
@@ -679,11 +698,18 @@ def timed_steps(pa, w, steps, warmup, part, dev, flush=None, barrier=None, sampl
     torch.cuda.synchronize()
     if pa.pa_get_device_error():
         raise RuntimeError("device error word set during the timed steps")
-    return {"total_ms": total_ms,
-            "step_ms": [e[0].elapsed_time(e[3]) for e in ev],
+    # per-kernel times: eager steps with events between the kernels
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for i in range(steps):
+        step(ev[i])
+    torch.cuda.synchronize()
+    if pa.pa_get_device_error():
+        raise RuntimeError("device error word set during the per-kernel steps")
+    return {"total_ms": sum(step_ms), "step_ms": step_ms, "graph": g is not None,
             "copy_ms": [e[0].elapsed_time(e[1]) for e in ev],
             "reshape_ms": [e[1].elapsed_time(e[2]) for e in ev],
             "decode_ms": [e[2].elapsed_time(e[3]) for e in ev],
+            "eager_step_ms": [e[0].elapsed_time(e[3]) for e in ev],
             "clocks": clocks, "out": out, "ws": ws, "copies": cow_src is not None}
 
 
@@ -729,14 +755,14 @@ def attention_summary(pa, w, config, part, t) -> dict:
             "bytes": nbytes, "decode_ms_mean": decode_ms}
 
 
-def config_row(pa, config, dev, steps, warmup, local) -> dict:
+def config_row(pa, config, dev, steps, warmup, local, graph=True) -> dict:
     """One workload's throughput for the bench line's `configs` object: a short run of
     its step with its own clock sample."""
     if config == "llama13b_swap":
         return swap_row(pa, dev, steps, warmup, local)
     w = make_workload(config, dev)
     sampler = ClockSampler(local)
-    t = timed_steps(pa, w, steps, warmup, 0, dev, sampler=sampler)
+    t = timed_steps(pa, w, steps, warmup, 0, dev, sampler=sampler, graph=graph)
     a = attention_summary(pa, w, config, 0, t)
     r = a["roofline"]
     dec, stp = percentiles(t["decode_ms"]), percentiles(t["step_ms"])
@@ -747,6 +773,7 @@ def config_row(pa, config, dev, steps, warmup, local) -> dict:
            "decode_us_p90": round(dec["p90"] * 1e3, 2),
            "step_us_p50": round(stp["p50"] * 1e3, 2),
            "step_us_mean": round(t["total_ms"] / steps * 1e3, 2),
+           "eager_step_us_p50": round(percentiles(t["eager_step_ms"])["p50"] * 1e3, 2),
            "steps": steps, "warmup": warmup, "clocks": t["clocks"]}
     if r["bound"] == "hbm":
         row["frac_of_nominal"] = r["frac_of_nominal"]
@@ -774,7 +801,7 @@ def run_ours(args, rank, world, local):
     sampler = ClockSampler(local) if rank == 0 else None
     barrier = torch.distributed.barrier if world > 1 else None
     t = timed_steps(pa, w, args.steps, args.warmup, part, dev, flush=flush, barrier=barrier,
-                    sampler=sampler)
+                    sampler=sampler, graph=not args.eager)
     total_ms = t["total_ms"]
     sec = max_over_ranks(total_ms / 1e3, dev) if world > 1 else total_ms / 1e3
     a = attention_summary(pa, w, args.config, part, t)
@@ -820,6 +847,9 @@ def run_ours(args, rank, world, local):
         "reshape_us": round(sum(t["reshape_ms"]) / args.steps * 1e3, 2),
         "step_us_p10": round(stp["p10"] * 1e3, 2), "step_us_p50": round(stp["p50"] * 1e3, 2),
         "step_us_p90": round(stp["p90"] * 1e3, 2),
+        "timing": ("replays of the step captured in a CUDA graph; per-kernel times from as "
+                   "many eager steps" if t["graph"] else "eager steps"),
+        "eager_step_us_p50": round(percentiles(t["eager_step_ms"])["p50"] * 1e3, 2),
         "decode_us_p10": round(dec["p10"] * 1e3, 2),
         "decode_us_p50": round(dec["p50"] * 1e3, 2),
         "decode_us_p90": round(dec["p90"] * 1e3, 2),
@@ -839,7 +869,8 @@ def run_ours(args, rank, world, local):
     if not args.no_configs and args.num_seqs is None and world == 1:
         del t
         torch.cuda.empty_cache()
-        line["configs"] = {c: config_row(pa, c, dev, args.config_steps, args.config_warmup, local)
+        line["configs"] = {c: config_row(pa, c, dev, args.config_steps, args.config_warmup, local,
+                                         graph=not args.eager)
                            for c in CONFIG_ROWS if c != args.config}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
