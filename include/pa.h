@@ -78,6 +78,9 @@ typedef enum {
 #define PA_DEVERR_CONTEXT_LEN 0x2u  /* context_len < 0 or > max_context_len */
 #define PA_DEVERR_SLOT        0x4u  /* slot_mapping entry >= num_blocks * block_size */
 #define PA_DEVERR_TIMEOUT     0x8u  /* a bounded pipeline wait gave up */
+#define PA_DEVERR_RANGE       0x10u /* chunk attention over a bf16 cache: a row weighed a V
+                                           element without an f16 value (|v| >= 65536,
+                                           infinite or NaN) */
 
 /*
  * Bytes of device workspace a pa_decode call with these sizes uses: when it splits
@@ -297,16 +300,21 @@ int pa_decode_fp8(void* out, pa_dtype out_dtype, const void* q, pa_dtype q_dtype
  *                    must not overlap out, q, the caches, block_tables,
  *                    context_lens or query_start (PA_ERR_INVALID)
  * Supported: head_dim 64 / 128, block_size 16 / 32, num_q_heads / num_kv_heads <= 128.
- * Accumulation is fp32 on the tensor cores; probabilities enter the P.V product as
- * hi + lo halves of the 16-bit type, so they keep fp32-level accuracy.  A kv head with
- * at most 32 (token, head) rows (max_query_len * num_q_heads / num_kv_heads: e.g.
- * verifying a few speculated tokens) runs on the memory-bound decode kernel in a
- * multi-row mode; longer chunks run on the tcgen05 kernel (256 rows per CTA).
+ * Accumulation is fp32 on the tensor cores.  A kv head with at most 32 (token, head)
+ * rows (max_query_len * num_q_heads / num_kv_heads: e.g. verifying a few speculated
+ * tokens) runs on the memory-bound decode kernel in a multi-row mode, where the
+ * probabilities enter P.V as hi + lo halves of the 16-bit type (fp32-level accuracy).
+ * Longer chunks run on the tcgen05 kernel (256 rows per CTA), where they enter as one
+ * f16 term (11 significant bits): the output is then off by at most 2^-11 of the
+ * largest |v| the row weighs, plus fp32 rounding.  That kernel multiplies P with V in
+ * f16, so over a bf16 cache it converts each V tile to f16 in shared memory; a V
+ * element of the context with |v| >= 65536, infinite or NaN, has no f16 value: the
+ * rows that weigh it come out infinite or NaN and set PA_DEVERR_RANGE.
  * Errors: invalid arguments return a negative pa_status with nothing launched.  On
  * the device, n_s > L_s, L_s > max_context_len, n_s > max_query_len or rows beyond
  * query_start[num_seqs] set PA_DEVERR_CONTEXT_LEN (the offending sequence's rows
  * become NaN; rows that no sequence owns are left unwritten); a block id outside the
- * pool sets PA_DEVERR_BLOCK_ID.
+ * pool sets PA_DEVERR_BLOCK_ID; see above for PA_DEVERR_RANGE.
  */
 size_t pa_chunk_workspace_bytes(int64_t num_query_tokens, int32_t num_q_heads, int32_t head_dim,
                                 int32_t max_context_len, int32_t partition_size);

@@ -14,6 +14,7 @@ _lib = None
 PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2, 3
 PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0, -1, -2, -3, -4
 PA_DEVERR_BLOCK_ID, PA_DEVERR_CONTEXT_LEN, PA_DEVERR_SLOT, PA_DEVERR_TIMEOUT = 1, 2, 4, 8
+PA_DEVERR_RANGE = 0x10
 PA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 # Every symbol include/pa.h and include/pa_block_manager.h declare, with (restype, argtypes).

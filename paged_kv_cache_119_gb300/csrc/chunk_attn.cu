@@ -8,11 +8,13 @@
 namespace pa {
 
 // F8: E4M3 caches (head_dim 128): three 16-bit stages and four raw one-byte stages.
+// E4M3 and bf16 caches add the four converter warps.
 template <typename T, int D, int BS, bool F8 = false>
 struct ChunkVariant {
     static constexpr int kStages = F8 ? 3 : ChunkStages<D>::value;
     static constexpr int kRaw = F8 ? 4 : 0;
-    static constexpr int kThreads = F8 ? kChunkThreadsF8 : kChunkThreads;
+    static constexpr int kThreads =
+        (F8 || std::is_same_v<T, __nv_bfloat16>) ? kChunkThreadsConv : kChunkThreads;
     using Sm = ChunkSmem<D, kStages, kRaw>;
     static constexpr auto kernel() { return chunk_attn_kernel<T, D, BS, kStages, kRaw>; }
     static cudaError_t configure()

@@ -14,8 +14,8 @@
 // r = token * G + head -- as two 128-row query tiles.  K and V stream through the
 // block table in tiles of 64 tokens, each tile serving both query tiles:
 //   S_q[128 x 64]  = Q_q[128 x D] . K^T      (tcgen05.mma kind::f16, fp32 in TMEM)
-//   O_q[128 x D]  += P_q[128 x 64] . V        (P = hi + lo halves of the 16-bit type,
-//                                              A operand read from tensor memory)
+//   O_q[128 x D]  += P_q[128 x 64] . V        (P in f16, A operand read from tensor
+//                                              memory; V in f16)
 //   * warp 0 (producer): block-table entries and tensor-map TMA of the tile's K
 //     and V boxes (64 dims x B tokens, 128-byte swizzle) into an mbarrier ring;
 //   * warps 1 and 10: one thread each issues the MMAs of one query tile (warp 1 also
@@ -25,8 +25,9 @@
 //     other while one waits;
 //   * warps 2-5 (query tile 0) and 6-9 (query tile 1), one thread per row = TMEM
 //     lane: read S, mask (causal within the chunk, end of context), online softmax
-//     in base 2, write P back over the S buffer it came from (packed 16-bit pairs),
-//     keep O up to date.
+//     in base 2, write P back over the S buffer it came from (packed f16 pairs),
+//     keep O up to date;
+//   * over bf16 caches, warps 11-14 rewrite each V tile in place as f16 (below).
 // The S/P buffers alternate between tiles, so the softmax of tile i+1 never waits
 // for P.V of tile i; the scores of tile i+2 reuse a buffer only once P.V of tile i
 // has read it.
@@ -36,10 +37,18 @@
 // exceeds it by more than 2^8 in probability, so p = 2^(x - m_ref) <= 256 and most
 // tiles need no tensor-memory round trip.  O / l is exact for any reference, as O
 // and l share it.
-// P is split into hi = rn(p) and lo = rn(p - hi) of the 16-bit operand type
-// (p = hi + lo to ~2^-17 relative) and both halves are multiplied with V, so the
-// probabilities keep fp32-level accuracy (one 8-bit-mantissa rounding of p would
-// cost up to 2^-9 relative per weight).
+// P enters P.V as one f16 term, 2^7 p (at most 2^15, and normal down to p = 2^-21),
+// rounded to nearest: up to 2^-11 relative per weight, so the output is off by at
+// most 2^-11 of the largest |v| the row weighs (fp32 accumulation), a quarter of the
+// bf16 output's own rounding step; one bf16 rounding of p would cost 2^-9, and a
+// second (lo) term would cost as much tensor and softmax work again.  The 2^7 is
+// carried by the exponent (p = 2^(x - m_ref + 7)) and cancels against the row sum.
+// So V must be f16 too: f16 caches are, E4M3 caches convert to f16 anyway, and over
+// bf16 caches four converter warps rewrite each V tile in place (same swizzled
+// layout, bf16 -> f16 is exact for 2^-14 <= |v| <= 65280) and zero its rows past the
+// range.  A value without an f16 value (|v| >= 65536, infinite or NaN) becomes
+// infinite or NaN; the epilogue sets PA_DEVERR_RANGE for a row whose probabilities are
+// finite but whose O is not.  K stays bf16 (the score product is bf16 x bf16).
 // Long contexts with few CTAs are split into partitions merged by
 // chunk_reduce_kernel, as in the decode path.
 // The epilogue reads O once its issuer's one-phase completion barrier has fired (P.V of
@@ -69,10 +78,13 @@ constexpr int kChunkRows = 128;      // M of the tensor-core tile
 constexpr int kChunkTileTok = 64;    // tokens per K/V tile (N of the score product)
 constexpr int kChunkSoftmaxWarps = 4 * kChunkQTiles;
 // warps: 0 producer, 1 tensor-memory allocator + MMA issuer of query tile 0, 2-9
-// softmax, 10 MMA issuer of query tile 1; over E4M3 caches, 11-14 convert tiles to f16
+// softmax, 10 MMA issuer of query tile 1; over E4M3 and bf16 caches, 11-14 convert
+// tiles to f16
 constexpr int kChunkThreads = 64 + 32 * kChunkSoftmaxWarps + 32;
 constexpr int kChunkConvWarps = 4;
-constexpr int kChunkThreadsF8 = kChunkThreads + 32 * kChunkConvWarps;
+constexpr int kChunkThreadsConv = kChunkThreads + 32 * kChunkConvWarps;
+// P.V takes P as 2^kChunkPExp p: p <= 2^8 (the lazy rescale), so 2^15 at most in f16
+constexpr float kChunkPExp = 7.f;
 
 // NRAW > 0 (E4M3 caches): a ring of NRAW raw one-byte K + V tiles that the converter
 // warps turn into the 16-bit tiles of the NST-stage ring.
@@ -91,14 +103,14 @@ struct ChunkSmem {
     static constexpr int kRawOff = kStageOff + NST * kStageBytes;
     static constexpr int kBarOff = kRawOff + NRAW * kRawStage;
     // full[NST], empty[NST], s_full[2][2], p_full[2][2], pv_done[2], q_full, mma_done[2],
-    // v_zero, raw_full[NRAW], raw_empty[NRAW]
-    static constexpr int kNumBars = 2 * NST + 14 + 2 * NRAW;
+    // v_zero, raw_full[NRAW], raw_empty[NRAW], vconv[NST]
+    static constexpr int kNumBars = 3 * NST + 14 + 2 * NRAW;
     static constexpr int kOkOff = kBarOff + 8 * kNumBars;        // stage_ok[NST], raw_ok[NRAW]
     static constexpr int kSlotOff = kOkOff + 4 * (NST + NRAW);   // TMEM address
     static constexpr int kBytes = kSlotOff + 16;
     static constexpr int kAlloc = kBytes + 1024;                 // 1 KB alignment slack
     // tensor memory: O of query tile q at column 128 q, its two S/P buffers at
-    // 256 + 128 q and 256 + 128 q + 64 (P: hi in the first 32 columns, lo in the next)
+    // 256 + 128 q and 256 + 128 q + 64 (P: f16 pairs in the first 32 columns)
     static constexpr int kTmemCols = 512;
     static constexpr int kSCol = 256;
     static_assert(D <= 128, "O must fit in 128 columns");
@@ -147,43 +159,31 @@ __device__ __forceinline__ void store_row32(void* base, int64_t idx, const float
         dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
 }
 
-// (p0, p1) -> hi = rn(p0, p1) and lo = rn(p - hi) in the 16-bit type T, packed.
-template <typename T>
-__device__ __forceinline__ void split_pair(float p0, float p1, uint32_t& hi, uint32_t& lo)
+// max(a, b, c) in one instruction (NaN operands are ignored, as by fmaxf).
+__device__ __forceinline__ float max3f(float a, float b, float c)
 {
-    float2 h;
-    if constexpr (DType<T>::id == PA_F16) {
-        __half2 v = __floats2half2_rn(p0, p1);
-        hi = *reinterpret_cast<uint32_t*>(&v);
-        h = __half22float2(v);
-    } else {
-        __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
-        hi = *reinterpret_cast<uint32_t*>(&v);
-        h = make_float2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u));
-    }
-    const float2 r = ffma2(h, make_float2(-1.f, -1.f), make_float2(p0, p1));   // p - hi, exact
-    if constexpr (DType<T>::id == PA_F16) {
-        __half2 v = __floats2half2_rn(r.x, r.y);
-        lo = *reinterpret_cast<uint32_t*>(&v);
-    } else {
-        __nv_bfloat162 v = __floats2bfloat162_rn(r.x, r.y);
-        lo = *reinterpret_cast<uint32_t*>(&v);
-    }
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
 }
 
-// grid = (partitions, num_kv_heads * m_tiles, num_seqs); kChunkThreads threads, or
-// kChunkThreadsF8 over E4M3 caches (NRAW > 0).  T: query / native output type.  Over
-// E4M3 caches (value = code * per-kv-head scale) the tensor-core operands are f16: the
-// codes convert exactly, a bf16 query row is scaled into f16 range by a power of two
-// (exact), and the scales fold into the scores and the output.
+// grid = (partitions, num_kv_heads * m_tiles, num_seqs); kChunkThreads threads over
+// f16 caches, kChunkThreadsConv over E4M3 (NRAW > 0) and bf16 caches.  T: query /
+// native output type.  Over E4M3 caches (value = code * per-kv-head scale) the
+// tensor-core operands are f16: the codes convert exactly, a bf16 query row is scaled
+// into f16 range by a power of two (exact), and the scales fold into the scores and
+// the output.
 template <typename T, int D, int BS, int NST, int NRAW = 0>
-__global__ void __launch_bounds__(NRAW > 0 ? kChunkThreadsF8 : kChunkThreads, 1)
+__global__ void __launch_bounds__((NRAW > 0 || std::is_same_v<T, __nv_bfloat16>) ? kChunkThreadsConv
+                                                                                 : kChunkThreads,
+                                  1)
     chunk_attn_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv)
 {
     using Sm = ChunkSmem<D, NST, NRAW>;
     constexpr bool kF8 = NRAW > 0;
-    using TM = std::conditional_t<kF8, __half, T>;   // tensor-core operand type
+    constexpr bool kVConv = !kF8 && std::is_same_v<T, __nv_bfloat16>;   // bf16 V -> f16 in place
+    using TM = std::conditional_t<kF8, __half, T>;   // operand type of the score product
     constexpr int NT = kChunkTileTok;
     constexpr int BPT = NT / BS;                 // cache blocks per K/V tile
     constexpr int KS = D / 16;                   // k-steps of the score product
@@ -203,6 +203,7 @@ __global__ void __launch_bounds__(NRAW > 0 ? kChunkThreadsF8 : kChunkThreads, 1)
     uint64_t* v_zero = mma_done + 2;             // the last tile's V rows past the range are 0
     uint64_t* raw_full = v_zero + 1;             // [raw slot] (E4M3 caches)
     uint64_t* raw_empty = raw_full + NRAW;
+    uint64_t* vconv = raw_empty + NRAW;          // [stage] (bf16 caches: V tile is f16)
     int* stage_ok = reinterpret_cast<int*>(smem + Sm::kOkOff);
     int* raw_ok = stage_ok + NST;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Sm::kSlotOff);
@@ -269,6 +270,9 @@ __global__ void __launch_bounds__(NRAW > 0 ? kChunkThreadsF8 : kChunkThreads, 1)
             mbar_init(&raw_full[s], 1);
             mbar_init(&raw_empty[s], kChunkConvWarps);
         }
+#pragma unroll
+        for (int s = 0; s < NST; ++s)
+            mbar_init(&vconv[s], kChunkConvWarps);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             mbar_init(&s_full[i], 1);
@@ -357,7 +361,7 @@ __global__ void __launch_bounds__(NRAW > 0 ? kChunkThreadsF8 : kChunkThreads, 1)
             for (int it = max(0, issued - NP); it < issued; ++it)
                 mbar_wait(&pfull[it % NP], (it / NP) & 1);
         __syncwarp();
-    } else if (kF8 && warp > 2 + kChunkSoftmaxWarps) {
+    } else if ((kF8 || kVConv) && warp > 2 + kChunkSoftmaxWarps) {
         // ------------------------------------------------ E4M3 -> f16 tile conversion
         // A raw tile row is 128 codes in 128-byte-swizzled order (16-byte chunk c of row
         // t at c ^ (t & 7)); the f16 tile is two 64-dim halves of 128-byte rows in the
@@ -406,6 +410,52 @@ __global__ void __launch_bounds__(NRAW > 0 ? kChunkThreadsF8 : kChunkThreads, 1)
                     mbar_arrive(&raw_empty[r]);
                 }
             }
+        } else if constexpr (kVConv) {
+            // bf16 -> f16 of each V tile in place, once its bytes are in (the K half is
+            // left to the score product meanwhile); rows past the range become 0, so
+            // that 0 * V stays 0 whatever an unused slot holds.  The stage is refilled
+            // only after both P.V of the tile, which wait for this hand-over.  A value
+            // without an f16 value becomes infinite (or stays NaN); the epilogue reports
+            // the rows it reaches.
+            const int ct = threadIdx.x - kChunkThreads;      // 0 .. 32 * kChunkConvWarps - 1
+            constexpr int kItems = NT * 8 * Sm::kHalves;     // 16-byte chunks of a V tile
+            constexpr int kPer = kItems / (32 * kChunkConvWarps);
+            static_assert(kItems % (32 * kChunkConvWarps) == 0, "whole chunks per thread");
+            for (int it = 0; it < ntiles; ++it) {
+                const int st = it % NST;
+                if (!mbar_wait(&full[st], (it / NST) & 1)) {
+                    if (lane == 0)
+                        atomicOr(p.err, PA_DEVERR_TIMEOUT);
+                    break;
+                }
+                const int nv = min(NT, t1 - (t0 + it * NT));  // rows inside the range
+                unsigned char* vt = smem + Sm::kStageOff + st * Sm::kStageBytes + Sm::kKBytes;
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) {
+                    const int item = ct + i * 32 * kChunkConvWarps;
+                    const int w = item % (NT * 8);           // chunk within a 64-dim half
+                    uint4* chunk = reinterpret_cast<uint4*>(vt + (item / (NT * 8)) * Sm::kKVHalf +
+                                                            w * 16);
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if ((w >> 3) < nv) {
+                        const uint4 b = *chunk;
+                        const uint32_t in[4] = {b.x, b.y, b.z, b.w};
+                        uint32_t o[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const __half2 h = __floats2half2_rn(__uint_as_float(in[j] << 16),
+                                                                __uint_as_float(in[j] & 0xffff0000u));
+                            o[j] = *reinterpret_cast<const uint32_t*>(&h);
+                        }
+                        v = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                    *chunk = v;
+                }
+                fence_proxy_async_smem();                    // f16 V -> tensor core
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&vconv[st]);
+            }
         }
     } else if (warp == 1 || warp == 2 + kChunkSoftmaxWarps) {
         // ------------------------------------------- MMA issue, one query tile per warp
@@ -413,7 +463,7 @@ __global__ void __launch_bounds__(NRAW > 0 ? kChunkThreadsF8 : kChunkThreads, 1)
         if (lane == 0) {
             const uint32_t sq = smem_addr(smem + Sm::kQOff + q * Sm::kQTile);
             const uint32_t idesc_s = mma_idesc_f16(kBf16, kChunkRows, NT, false);
-            const uint32_t idesc_o = mma_idesc_f16(kBf16, kChunkRows, D, true);
+            const uint32_t idesc_o = mma_idesc_f16(false, kChunkRows, D, true);   // f16 P, V
             bool ok = mbar_wait(q_full, 0);
             // S of tile it into this query tile's S buffer it & 1
             auto issue_scores = [&](int it) {
@@ -446,8 +496,13 @@ __global__ void __launch_bounds__(NRAW > 0 ? kChunkThreadsF8 : kChunkThreads, 1)
                     issue_scores(it + 1);
                 }
                 ok = mbar_wait(&p_full[q * 2 + (it & 1)], (it >> 1) & 1);
-                if (ok && t0 + (it + 1) * NT > t1)
-                    ok = mbar_wait(v_zero, 0);       // last tile: V rows past the range zeroed
+                if constexpr (kVConv) {
+                    if (ok)                           // V in f16, rows past the range zeroed
+                        ok = mbar_wait(&vconv[it % NST], (it / NST) & 1);
+                } else {
+                    if (ok && t0 + (it + 1) * NT > t1)
+                        ok = mbar_wait(v_zero, 0);   // last tile: V rows past the range zeroed
+                }
                 if (!ok)
                     break;
                 tc_fence_after();
@@ -455,13 +510,11 @@ __global__ void __launch_bounds__(NRAW > 0 ? kChunkThreadsF8 : kChunkThreads, 1)
                     smem_addr(smem + Sm::kStageOff + (it % NST) * Sm::kStageBytes + Sm::kKBytes);
                 const uint32_t pcol = tbase + Sm::kSCol + q * 128 + (it & 1) * NT;
 #pragma unroll
-                for (int half = 0; half < 2; ++half)          // hi, then lo
-#pragma unroll
-                    for (int kk = 0; kk < NT / 16; ++kk) {
-                        const uint64_t b = sw128_desc(vb + kk * 16 * 128, Sm::kKVHalf, 1024);
-                        tc_mma_f16_ts(tbase + q * 128, pcol + half * (NT / 2) + kk * 8, b, idesc_o,
-                                      (it > 0 || half > 0 || kk > 0) ? 1u : 0u);
-                    }
+                for (int kk = 0; kk < NT / 16; ++kk) {        // 16 tokens = 8 columns of P
+                    const uint64_t b = sw128_desc(vb + kk * 16 * 128, Sm::kKVHalf, 1024);
+                    tc_mma_f16_ts(tbase + q * 128, pcol + kk * 8, b, idesc_o,
+                                  (it > 0 || kk > 0) ? 1u : 0u);
+                }
                 tc_commit(&pv_done[q]);
                 tc_commit(&empty[it % NST]);
             }
@@ -583,10 +636,15 @@ __global__ void __launch_bounds__(NRAW > 0 ? kChunkThreadsF8 : kChunkThreads, 1)
                 for (int i = 0; i < 8; ++i)
                     mx[i] = s[i];
 #pragma unroll
-                for (int c = 8; c < NT; ++c)
+                for (int c = 8; c + 16 <= NT; c += 16)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        mx[i] = max3f(mx[i], s[c + i], s[c + 8 + i]);
+#pragma unroll
+                for (int c = 8 + (NT - 8) / 16 * 16; c < NT; ++c)
                     mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-                const float smax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                const float smax = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]),
+                                         fmaxf(mx[6], mx[7]));
                 const float tmax = smax == -INFINITY ? -INFINITY : smax * sl2;
                 const bool need = tmax > m_ref + 8.f;
                 if (it > 0 && __any_sync(kFullMask, need)) {
@@ -616,8 +674,9 @@ __global__ void __launch_bounds__(NRAW > 0 ? kChunkThreadsF8 : kChunkThreads, 1)
                     lsum *= ex2_approx(m_ref - tmax);
                     m_ref = tmax;
                 }
-                // p = 2^(s * sl2 - m_ref), in place; 0 where masked (s = -inf) or no reference
-                const float nm = m_ref == -INFINITY ? 0.f : -m_ref;
+                // 2^7 p = 2^(s * sl2 - m_ref + 7), in place; 0 where masked (s = -inf) or no
+                // reference; the row sum carries the same 2^7
+                const float nm = (m_ref == -INFINITY ? 0.f : -m_ref) + kChunkPExp;
                 float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                  make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
@@ -633,15 +692,16 @@ __global__ void __launch_bounds__(NRAW > 0 ? kChunkThreadsF8 : kChunkThreads, 1)
                         ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
             }
             if (warp_live) {
-                // P over the S buffer: hi in its first 32 columns, lo in the next 32,
-                // written by one 64-column store (one wait)
-                uint32_t hl[NT];
+                // P over the first 32 columns of the S buffer, as f16 pairs
+                uint32_t ph[NT / 2];
 #pragma unroll
-                for (int k = 0; k < NT / 2; ++k)
-                    split_pair<TM>(s[2 * k], s[2 * k + 1], hl[k], hl[NT / 2 + k]);
-                tmem_st64_raw(sp_col, hl);
+                for (int k = 0; k < NT / 2; ++k) {
+                    const __half2 h = __floats2half2_rn(s[2 * k], s[2 * k + 1]);
+                    ph[k] = *reinterpret_cast<const uint32_t*>(&h);
+                }
+                tmem_st32_raw(sp_col, ph);
             }
-            if (tb + NT > t1) {
+            if (!kVConv && tb + NT > t1) {
                 // V rows past the range may hold anything (unused slots, stale tiles):
                 // zero them so that 0 * V stays 0; both issuers wait for v_zero before
                 // their last P.V
@@ -680,12 +740,21 @@ __global__ void __launch_bounds__(NRAW > 0 ? kChunkThreadsF8 : kChunkThreads, 1)
             // over E4M3 caches the V scale of the kv head multiplies the output
             const float inv = lsum > 0.f ? (kF8 ? p.v_scale[kvh] : 1.f) / lsum : 0.f;
             const int which = (split || p.out_f32) ? 0 : (DType<T>::id == PA_F16 ? 1 : 2);
+            // over a bf16 cache, O that is not finite while the probabilities and their
+            // sum are means the row weighed a V element without an f16 value (O itself
+            // cannot overflow: |O| <= l max|v|, far inside fp32)
+            const bool watch = kVConv && row_valid && !poisoned && lsum > 0.f && lsum < INFINITY;
+            bool unconvertible = false;
 #pragma unroll 1
             for (int c4 = 0; c4 < D / 32; ++c4) {
                 float o[32];
                 tmem_ld32(o_col + 32 * c4, o);
                 if (!row_valid)
                     continue;
+                if (watch)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        unconvertible |= !(fabsf(o[i]) < INFINITY);
                 if (split) {
                     const int64_t prw = qrow * p.max_parts + part;
                     store_row32(p.part_o, prw * D + 32 * c4, o, inv, poisoned, 0);
@@ -697,6 +766,8 @@ __global__ void __launch_bounds__(NRAW > 0 ? kChunkThreadsF8 : kChunkThreads, 1)
                     store_row32(p.out, qrow * D + 32 * c4, o, inv, poisoned, which);
                 }
             }
+            if (kVConv && __any_sync(kFullMask, unconvertible) && lane == 0)
+                atomicOr(p.err, PA_DEVERR_RANGE);
         }
         tc_fence_before();
     }

@@ -5,7 +5,9 @@ Each case runs the step as a caller would: pa_reshape_and_cache writes the chunk
 K/V rows (bit-exact against the oracle's byte copy), then pa_chunk_attention; the
 attention output is compared element by element with the oracle's fp64 result
 (max abs error <= 2e-3 on fp32 output; native output must be the round-to-nearest-
-even of a value within 5e-5 of the oracle).  Head groupings 1, 4, 5 and 8, head_dim
+even of a value within 5e-5 of the oracle on the decode kernels' multi-row mode, whose
+probabilities carry fp32-level accuracy, and within 2e-3 on the tcgen05 chunk kernel,
+whose probabilities are one f16 term).  Head groupings 1, 4, 5 and 8, head_dim
 64 / 128, block_size 16 / 32, fp16 / bf16, ragged chunks (n = L, n = 1, n = 0),
 forced and automatic context splits.
 """
@@ -26,6 +28,15 @@ if not torch.cuda.is_available():
 
 ATOL = 2e-3
 NATIVE_EPS = 5e-5
+
+
+def native_eps(w):
+    """Half-width of the native-output bracket: the attention tolerance on the tcgen05
+    chunk kernel (one f16 rounding of each probability: up to 2^-11 of max |v|), 5e-5
+    where the probabilities enter P.V as hi + lo halves."""
+    name = P.pa_chunk_kernel_name(w.k_cache.dtype, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                  w.max_query_len)
+    return ATOL if name.startswith("chunk_attn_kernel") else NATIVE_EPS
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -72,8 +83,9 @@ def run_and_compare(w, out_dtype=torch.float32, partition_size=0, check_caches=T
         err = np.abs(got - ref).max() if got.size else 0.0
         assert err <= ATOL, f"max abs error {err:.3e}"
     else:
-        lo = torch.from_numpy((ref - NATIVE_EPS).astype(np.float32)).to(out_dtype).double().numpy()
-        hi = torch.from_numpy((ref + NATIVE_EPS).astype(np.float32)).to(out_dtype).double().numpy()
+        eps = native_eps(w)
+        lo = torch.from_numpy((ref - eps).astype(np.float32)).to(out_dtype).double().numpy()
+        hi = torch.from_numpy((ref + eps).astype(np.float32)).to(out_dtype).double().numpy()
         bad = (got < lo) | (got > hi)
         assert not bad.any(), f"{bad.sum()} outputs outside the rounding bracket"
     assert P.pa_get_device_error() == 0
@@ -295,8 +307,9 @@ def run_and_compare_fp8(w, out_dtype=torch.float32, partition_size=0):
         err = np.abs(got - ref).max()
         assert err <= ATOL, f"max abs error {err:.3e}"
     else:
-        lo = torch.from_numpy((ref - NATIVE_EPS).astype(np.float32)).to(out_dtype).double().numpy()
-        hi = torch.from_numpy((ref + NATIVE_EPS).astype(np.float32)).to(out_dtype).double().numpy()
+        eps = native_eps(w)
+        lo = torch.from_numpy((ref - eps).astype(np.float32)).to(out_dtype).double().numpy()
+        hi = torch.from_numpy((ref + eps).astype(np.float32)).to(out_dtype).double().numpy()
         assert not ((got < lo) | (got > hi)).any()
     assert P.pa_get_device_error() == 0
 
@@ -461,3 +474,68 @@ def test_rows_beyond_the_last_chunk_are_flagged(fp8, Hq, Hkv, nmax):
                                  v_scale=None if vs is None else vs.cpu())
     err = np.abs(out[:R].double().cpu().numpy() - ref).max()
     assert err <= ATOL, err
+
+
+# ------------------- the tcgen05 chunk kernel: one f16 rounding of each probability
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_tensor_core_probabilities_within_their_f16_bound(dtype):
+    """Values four times larger (peaked rows, |v| up to about 20) on the tcgen05 chunk
+    kernel: each probability enters P.V as one f16 rounding (2^-11 relative), so the
+    output is within 2^-11 of the largest |v| of the cache, plus fp32 rounding."""
+    w = make_case(59, 3, 32, 8, 128, 16, dtype, [900, 2100, 130], [100, 64, 40], std=4.0)
+    assert P.pa_chunk_kernel_name(w.k_cache.dtype, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                  w.max_query_len).startswith("chunk_attn_kernel")
+    P.pa_reshape_and_cache(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping)
+    out = torch.empty(w.q.shape, dtype=torch.float32, device="cuda")
+    P.pa_chunk_attention(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                         w.query_start, w.scale, w.num_kv_heads, w.block_size,
+                         max_query_len=w.max_query_len, max_context_len=w.max_context_len)
+    torch.cuda.synchronize()
+    assert P.pa_get_device_error() == 0
+    ref = oracle.chunk_attention(w.q.cpu(), w.k_cache.cpu(), w.v_cache.cpu(),
+                                 w.block_tables.cpu(), w.context_lens.cpu(), w.query_start.cpu(),
+                                 w.scale, w.num_kv_heads, w.block_size,
+                                 num_threads=oracle.max_threads())
+    vmax = torch.nan_to_num(w.v_cache.float(), nan=0.0).abs().max().item()   # unused slots: NaN
+    err = np.abs(out.double().cpu().numpy() - ref).max()
+    assert err <= 2.0 ** -11 * vmax + 1e-4, (err, vmax)
+
+
+def test_bf16_value_outside_f16_range_is_flagged():
+    """The tcgen05 chunk kernel multiplies P with V in f16, so over a bf16 cache a
+    context value with |v| >= 65536 has no f16 value: the rows that weigh it are not
+    finite and set PA_DEVERR_RANGE; every other row is the oracle's.  The largest bf16
+    value below that (65280) converts exactly and sets nothing."""
+    from paged_kv_cache_119_gb300 import _native as N
+    for value, flagged in ((65280.0, False), (1.0e5, True)):
+        w = make_case(61, 2, 32, 8, 128, 16, torch.bfloat16, [300, 200], [100, 50])
+        assert P.pa_chunk_kernel_name(w.k_cache.dtype, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                      w.max_query_len).startswith("chunk_attn_kernel")
+        P.pa_reshape_and_cache(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping)
+        kvh = 3
+        w.v_cache[int(w.block_tables[0, 0]), kvh, 5, 17] = value    # sequence 0, position 5
+        out = torch.empty(w.q.shape, dtype=torch.float32, device="cuda")
+        P.pa_get_device_error()
+        P.pa_chunk_attention(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                             w.query_start, w.scale, w.num_kv_heads, w.block_size,
+                             max_query_len=w.max_query_len, max_context_len=w.max_context_len)
+        torch.cuda.synchronize()
+        flags = P.pa_get_device_error()
+        assert flags == (N.PA_DEVERR_RANGE if flagged else 0), hex(flags)
+        ref = oracle.chunk_attention(w.q.cpu(), w.k_cache.cpu(), w.v_cache.cpu(),
+                                     w.block_tables.cpu(), w.context_lens.cpu(),
+                                     w.query_start.cpu(), w.scale, w.num_kv_heads, w.block_size,
+                                     num_threads=oracle.max_threads())
+        got = out.double().cpu().numpy()
+        G = w.num_q_heads // w.num_kv_heads
+        heads = slice(kvh * G, (kvh + 1) * G)
+        n0 = int(w.query_start[1])                # sequence 0's rows
+        hit = np.zeros(got.shape, dtype=bool)
+        hit[:n0, heads, :] = True
+        if flagged:
+            assert not np.isfinite(got[:n0, heads, 17]).any()
+        else:
+            # the rows that weigh 65280: within 2^-11 of it (one f16 rounding per weight)
+            assert np.abs(got[hit] - ref[hit]).max() <= 2.0 ** -11 * value
+        assert np.abs(got[~hit] - ref[~hit]).max() <= ATOL
