@@ -52,9 +52,10 @@ struct ChunkVariant {
 // TK: cache element type (T, or __nv_fp8_e4m3 for a quantised cache).
 template <typename T, int D, int BS, int NH, typename TK = T>
 struct ChunkRowsVariant {
-    static constexpr int kStages = MmaStages<TK, D, BS>::value;
-    using Sm = MmaSmem<TK, D, BS, kStages>;
-    static constexpr auto kernel() { return decode_mma_kernel<T, TK, D, BS, NH, kStages, true>; }
+    static constexpr int kBPT = mma_blocks_per_tile<TK, D, BS>();
+    static constexpr int kStages = MmaStages<TK, D, BS * kBPT>::value;
+    using Sm = MmaSmem<TK, D, BS * kBPT, kStages>;
+    static constexpr auto kernel() { return decode_mma_kernel<T, TK, D, BS, NH, kStages, true, kBPT>; }
     static cudaError_t configure()
     {
         return configure_once(reinterpret_cast<const void*>(kernel()), Sm::kAlloc);

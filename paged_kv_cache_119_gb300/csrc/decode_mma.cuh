@@ -200,12 +200,14 @@ constexpr int mma_min_blocks() { return (sizeof(TK) == 1 && BS == 32) ? 3 : 4; }
 // (chunk token, query head) rows of one kv head -- several new query tokens of a
 // sequence attended causally, each row masked at its own position (speculative
 // verification, short chunks) -- instead of NH query heads of one token.
-template <typename T, typename TK, int D, int BS, int NH, int NSTAGE, bool CH = false>
-__global__ void __launch_bounds__(kDecodeThreads, mma_min_blocks<TK, BS>())
+// BPT: cache blocks per tile (a ring stage); the tile is TB = BS * BPT tokens.
+template <typename T, typename TK, int D, int BS, int NH, int NSTAGE, bool CH = false, int BPT = 1>
+__global__ void __launch_bounds__(kDecodeThreads, mma_min_blocks<TK, BS * BPT>())
     decode_mma_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv)
 {
-    using Sm = MmaSmem<TK, D, BS, NSTAGE>;
+    constexpr int TB = BS * BPT;      // tokens per tile
+    using Sm = MmaSmem<TK, D, TB, NSTAGE>;
     constexpr bool kFp8 = Sm::kFp8;
     // tensor-core operand type: the query type for 16-bit caches; f16 for E4M3 caches
     // (an E4M3 code converts to f16 exactly in one instruction per pair)
@@ -213,7 +215,8 @@ __global__ void __launch_bounds__(kDecodeThreads, mma_min_blocks<TK, BS>())
     constexpr bool kDirect = Sm::kDirect;
     constexpr int NCW = kDecodeConsumerWarps;
     constexpr int KS = D / 16;        // k-steps of the score product / m-blocks of P.V
-    constexpr int MB = BS / 16;       // 16-token row blocks per tile
+    constexpr int MB = TB / 16;       // 16-token row blocks per tile
+    static_assert(BPT == 1 || (BPT == 2 && Sm::kDirect), "two blocks per tile: direct E4M3 tiles");
     static_assert(NH == 1 || NH == 2 || NH == 4 || NH == 8, "1, 2, 4 or 8 query heads per CTA");
     static_assert(NSTAGE % NCW == 0, "each ring stage must belong to one consumer warp");
     static_assert(BS % 16 == 0 && D % 64 == 0, "block_size 16/32, head_dim 64/128");
@@ -280,8 +283,9 @@ __global__ void __launch_bounds__(kDecodeThreads, mma_min_blocks<TK, BS>())
             return;
         t1 = min(t_end, t0 + p.partition_tokens);
     }
-    const int jb = t0 / BS;
-    const int ntiles = (t1 > t0) ? (t1 + BS - 1) / BS - jb : 0;
+    const int jb = t0 / BS;                       // first cache block (partitions start on one)
+    const int nblk = (t1 > t0) ? (t1 + BS - 1) / BS - jb : 0;
+    const int ntiles = (nblk + BPT - 1) / BPT;    // tile it: blocks jb + BPT it .. + BPT - 1
 
     if (threadIdx.x == 0) {
 #pragma unroll
@@ -302,16 +306,22 @@ __global__ void __launch_bounds__(kDecodeThreads, mma_min_blocks<TK, BS>())
         // ------------------------------------------------------------------ producer
         const int32_t* bt_row = p.block_tables + (int64_t)seq * p.bt_stride + jb;
         const uint64_t policy = l2_evict_first_policy();
-        int next = (lane < ntiles) ? __ldg(bt_row + lane) : 0;
+        int next = (lane < nblk) ? __ldg(bt_row + lane) : 0;
         bool aborted = false;
-        for (int base = 0; base < ntiles && !aborted; base += 32) {
+        // block-table entries 32 at a time (BPT divides 32, so no tile straddles two
+        // batches), the next 32 in flight while the current ones are used
+        for (int base = 0; base < nblk && !aborted; base += 32) {
             const int cur = next;
-            if (base + 32 + lane < ntiles)
+            if (base + 32 + lane < nblk)
                 next = __ldg(bt_row + base + 32 + lane);
-            const int cnt = min(32, ntiles - base);
-            for (int i = 0; i < cnt; ++i) {
-                const int pbn = __shfl_sync(kFullMask, cur, i);
-                const int it = base + i;
+            const int cnt = min(32, nblk - base);
+            for (int i = 0; i < cnt; i += BPT) {
+                int pbn[BPT];
+#pragma unroll
+                for (int b = 0; b < BPT; ++b)
+                    pbn[b] = __shfl_sync(kFullMask, cur, i + b);   // i + b <= 31
+                const int nb = min(BPT, cnt - i);                  // blocks of the tile in range
+                const int it = (base + i) / BPT;
                 const int stage = it % NSTAGE;
                 int ok = 1;
                 if (lane == 0) {
@@ -320,37 +330,51 @@ __global__ void __launch_bounds__(kDecodeThreads, mma_min_blocks<TK, BS>())
                         ok = 0;
                     }
                     if (ok) {
-                        const bool valid = pbn >= 0 && (int64_t)pbn < p.num_blocks;
-                        stage_ok[stage] = valid ? 1 : 0;
-                        if (valid) {
-                            unsigned char* dst = smem + Sm::kRingOffset + stage * Sm::kStageBytes;
-                            mbar_arrive_expect_tx(&full[stage], Sm::kStageBytes);
-                            if constexpr (kDirect) {
-                                const int z = pbn * p.num_kv_heads + kvh;
-                                tma_load_3d(dst, &tk, 0, 0, z, &full[stage], policy);
-                                tma_load_3d(dst + Sm::kFp8TileBytes, &tv, 0, 0, z, &full[stage],
-                                            policy);
-                            } else if constexpr (kFp8) {
-                                const int64_t off =
-                                    ((int64_t)pbn * p.num_kv_heads + kvh) * Sm::kFp8TileBytes;
-                                bulk_g2s(dst, reinterpret_cast<const unsigned char*>(p.k_cache) + off,
-                                         Sm::kFp8TileBytes, &full[stage], policy);
-                                bulk_g2s(dst + Sm::kFp8TileBytes,
-                                         reinterpret_cast<const unsigned char*>(p.v_cache) + off,
-                                         Sm::kFp8TileBytes, &full[stage], policy);
-                            } else {
-                                const int z = pbn * p.num_kv_heads + kvh;   // < 2^31 (checked on the host)
+                        bool all_valid = true;
+                        uint32_t tx = 0;
 #pragma unroll
-                                for (int h = 0; h < D / 64; ++h) {
-                                    tma_load_3d(dst + h * Sm::kHalfBytes, &tk, 64 * h, 0, z,
-                                                &full[stage], policy);
-                                    tma_load_3d(dst + Sm::kTileBytes + h * Sm::kHalfBytes, &tv, 64 * h,
-                                                0, z, &full[stage], policy);
+                        for (int b = 0; b < BPT; ++b) {
+                            const bool valid = b < nb && pbn[b] >= 0 && (int64_t)pbn[b] < p.num_blocks;
+                            all_valid = all_valid && (b >= nb || valid);
+                            tx += valid ? 2u * (kFp8 ? BS * D : BS * D * 2) : 0u;
+                        }
+                        stage_ok[stage] = all_valid ? 1 : 0;
+                        if (!all_valid)
+                            atomicOr(p.err, PA_DEVERR_BLOCK_ID);
+                        if (tx == 0) {
+                            mbar_arrive(&full[stage]);
+                        } else {
+                            unsigned char* dst = smem + Sm::kRingOffset + stage * Sm::kStageBytes;
+                            mbar_arrive_expect_tx(&full[stage], tx);
+#pragma unroll
+                            for (int b = 0; b < BPT; ++b) {
+                                if (b >= nb || pbn[b] < 0 || (int64_t)pbn[b] >= p.num_blocks)
+                                    continue;
+                                unsigned char* bdst = dst + b * (BS * 128);   // rows of block b
+                                if constexpr (kDirect) {
+                                    const int z = pbn[b] * p.num_kv_heads + kvh;
+                                    tma_load_3d(bdst, &tk, 0, 0, z, &full[stage], policy);
+                                    tma_load_3d(bdst + Sm::kFp8TileBytes, &tv, 0, 0, z, &full[stage],
+                                                policy);
+                                } else if constexpr (kFp8) {
+                                    const int64_t off =
+                                        ((int64_t)pbn[b] * p.num_kv_heads + kvh) * Sm::kFp8TileBytes;
+                                    bulk_g2s(dst, reinterpret_cast<const unsigned char*>(p.k_cache) + off,
+                                             Sm::kFp8TileBytes, &full[stage], policy);
+                                    bulk_g2s(dst + Sm::kFp8TileBytes,
+                                             reinterpret_cast<const unsigned char*>(p.v_cache) + off,
+                                             Sm::kFp8TileBytes, &full[stage], policy);
+                                } else {
+                                    const int z = pbn[b] * p.num_kv_heads + kvh;   // < 2^31 (checked on the host)
+#pragma unroll
+                                    for (int h = 0; h < D / 64; ++h) {
+                                        tma_load_3d(bdst + h * Sm::kHalfBytes, &tk, 64 * h, 0, z,
+                                                    &full[stage], policy);
+                                        tma_load_3d(bdst + Sm::kTileBytes + h * Sm::kHalfBytes, &tv,
+                                                    64 * h, 0, z, &full[stage], policy);
+                                    }
                                 }
                             }
-                        } else {
-                            atomicOr(p.err, PA_DEVERR_BLOCK_ID);
-                            mbar_arrive(&full[stage]);
                         }
                     }
                 }
@@ -466,8 +490,8 @@ __global__ void __launch_bounds__(kDecodeThreads, mma_min_blocks<TK, BS>())
             unsigned char* stg = smem + warp * 2 * Sm::kTileBytes;
             const unsigned char* raw = smem + Sm::kRingOffset + stage * Sm::kStageBytes;
             __syncwarp();                      // the previous tile's ldmatrix reads are done
-            convert_e4m3_tile<TM, D, BS>(raw, stg, lane);
-            convert_e4m3_tile<TM, D, BS>(raw + Sm::kFp8TileBytes, stg + Sm::kTileBytes, lane);
+            convert_e4m3_tile<TM, D, TB>(raw, stg, lane);
+            convert_e4m3_tile<TM, D, TB>(raw + Sm::kFp8TileBytes, stg + Sm::kTileBytes, lane);
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&empty[stage]);
@@ -477,7 +501,7 @@ __global__ void __launch_bounds__(kDecodeThreads, mma_min_blocks<TK, BS>())
             kbase = smem_addr(smem + stage * Sm::kStageBytes);
             vbase = kbase + Sm::kTileBytes;
         }
-        const int nvalid = min(BS, t1 - (jb + it) * BS);
+        const int nvalid = min(TB, t1 - (jb * BS + it * TB));
 
 #pragma unroll
         for (int mb = 0; mb < MB; ++mb) {
@@ -518,7 +542,7 @@ __global__ void __launch_bounds__(kDecodeThreads, mma_min_blocks<TK, BS>())
             x[3] = tok_b < nvalid ? s[3] * sl2 : -INFINITY;
             if constexpr (CH) {
                 // causal within the chunk: token t is visible to a row at position >= t
-                const int abs_a = (jb + it) * BS + tok_a, abs_b = abs_a + 8;
+                const int abs_a = jb * BS + it * TB + tok_a, abs_b = abs_a + 8;
                 x[0] = abs_a <= lim[0] ? x[0] : -INFINITY;
                 x[1] = abs_a <= lim[1] ? x[1] : -INFINITY;
                 x[2] = abs_b <= lim[0] ? x[2] : -INFINITY;
@@ -705,16 +729,24 @@ __global__ void __launch_bounds__(kDecodeThreads, mma_min_blocks<TK, BS>())
 // resident CTAs per SM beat a deeper ring: measured on GB300, 75 vs 95 us for the
 // shared-prefix decode and 175 vs 194 us for the 8 x 32768-token decode), two for
 // E4M3 caches, whose stages are half the size.
-template <typename TK, int D, int BS>
+template <typename TK, int D, int TB>
 struct MmaStages {
     static constexpr int value = kDecodeConsumerWarps * (sizeof(TK) == 1 ? 2 : 1);
 };
 
+// Cache blocks per tile: two for E4M3 tiles read directly at block size 16, so that a
+// tile (an 8 KB stage, 32 tokens) spreads each consumer's per-tile softmax and
+// hand-over work over as many bytes as at block size 32 (one block of 16 tokens is
+// 4 KB of K + V).
+template <typename TK, int D, int BS>
+constexpr int mma_blocks_per_tile() { return (sizeof(TK) == 1 && D == 128 && BS == 16) ? 2 : 1; }
+
 template <typename T, typename TK, int D, int BS, int NH>
 struct MmaVariant {
-    static constexpr int kStages = MmaStages<TK, D, BS>::value;
-    using Sm = MmaSmem<TK, D, BS, kStages>;
-    static constexpr auto kernel() { return decode_mma_kernel<T, TK, D, BS, NH, kStages>; }
+    static constexpr int kBPT = mma_blocks_per_tile<TK, D, BS>();
+    static constexpr int kStages = MmaStages<TK, D, BS * kBPT>::value;
+    using Sm = MmaSmem<TK, D, BS * kBPT, kStages>;
+    static constexpr auto kernel() { return decode_mma_kernel<T, TK, D, BS, NH, kStages, false, kBPT>; }
     static cudaError_t configure()
     {
         return configure_once(reinterpret_cast<const void*>(kernel()), Sm::kAlloc);
