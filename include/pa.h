@@ -161,7 +161,7 @@ int pa_decode(void* out, pa_dtype out_dtype, const void* q, const void* k_cache,
  * PA_NOALLOC_SCRATCH_BYTES (pa_decode_workspace_bytes gives the need).
  * Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
  * The first call on each device looks up the array's device address (with that
- * device current); make that first call before any stream capture.
+ * device current).
  * All calls share the one array, so calls that overlap on the GPU (say, on two
  * streams) race and corrupt each other's results; serialise them.  The array
  * keeps the last call's contents; nothing in it needs to start at zero, because
