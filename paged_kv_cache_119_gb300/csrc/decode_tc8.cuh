@@ -585,12 +585,16 @@ __global__ void __launch_bounds__(kTc8Threads, 3)
                     for (int k = 0; k < kTc8Terms; ++k)
                         pt[r + 1][k] = tb2[k];
             }
+            // byte tl of swizzled row n of Pt: n * 128 + (tl ^ ((n & 7) << 4)) for tl < 128,
+            // the same place as sw128_byte(n, tl)
             unsigned char* pbuf = smem + Sm::kPOff + b * N * 128;
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
-                for (int k = 0; k < kTc8Terms; ++k)
-                    pbuf[sw128_byte(kTc8Terms * r + k, tl)] = (unsigned char)pt[r][k];
+                for (int k = 0; k < kTc8Terms; ++k) {
+                    const int n = kTc8Terms * r + k;
+                    pbuf[n * 128 + (tl ^ ((n & 7) << 4))] = (unsigned char)pt[r][k];
+                }
             if (tb + kTc8Tok > t1) {
                 // last tile: V rows of tokens past the range (unused slot, missing block,
                 // stale tile) become 0, once the tile's V is in (its slot is not reused
