@@ -319,7 +319,7 @@ def test_fp8_verify4_llama13b_shape():
     run_and_compare_fp8(w)
 
 
-@pytest.mark.parametrize("Hq,Hkv,nmax", [(8, 8, 4), (16, 4, 8), (40, 8, 3), (64, 8, 40)])
+@pytest.mark.parametrize("Hq,Hkv,nmax", [(8, 8, 4), (16, 4, 8), (40, 8, 3), (64, 8, 4), (64, 8, 40)])
 @pytest.mark.parametrize("D,B", [(128, 16), (64, 32)])
 @pytest.mark.parametrize("qdtype", [torch.bfloat16, torch.float16])
 def test_fp8_chunks(Hq, Hkv, nmax, D, B, qdtype):

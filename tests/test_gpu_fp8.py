@@ -138,3 +138,37 @@ def test_fp8_config_full_size(name):
     times (automatic split), every output against the oracle."""
     w = workloads.to_fp8(workloads.make(name, device="cuda"))
     step_and_compare(w)
+
+
+@pytest.mark.parametrize("part", [-1, 64])
+def test_fp8_bad_block_inside_a_two_block_tile(part):
+    """GQA 8 at head_dim 128 and block size 16 reads two cache blocks per tile.  An
+    invalid id in either block of a tile (the second block of tile 1 of sequence 1, the
+    first block of tile 2 of sequence 2) sets the block-id bit and makes exactly that
+    sequence's rows NaN, in one pass and split into 64-token partitions; sequence 0,
+    whose tiles are valid (its last tile holds one block), still matches the oracle."""
+    rng = np.random.default_rng(71)
+    lens = [37, 100, 250]                      # 3, 7 and 16 blocks of 16
+    w = workloads.to_fp8(workloads._assemble("bad_ids", rng, "cuda", lens=lens, Hq=64, Hkv=8,
+                                             D=128, B=16, dtype=torch.bfloat16, std=1.0))
+    ks, vs = w.meta["k_scale"], w.meta["v_scale"]
+    assert P.pa_decode_kernel_name(w.k_cache.dtype, 64, 8, 128) == "decode_mma_kernel"
+    # the step's new tokens first (their slots hold the pool's NaN fill until written)
+    P.pa_reshape_and_cache_fp8(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping, ks, vs)
+    torch.cuda.synchronize()
+    ref = oracle.paged_attention(w.q[:1].cpu(), u8(w.k_cache.cpu()), u8(w.v_cache.cpu()),
+                                 w.block_tables[:1].cpu(), w.context_lens[:1].cpu(), w.scale,
+                                 w.num_kv_heads, w.block_size, num_threads=oracle.max_threads(),
+                                 k_scale=ks.cpu(), v_scale=vs.cpu())
+    w.block_tables[1, 3] = w.k_cache.shape[0] + 5      # outside the pool
+    w.block_tables[2, 4] = -7
+    out = torch.empty(w.q.shape, dtype=torch.float32, device="cuda")
+    P.pa_decode_fp8(out, w.q, w.k_cache, w.v_cache, ks, vs, w.block_tables, w.context_lens,
+                    w.scale, w.num_kv_heads, w.block_size, max_context_len=w.max_context_len,
+                    partition_size=part)
+    torch.cuda.synchronize()
+    assert P.pa_get_device_error() == 1
+    got = out.cpu()
+    assert torch.isnan(got[1]).all() and torch.isnan(got[2]).all()
+    err = np.abs(got[:1].double().numpy() - ref).max()
+    assert err <= ATOL, f"max abs error {err:.3e}"
