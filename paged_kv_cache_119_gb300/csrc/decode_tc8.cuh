@@ -605,12 +605,12 @@ __global__ void __launch_bounds__(kTc8Threads, 3)
                     poisoned = aborted = true;
                     break;
                 }
-                if (pos >= t1) {
-                    uint4* vrow = reinterpret_cast<uint4*>(smem + st * Sm::kStage + Sm::kTile + tl * 128);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        vrow[c] = make_uint4(0u, 0u, 0u, 0u);
-                }
+                // rows nv .. 127 are one contiguous span: the 128 threads zero it together,
+                // consecutive 16-byte stores (no bank conflicts)
+                const int nv = t1 - tb;                  // 1 .. 127 rows of the range
+                uint4* vz = reinterpret_cast<uint4*>(smem + st * Sm::kStage + Sm::kTile + nv * 128);
+                for (int j = tl; j < (kTc8Tok - nv) * 8; j += kTc8Tok)
+                    vz[j] = make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
             tc_fence_before();
