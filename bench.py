@@ -109,6 +109,9 @@ def parse_args(argv=None):
     ap.add_argument("--config-warmup", type=int, default=3)
     ap.add_argument("--eager", action="store_true",
                     help="time eager steps instead of replays of the captured step graph")
+    ap.add_argument("--run-probe", action="store_true",
+                    help="print the read rate of randomly ordered fixed-size runs (1-16 KB, the "
+                         "granularity of one kv head's block) instead of a bench line")
     ap.add_argument("--no-read-probe", action="store_true",
                     help="skip the read-only bandwidth probe reported beside the copy peak")
     return ap.parse_args(argv)
@@ -159,12 +162,13 @@ def load_tensor_peak():
 
 
 def kernel_hash() -> str:
-    """Hash of every kernel source (csrc/*.cuh, *.cu, *.h): a recorded traffic row
-    counts only for the exact sources it was captured from."""
+    """Hash of every kernel source (csrc/*.cuh, *.cu, *.h) but the bandwidth probe, which
+    no attention kernel includes: a recorded traffic row counts only for the exact
+    sources it was captured from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_119_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cuh", ".cu", ".h")):
+        if name.endswith((".cuh", ".cu", ".h")) and name != "probe.cu":
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
@@ -319,6 +323,39 @@ def read_probe_gbs(pa, dev, nbytes=4 << 30, reps=10) -> float:
     ms = percentiles([b.elapsed_time(e) for b, e in ev])["p50"]
     del buf
     return nbytes / (ms / 1e3) / 1e9
+
+
+def run_probe(dev, nbytes=4 << 30, reps=10) -> dict:
+    """Read rate of a 4 GiB buffer read as fixed-size runs in a seeded random order
+    (pa_stream_read_runs; best of `reps` launches, CUDA events): the ceiling for a paged
+    cache whose blocks of one kv head are runs of block_size x head_dim x element bytes
+    scattered through the pool.  Sequential pa_stream_read beside it."""
+    import paged_kv_cache_119_gb300 as pa
+    from paged_kv_cache_119_gb300 import build as pa_build
+    pa_build.build()
+    buf = torch.ones(nbytes // 4, dtype=torch.int32, device=dev)
+    sink = torch.zeros(2, dtype=torch.int32, device=dev)
+    gen = torch.Generator().manual_seed(119)
+    out = {"metric": "random-run read GB/s", "unit": "GB/s", "bytes": nbytes,
+           "order": "seeded random permutation of all runs; CTAs take consecutive entries"}
+    for run in (1024, 2048, 4096, 8192, 16384):
+        order = torch.randperm(nbytes // run, generator=gen, dtype=torch.int32).to(dev)
+        for _ in range(3):
+            pa.pa_stream_read_runs(buf, run, order, sink)
+        best = float("inf")
+        for _ in range(reps):
+            b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b.record()
+            pa.pa_stream_read_runs(buf, run, order, sink)
+            e.record()
+            torch.cuda.synchronize()
+            best = min(best, b.elapsed_time(e))
+        out[f"run_{run // 1024}KB_gbs"] = round(nbytes / (best / 1e3) / 1e9, 1)
+        del order
+    if int(sink[1].item()) != 0:
+        raise RuntimeError("run probe: entries outside the buffer")
+    out["sequential_gbs"] = round(read_probe_gbs(pa, dev, nbytes, reps), 1)
+    return out
 
 
 def step_ops(pa, w):
@@ -1134,8 +1171,12 @@ def main(argv=None):
     rank, world, local = dist_env()
     if args.gpus != world and world > 1:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
-    line = run_reference(args, rank, world) if args.impl == "reference" else \
-        run_ours(args, rank, world, local)
+    if args.run_probe:
+        torch.cuda.set_device(local)
+        line = run_probe(torch.device("cuda", local)) if rank == 0 else None
+    else:
+        line = run_reference(args, rank, world) if args.impl == "reference" else \
+            run_ours(args, rank, world, local)
     if line is not None:
         print(json.dumps(line), flush=True)
 

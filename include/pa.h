@@ -419,6 +419,18 @@ int pa_test_arm_wait_timeout(int32_t cta_index, uint32_t wait_limit_us);
 int pa_stream_read(const void* buf, size_t bytes, uint32_t* sink, void* stream);
 
 /*
+ * pa_stream_read_runs: measurement helper, the read ceiling of scattered runs.  buf
+ * (DEVICE, 16-byte aligned) is divided into runs of run_bytes (1024, 2048, 4096, 8192
+ * or 16384); the call reads run order[i] for every i < num_runs (order: DEVICE int32,
+ * values in [0, bytes / run_bytes)), CTAs taking consecutive entries as a decode CTA
+ * walks a block table.  sink: DEVICE uint32[2]; sink[0] receives a checksum, sink[1]
+ * counts entries outside the range (skipped).  Asynchronous on stream.  Returns
+ * PA_ERR_INVALID for a null or misaligned pointer, num_runs <= 0 or another run size.
+ */
+int pa_stream_read_runs(const void* buf, size_t bytes, uint32_t run_bytes, const int32_t* order,
+                        int64_t num_runs, uint32_t* sink, void* stream);
+
+/*
  * Reads and clears the calling device's error word (PA_DEVERR_* bits).
  * Synchronises with `stream` to do so.  flags: host pointer.
  */

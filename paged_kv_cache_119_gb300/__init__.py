@@ -22,7 +22,7 @@ _API = ("pa_decode", "pa_decode_noalloc", "pa_decode_fp8", "pa_reshape_and_cache
         "pa_chunk_attention", "pa_chunk_workspace_bytes", "pa_decode_partition_tokens",
         "pa_decode_orders_sequences",
         "pa_chunk_partition_tokens", "pa_swap_blocks", "pa_chunk_attention_fp8",
-        "pa_decode_kernel_name", "pa_chunk_kernel_name", "pa_stream_read",
+        "pa_decode_kernel_name", "pa_chunk_kernel_name", "pa_stream_read", "pa_stream_read_runs",
         "pa_get_device_error", "pa_version")
 
 __all__ = list(_API) + ["workloads", "build"]

@@ -56,6 +56,7 @@ SIGNATURES = {
     "pa_decode_kernel_name": (ctypes.c_char_p, [ctypes.c_int, _i32, _i32, _i32]),
     "pa_chunk_kernel_name": (ctypes.c_char_p, [ctypes.c_int, _i32, _i32, _i32, _i32]),
     "pa_stream_read": (ctypes.c_int, [_vp, _sz, _vp, _vp]),
+    "pa_stream_read_runs": (ctypes.c_int, [_vp, _sz, ctypes.c_uint32, _vp, ctypes.c_int64, _vp, _vp]),
     "pa_test_arm_wait_timeout": (ctypes.c_int, [_i32, ctypes.c_uint32]),
     "pa_get_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), _vp]),
     "pa_bm_create": (_vp, [_i32, _i32, ctypes.POINTER(_i32)]),

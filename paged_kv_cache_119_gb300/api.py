@@ -491,6 +491,23 @@ def pa_stream_read(buf: torch.Tensor, sink: torch.Tensor, stream=None) -> None:
                                                        sink.data_ptr(), _stream(stream)))
 
 
+def pa_stream_read_runs(buf: torch.Tensor, run_bytes: int, order: torch.Tensor,
+                        sink: torch.Tensor, stream=None) -> None:
+    """Measurement helper: read run order[i] (run_bytes each) of buf for every i, CTAs
+    taking consecutive entries (a block-table walk); sink (int32 CUDA, two elements)
+    gets a checksum in [0] and the count of out-of-range entries in [1]."""
+    for name, t in (("buf", buf), ("order", order), ("sink", sink)):
+        _cuda(name, t)
+    if order.dtype != torch.int32 or not order.is_contiguous():
+        raise TypeError("order must be a contiguous int32 CUDA tensor")
+    if sink.dtype != torch.int32 or sink.numel() < 2:
+        raise TypeError("sink must be an int32 CUDA tensor of two elements")
+    N.check("pa_stream_read_runs",
+            N.load().pa_stream_read_runs(buf.data_ptr(), buf.numel() * buf.element_size(),
+                                         int(run_bytes), order.data_ptr(), order.numel(),
+                                         sink.data_ptr(), _stream(stream)))
+
+
 def pa_get_device_error(stream=None) -> int:
     """Read and clear the device error word (PA_DEVERR_* bits).  Synchronises."""
     flags = ctypes.c_uint32(0)
